@@ -1,0 +1,204 @@
+"""Pins for the oracle's decode, LSE merge and prefill (CPU only).
+
+The oracle is tied to torch's scaled_dot_product_attention in float64 on
+inputs where NVFP4 quantisation is lossless, to closed forms, and to
+invariances that a wrong index, sign or operand would break.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import attention, cache, nvfp4
+
+SCALE = 1.0 / math.sqrt(192.0)
+
+
+def _on_grid_latent(rng, T, gs):
+    """bf16-representable latent rows that NVFP4 reproduces exactly."""
+    sb = rng.integers(0x20, 0x48, (T, 32))
+    codes = rng.integers(0, 16, (T, 32, 16))
+    codes[..., 3] = 7 | (rng.integers(0, 2, (T, 32)) << 3)  # |.| = 6 in every block
+    x = nvfp4.e2m1_decode(codes) * nvfp4.e4m3_decode(sb)[..., None] * float(gs)
+    return x.reshape(T, 512).astype(np.float32)
+
+
+def _bf16(rng, shape):
+    x = rng.standard_normal(shape).astype(np.float32)
+    return (x.view(np.uint32) & 0xFFFF0000).view(np.float32)
+
+
+def _sdpa(q, k, v, scale, causal=False):
+    return F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(k),
+                                          torch.from_numpy(v), scale=scale,
+                                          is_causal=causal).numpy()
+
+
+@pytest.mark.parametrize("rb", [432, 368])
+def test_decode_lossless_matches_sdpa(rb):
+    rng = np.random.default_rng(10)
+    B, H, P = 2, 4, 64
+    lens = [64, 100]
+    gs = np.float32(2.0 ** -3)
+    n_pages = 4
+    perm = np.array([3, 0, 2, 1])
+    table = np.array([[perm[0], 0], [perm[1], perm[2]]])
+    slots = attention.decode_slots_paged(table, lens, P)
+    kv = _on_grid_latent(rng, sum(lens), gs)
+    pe = _bf16(rng, (sum(lens), 64))
+    if rb == 368:  # fp8 rope must be on the e4m3 grid to be lossless
+        pe = nvfp4.e4m3_decode(nvfp4.e4m3_encode(pe.astype(np.float64))).astype(np.float32)
+    c = np.zeros((n_pages * P, rb), dtype=np.uint8)
+    cache.write_cache(c, kv, pe, np.concatenate(slots), gs, rb)
+    q = _bf16(rng, (B, H, 576)).astype(np.float64)
+    out, lse = attention.decode(q, c, rb, gs, SCALE, slots)
+    pos = 0
+    for b, L in enumerate(lens):
+        k = np.concatenate([kv[pos:pos + L], pe[pos:pos + L]], axis=1).astype(np.float64)
+        v = kv[pos:pos + L].astype(np.float64)
+        ref = _sdpa(q[b][:, None, :], np.broadcast_to(k, (H, L, 576)).copy(),
+                    np.broadcast_to(v, (H, L, 512)).copy(), SCALE)[:, 0]
+        np.testing.assert_allclose(out[b], ref, rtol=0, atol=1e-12)
+        s = SCALE * q[b] @ k.T
+        np.testing.assert_allclose(lse[b], np.log(np.exp(s).sum(1)), rtol=1e-13)
+        pos += L
+
+
+def test_lse_is_natural_log():
+    q = np.zeros((1, 576))
+    k = np.zeros((5, 576))
+    v = np.arange(5 * 512, dtype=np.float64).reshape(5, 512)
+    o, lse = attention.attend(q, k, v, 1.0)
+    assert lse[0] == pytest.approx(math.log(5.0), abs=1e-15)
+    np.testing.assert_allclose(o[0], v.mean(0))
+
+
+def test_split_merge_invariance():
+    rng = np.random.default_rng(11)
+    H, N = 8, 300
+    q = rng.standard_normal((H, 576))
+    k = rng.standard_normal((N, 576))
+    v = rng.standard_normal((N, 512))
+    o_full, l_full = attention.attend(q, k, v, SCALE)
+    for cuts in ([0, 100, 300], [0, 1, 64, 65, 299, 300], [0, 150, 150, 300]):
+        parts = [attention.attend(q, k[a:b], v[a:b], SCALE) for a, b in zip(cuts[:-1], cuts[1:])]
+        o, l = attention.lse_merge([p[0] for p in parts], [p[1] for p in parts])
+        np.testing.assert_allclose(o, o_full, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, l_full, rtol=1e-14)
+
+
+def test_merge_all_empty():
+    o, l = attention.lse_merge(np.zeros((2, 3, 4)), np.full((2, 3), -np.inf))
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+def test_paged_addressing_matches_contiguous():
+    rng = np.random.default_rng(12)
+    lens = [130, 64, 1]
+    P = 64
+    pages = [(L + P - 1) // P for L in lens]
+    n_pages = sum(pages)
+    perm = rng.permutation(n_pages)
+    table = np.zeros((3, max(pages)), dtype=np.int64)
+    pos = 0
+    for b, n in enumerate(pages):
+        table[b, :n] = perm[pos:pos + n]
+        pos += n
+    slots = attention.decode_slots_paged(table, lens, P)
+    # token t of sequence b must sit in page table[b][t//64] at row t%64
+    assert slots[0][129] == table[0, 2] * 64 + 1
+    assert slots[2][0] == table[2, 0] * 64
+    allslots = np.concatenate(slots)
+    assert len(np.unique(allslots)) == len(allslots)
+    gs = np.float32(0.01)
+    kv = _bf16(rng, (sum(lens), 512))
+    pe = _bf16(rng, (sum(lens), 64))
+    c = np.zeros((n_pages * P, 432), dtype=np.uint8)
+    cache.write_cache(c, kv, pe, allslots, gs, 432)
+    q = _bf16(rng, (3, 2, 576))
+    out, _ = attention.decode(q, c, 432, gs, SCALE, slots)
+    rec = cache.encode_records(kv, pe, gs, 432)
+    pos = 0
+    for b, L in enumerate(lens):
+        lat, rope = cache.decode_records(rec[pos:pos + L], gs, 432)
+        o, _ = attention.attend(q[b], np.concatenate([lat, rope], 1), lat, SCALE)
+        np.testing.assert_allclose(out[b], o, atol=1e-13)
+        pos += L
+
+
+def test_topk_padding_and_order():
+    rng = np.random.default_rng(13)
+    gs = np.float32(0.005)
+    kv = _bf16(rng, (50, 512))
+    pe = _bf16(rng, (50, 64))
+    c = np.zeros((50, 432), dtype=np.uint8)
+    cache.write_cache(c, kv, pe, np.arange(50), gs, 432)
+    q = _bf16(rng, (3, 4, 576))
+    idx = np.array([[5, 7, 9, -1], [9, 5, 7, -1], [-1, -1, -1, -1]])
+    out, lse = attention.decode(q, c, 432, gs, SCALE, attention.decode_slots_topk(idx))
+    q1 = q.copy()
+    q1[1] = q[0]
+    out1, _ = attention.decode(q1, c, 432, gs, SCALE, attention.decode_slots_topk(idx))
+    np.testing.assert_allclose(out1[1], out[0], atol=1e-14)
+    assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
+
+
+def test_decode_brute_force_vs_unquantised():
+    # tiny case: quantised attention stays within the NVFP4 error of exact
+    # attention on the unquantised latent
+    rng = np.random.default_rng(14)
+    L, H = 8, 2
+    kv = _bf16(rng, (L, 512))
+    pe = _bf16(rng, (L, 64))
+    gs = nvfp4.global_scale(np.abs(kv).max())
+    c = np.zeros((L, 432), dtype=np.uint8)
+    cache.write_cache(c, kv, pe, np.arange(L), gs, 432)
+    q = _bf16(rng, (1, H, 576))
+    out, _ = attention.decode(q, c, 432, gs, SCALE, [np.arange(L)])
+    k = np.concatenate([kv, pe], 1).astype(np.float64)
+    s = SCALE * q[0].astype(np.float64) @ k.T
+    p = np.exp(s - s.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    exact = p @ kv.astype(np.float64)
+    rel = np.linalg.norm(out[0] - exact) / np.linalg.norm(exact)
+    assert rel < 0.2
+    # and the quantised output is not the exact one (quantisation is live)
+    assert rel > 1e-3
+
+
+def test_prefill_matches_causal_sdpa():
+    rng = np.random.default_rng(15)
+    lens = [1, 37, 128, 5]
+    H = 3
+    T = sum(lens)
+    q, k = _bf16(rng, (T, H, 192)), _bf16(rng, (T, H, 192))
+    v = _bf16(rng, (T, H, 128))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, lse = attention.prefill(q, k, v, cu, SCALE)
+    for s in range(len(lens)):
+        a, e = cu[s], cu[s + 1]
+        ref = _sdpa(q[a:e].transpose(1, 0, 2).astype(np.float64),
+                    k[a:e].transpose(1, 0, 2).astype(np.float64),
+                    v[a:e].transpose(1, 0, 2).astype(np.float64), SCALE, causal=True)
+        np.testing.assert_allclose(o[a:e].transpose(1, 0, 2), ref, atol=1e-12)
+    # first row of each sequence attends to itself only: o = v, lse = s_00
+    for s in range(len(lens)):
+        a = cu[s]
+        np.testing.assert_allclose(o[a], v[a], atol=1e-15)
+        np.testing.assert_allclose(lse[:, a], SCALE * np.einsum("hd,hd->h", q[a].astype(np.float64),
+                                                                k[a].astype(np.float64)), rtol=1e-13)
+    rows = [0, 1, 37, 100, T - 1]
+    orow, lrow = attention.prefill_rows(q, k, v, cu, SCALE, rows, head=2)
+    np.testing.assert_allclose(orow, o[rows, 2], atol=1e-14)
+    np.testing.assert_allclose(lrow, lse[2, rows], rtol=1e-14)
+
+
+def test_absorption_identity():
+    # q_nope . (W_UK c) == (q_nope W_UK) . c: the 512-d latent query is exact
+    rng = np.random.default_rng(16)
+    W = rng.standard_normal((128, 512))
+    qn = rng.standard_normal(128)
+    c = rng.standard_normal(512)
+    assert np.isclose(qn @ (W @ c), (qn @ W) @ c, rtol=1e-12)
