@@ -1,0 +1,188 @@
+/*
+ * mla_nvfp4.h -- C ABI of the GB300 (sm_103a) MLA attention library with an
+ * NVFP4 latent cache and NVFP4 fused prefill output.
+ *
+ * NVFP4 here: e2m1 codes packed two per byte (even element in the low
+ * nibble), one e4m3 block scale per 16 elements along the contraction axis,
+ * and an fp32 global scale gs in the dequantisation direction:
+ *     x_hat = e2m1(code) * e4m3(scale) * gs,   gs = amax / (6 * 448).
+ * Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for MLA (vLLM
+ * TRITON_MLA) - #2244", PR description, "Contract notes".
+ *
+ * Conventions for every entry point:
+ *  - All pointers are DEVICE pointers unless stated otherwise.  The caller
+ *    owns every buffer (including decode workspace); the library allocates
+ *    nothing and keeps no state between calls.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *    enqueued asynchronously; the return value covers host-side argument
+ *    checks and the launch only.
+ *  - `error_word` (nullable) is a device uint32 the kernels OR MLA_DEVERR_*
+ *    bits into when they meet out-of-range indices (the access is skipped)
+ *    or an invalid global scale.  The caller clears it; the library never
+ *    does.
+ *  - Return values are mla_status_t codes; nothing is launched when a check
+ *    fails.  The library must run on an sm_103 device (GB300); any other
+ *    device gives MLA_ERR_UNSUPPORTED_DEVICE before any launch.
+ */
+#ifndef MLA_NVFP4_H
+#define MLA_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_NVFP4_ABI_VERSION 1
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,        /* null pointer, bad size, bad mode mix    */
+  MLA_ERR_RECORD_BYTES = 2,       /* record_bytes not 432 or 368             */
+  MLA_ERR_ALIGNMENT = 3,          /* pointer or stride not 16-byte aligned   */
+  MLA_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103            */
+  MLA_ERR_WORKSPACE = 5,          /* decode workspace missing or too small   */
+  MLA_ERR_LAUNCH = 6,             /* CUDA launch or attribute error          */
+} mla_status_t;
+
+/* Bits OR-ed into *error_word by the kernels. */
+#define MLA_DEVERR_BOUNDS 0x1u  /* slot, page or index out of range: skipped */
+#define MLA_DEVERR_TIMEOUT 0x2u /* a bounded pipeline wait gave up           */
+#define MLA_DEVERR_SCALE 0x4u   /* global scale <= 0 or not finite           */
+
+/* Fixed MLA dimensions (DeepSeek-style absorbed MLA). */
+#define MLA_D_LATENT 512   /* kv_c, the NVFP4 latent; also the decode V dim */
+#define MLA_D_ROPE 64      /* k_pe                                          */
+#define MLA_D_QK_DECODE 576
+#define MLA_D_QK_PREFILL 192
+#define MLA_D_V_PREFILL 128
+#define MLA_RECORD_BF16_ROPE 432
+#define MLA_RECORD_FP8_ROPE 368
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_nvfp4_status_string(int status);
+
+/* MLA_NVFP4_ABI_VERSION of the loaded library. */
+int mla_nvfp4_abi_version(void);
+
+/*
+ * Global (outer) scale of a bf16 tensor: *gs = fp32(amax|x| / 2688).
+ * Source: "#2244" PR description, "Contract notes" (amax/(6*448)); the
+ * b12x "nvfp4 MLA KV cache + per-layer outer-scale ... - #33" description
+ * restores this per-layer fp32 scale on read.
+ *   x  : bf16 [n], 16-byte aligned.   n >= 1.
+ *   gs : one fp32, overwritten (cleared and reduced on `stream`).
+ */
+int mla_nvfp4_global_scale(const void* x, int64_t n, float* gs, void* stream);
+
+/*
+ * Quantise-on-write of the MLA latent cache (one record per token).
+ * Source: "#2244", second commit message (the latent is quantised once at
+ * cache-write time and both attention products read those bytes); "#33",
+ * review of api.py (432-byte record = bf16 RoPE, 368-byte = fp8 RoPE, any
+ * other width is an error).
+ *   kv_c         : bf16 [num_tokens, 512], row stride kv_c_stride elements.
+ *   k_pe         : bf16 [num_tokens, 64], row stride k_pe_stride elements.
+ *   slot_mapping : int64 [num_tokens]; -1 skips the token; a slot >= num_slots
+ *                  is skipped and flagged MLA_DEVERR_BOUNDS.
+ *   cache        : uint8 [num_slots, record_bytes], 16-byte aligned.
+ *   record_bytes : 432 or 368.
+ *   global_scale : device fp32 gs.
+ * Record layout: [0,256) codes, [256,288) 32 e4m3 scales, then k_pe as 64
+ * bf16 (432) or 64 e4m3 RNE-saturating (368), then 16 zero bytes.
+ * kv_c, k_pe and both strides (in bytes) must be 16-byte aligned.
+ */
+int mla_nvfp4_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                          int64_t k_pe_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                          uint8_t* cache, int64_t num_slots, int record_bytes,
+                          const float* global_scale, uint32_t* error_word, void* stream);
+
+/*
+ * Bytes of decode workspace needed for (batch, num_heads, num_splits);
+ * num_splits <= 0 selects the library default, which is also what
+ * mla_nvfp4_decode uses when given num_splits <= 0.  Never fails: returns 0
+ * for invalid sizes.
+ */
+size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits);
+
+/*
+ * Absorbed MLA decode over the NVFP4 latent cache, split along the keys and
+ * merged by natural-log LSE.
+ * Source: "#2244", first commit message (split-K absorbed decode over the
+ * paged latent cache, grouped query heads, natural-log LSE) and third commit
+ * message (both products read the write-once latent; V is the latent);
+ * "#33" (sparse top-k decode; bf16 Q staged unquantised, review of
+ * kernel.py).
+ *   q            : bf16 [batch, num_heads, 576] contiguous = [q_nope.W_UK (512),
+ *                  q_pe (64)] per head, 16-byte aligned.
+ *   cache        : uint8 [num_slots, record_bytes] written by
+ *                  mla_nvfp4_cache_write with the same global_scale.
+ *   Paged mode   : page_table int32 [batch, page_table_stride], seq_lens int32
+ *                  [batch]; token t of sequence b is slot
+ *                  page_table[b][t / page_size] * page_size + t % page_size.
+ *                  topk_indices must be NULL.
+ *   Top-k mode   : topk_indices int32 [batch, topk] of global slot ids, -1 =
+ *                  padding; page_table and seq_lens must be NULL.
+ *   out          : bf16 [batch, num_heads, 512].
+ *   lse          : fp32 [batch, num_heads] natural-log LSE of the scaled
+ *                  scores, or NULL.  A sequence with no keys gives out = 0 and
+ *                  lse = -inf.
+ *   workspace    : >= mla_nvfp4_decode_workspace_size(batch, num_heads,
+ *                  num_splits) bytes, 256-byte aligned, contents ignored.
+ * scores = softmax_scale * q . [x_hat (512), k_pe (64)], out = softmax . x_hat.
+ */
+int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cache,
+                     int64_t num_slots, int record_bytes, const int32_t* page_table,
+                     int64_t page_table_stride, int page_size, const int32_t* seq_lens,
+                     const int32_t* topk_indices, int topk, float softmax_scale,
+                     const float* global_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, int num_splits, uint32_t* error_word, void* stream);
+
+/*
+ * Causal varlen MLA prefill whose epilogue writes NVFP4 directly.
+ * Source: "feat: MLA prefill NVFP4 fused output - #8" (PR description:
+ * packed e2m1 output plus the global scale plus the 128x4-swizzled e4m3
+ * block-scale buffer consumed by NVFP4 GEMMs, no standalone quantisation;
+ * the call owns the whole scale buffer, which is why fusion needs a pure
+ * prefill batch); "#2244", first commit (varlen, asymmetric 192/128 dims).
+ *   q, k         : bf16 [total_tokens, num_heads, 192]; v: bf16 [total_tokens,
+ *                  num_heads, 128]; element strides per token and per head
+ *                  given, last dim contiguous; base and strides (in bytes)
+ *                  16-byte aligned.
+ *   cu_seqlens   : int32 [num_seqs + 1] on the device, cu_seqlens[0] = 0,
+ *                  non-decreasing, cu_seqlens[num_seqs] = total_tokens;
+ *                  max_seqlen (host) >= every sequence length.
+ *   out_codes    : uint8 [total_tokens, num_heads * 64]: row m, byte
+ *                  h*64 + d/2 holds features d, d+1 of head h.
+ *   out_scales   : uint8 [roundup(T,128) * roundup(num_heads*8,4)]: e4m3 scale
+ *                  of (row m, column k = h*8 + d/16) at
+ *                  ((m/128)*(Kp/4) + k/4)*512 + (m%32)*16 + ((m%128)/32)*4 + k%4,
+ *                  Kp = roundup(num_heads*8, 4); padding rows are zeroed.
+ *   lse          : fp32 [num_heads, total_tokens] or NULL.
+ * Query i of a sequence attends to keys 0..i of the same sequence; the
+ * normalised fp32 output rows are quantised with blocks of 16 along d.
+ */
+int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
+                                int64_t q_stride_t, int64_t q_stride_h, int64_t k_stride_t,
+                                int64_t k_stride_h, int64_t v_stride_t, int64_t v_stride_h,
+                                const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
+                                int max_seqlen, int num_heads, float softmax_scale,
+                                const float* global_scale, uint8_t* out_codes,
+                                uint8_t* out_scales, float* lse, uint32_t* error_word,
+                                void* stream);
+
+/*
+ * The prefill epilogue's quantiser on its own (test hook): fp32 [M, N]
+ * row-major, N a multiple of 16, into packed codes uint8 [M, N/2] and the
+ * swizzled scale buffer of a [M, N/16] scale matrix (layout as for
+ * out_scales above, padding zeroed).  Same device code as the epilogue.
+ */
+int mla_nvfp4_quantize_rows(const float* x, int64_t M, int64_t N, const float* global_scale,
+                            uint8_t* codes, uint8_t* scales, uint32_t* error_word, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_NVFP4_H */

@@ -1,0 +1,247 @@
+"""MLA attention with an NVFP4 latent cache and NVFP4 fused prefill output,
+for one GB300 (sm_103a).
+
+This package is a thin ctypes binding over libmla_nvfp4.so (C ABI declared
+in include/mla_nvfp4.h).  The Python functions carry the same names as the C
+entry points and only marshal arguments: every step of the computation runs
+in the library's CUDA kernels.  PyTorch supplies device memory and the
+current stream.  There is no CPU fallback: if the library is missing or the
+device is not sm_103, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "load_library", "MLAError", "mla_nvfp4_global_scale", "mla_nvfp4_cache_write",
+    "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode", "mla_nvfp4_prefill_fused_out",
+    "mla_nvfp4_quantize_rows", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
+    "LAUNCHES_PER_CALL",
+]
+
+RECORD_BF16_ROPE = 432
+RECORD_FP8_ROPE = 368
+DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE = 0x1, 0x2, 0x4
+
+# Kernels each entry point launches (for launch accounting in the benchmark).
+LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 2, "prefill": 1, "global_scale": 2}
+
+_LIB = None
+
+_c_i64, _c_int, _c_vp, _c_f = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+_SIGS = {
+    "mla_nvfp4_status_string": (ctypes.c_char_p, [_c_int]),
+    "mla_nvfp4_abi_version": (_c_int, []),
+    "mla_nvfp4_global_scale": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp]),
+    "mla_nvfp4_cache_write": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64,
+                                       _c_int, _c_vp, _c_vp, _c_vp]),
+    "mla_nvfp4_decode_workspace_size": (ctypes.c_size_t, [_c_int, _c_int, _c_int]),
+    "mla_nvfp4_decode": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64, _c_int,
+                                  _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp, _c_vp,
+                                  ctypes.c_size_t, _c_int, _c_vp, _c_vp]),
+    "mla_nvfp4_prefill_fused_out": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
+                                             _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_int, _c_int,
+                                             _c_f, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_nvfp4_quantize_rows": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+}
+
+
+def abi_symbols():
+    """Entry points the header declares (and the library must export)."""
+    return list(_SIGS)
+
+
+class MLAError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def load_library(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the in-tree libmla_nvfp4.so."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    lib_path = path or _build.LIB
+    if path is None and build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(lib_path):
+        raise RuntimeError(f"libmla_nvfp4.so not found at {lib_path}; run the package build")
+    lib = ctypes.CDLL(lib_path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().mla_nvfp4_status_string(status).decode()
+
+
+def _check(fn, status):
+    if status != 0:
+        raise MLAError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t, name, dtype, device=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def mla_nvfp4_global_scale(x: torch.Tensor, gs: torch.Tensor | None = None) -> torch.Tensor:
+    """gs = amax|x| / (6 * 448) as a device fp32 scalar tensor (shape [1])."""
+    _need(x, "x", torch.bfloat16)
+    if gs is None:
+        gs = torch.empty(1, dtype=torch.float32, device=x.device)
+    _need(gs, "gs", torch.float32, x.device)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    with torch.cuda.device(x.device):
+        _check("mla_nvfp4_global_scale",
+               load_library().mla_nvfp4_global_scale(_ptr(x), x.numel(), _ptr(gs), _stream(x)))
+    return gs
+
+
+def mla_nvfp4_cache_write(kv_c, k_pe, slot_mapping, cache, global_scale, error_word=None):
+    """Quantise kv_c [T,512] / k_pe [T,64] (bf16) into cache [num_slots, 432|368] (uint8)."""
+    dev = cache.device
+    _need(kv_c, "kv_c", torch.bfloat16, dev)
+    _need(k_pe, "k_pe", torch.bfloat16, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    _need(cache, "cache", torch.uint8, dev)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    if cache.dim() != 2 or kv_c.dim() != 2 or k_pe.dim() != 2:
+        raise ValueError("kv_c, k_pe and cache must be 2-D")
+    if kv_c.stride(1) != 1 or k_pe.stride(1) != 1 or not cache.is_contiguous() or not slot_mapping.is_contiguous():
+        raise ValueError("last dimensions must be contiguous")
+    T = kv_c.shape[0]
+    if k_pe.shape[0] != T or slot_mapping.numel() != T or kv_c.shape[1] != 512 or k_pe.shape[1] != 64:
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_cache_write", load_library().mla_nvfp4_cache_write(
+            _ptr(kv_c), kv_c.stride(0), _ptr(k_pe), k_pe.stride(0), _ptr(slot_mapping), T,
+            _ptr(cache), cache.shape[0], cache.shape[1], _ptr(global_scale), _ptr(error_word),
+            _stream(cache)))
+
+
+def mla_nvfp4_decode_workspace_size(batch: int, num_heads: int, num_splits: int = 0) -> int:
+    return int(load_library().mla_nvfp4_decode_workspace_size(batch, num_heads, num_splits))
+
+
+def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, seq_lens=None,
+                     page_size=64, topk_indices=None, out=None, lse=None, workspace=None,
+                     num_splits=0, error_word=None, return_lse=False):
+    """Absorbed MLA decode.  q [B,H,576] bf16 -> out [B,H,512] bf16 (and lse [B,H] fp32)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16)
+    _need(cache, "cache", torch.uint8, dev)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    _need(page_table, "page_table", torch.int32, dev)
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    _need(topk_indices, "topk_indices", torch.int32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    if q.dim() != 3 or q.shape[2] != 576 or not q.is_contiguous():
+        raise ValueError("q must be contiguous [B, H, 576]")
+    B, H, _ = q.shape
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    _need(lse, "lse", torch.float32, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        need = lib.mla_nvfp4_decode_workspace_size(B, H, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(int(need), 256), dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, dev)
+        pt_stride = page_table.stride(0) if page_table is not None else 0
+        topk = topk_indices.shape[1] if topk_indices is not None else 0
+        if topk_indices is not None and topk_indices.stride(1) != 1:
+            raise ValueError("topk_indices rows must be contiguous")
+        _check("mla_nvfp4_decode", lib.mla_nvfp4_decode(
+            _ptr(q), B, H, _ptr(cache), cache.shape[0], cache.shape[1], _ptr(page_table), pt_stride,
+            page_size, _ptr(seq_lens), _ptr(topk_indices), topk, float(softmax_scale),
+            _ptr(global_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+            num_splits, _ptr(error_word), _stream(q)))
+    return (out, lse) if return_lse else out
+
+
+def prefill_scale_bytes(total_tokens: int, num_heads: int) -> int:
+    return ((total_tokens + 127) // 128 * 128) * ((num_heads * 8 + 3) // 4 * 4)
+
+
+def mla_nvfp4_prefill_fused_out(q, k, v, cu_seqlens, max_seqlen, softmax_scale, global_scale, *,
+                                out_codes=None, out_scales=None, lse=None, return_lse=False,
+                                error_word=None):
+    """Causal varlen prefill -> (codes [T, H*64] uint8, swizzled scales uint8[, lse [H, T]])."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, dev)
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError(f"{n} must be [T, H, D] with a contiguous last dimension")
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    T, H, dq = q.shape
+    if dq != 192 or k.shape != (T, H, 192) or v.shape != (T, H, 128):
+        raise ValueError("expected q, k [T,H,192] and v [T,H,128]")
+    if out_codes is None:
+        out_codes = torch.empty((T, H * 64), dtype=torch.uint8, device=dev)
+    if out_scales is None:
+        out_scales = torch.empty(prefill_scale_bytes(T, H), dtype=torch.uint8, device=dev)
+    _need(out_codes, "out_codes", torch.uint8, dev)
+    _need(out_scales, "out_scales", torch.uint8, dev)
+    if return_lse and lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    _need(lse, "lse", torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_prefill_fused_out", load_library().mla_nvfp4_prefill_fused_out(
+            _ptr(q), _ptr(k), _ptr(v), q.stride(0), q.stride(1), k.stride(0), k.stride(1),
+            v.stride(0), v.stride(1), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), H,
+            float(softmax_scale), _ptr(global_scale), _ptr(out_codes), _ptr(out_scales), _ptr(lse),
+            _ptr(error_word), _stream(q)))
+    return (out_codes, out_scales, lse) if return_lse else (out_codes, out_scales)
+
+
+def mla_nvfp4_quantize_rows(x, global_scale, *, codes=None, scales=None, error_word=None):
+    """fp32 [M, N] -> (packed codes [M, N/2] uint8, swizzled scales uint8)."""
+    dev = x.device
+    _need(x, "x", torch.float32)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    M, N = x.shape
+    if codes is None:
+        codes = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(((M + 127) // 128 * 128) * ((N // 16 + 3) // 4 * 4), dtype=torch.uint8,
+                             device=dev)
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_quantize_rows", load_library().mla_nvfp4_quantize_rows(
+            _ptr(x), M, N, _ptr(global_scale), _ptr(codes), _ptr(scales), _ptr(error_word),
+            _stream(x)))
+    return codes, scales

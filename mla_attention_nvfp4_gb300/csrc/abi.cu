@@ -1,0 +1,177 @@
+// C ABI of the library: host-side argument checks, then one launch sequence
+// on the caller's stream.  Nothing here allocates or keeps state beyond a
+// per-device cache of the SM count and compute capability.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_info[kMaxDevices];  // 0 = unknown, else (cc << 16) | num_sms
+
+// Current device's SM count, or a negative status when the device is not
+// sm_103 (the only target the library is built for).
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -MLA_ERR_UNSUPPORTED_DEVICE;
+  int info = dev < kMaxDevices ? g_dev_info[dev].load(std::memory_order_relaxed) : 0;
+  if (info == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return -MLA_ERR_UNSUPPORTED_DEVICE;
+    info = ((major * 10 + minor) << 16) | (sms & 0xFFFF);
+    if (dev < kMaxDevices) g_dev_info[dev].store(info, std::memory_order_relaxed);
+  }
+  if ((info >> 16) != 103) return -MLA_ERR_UNSUPPORTED_DEVICE;
+  return info & 0xFFFF;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_nvfp4_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: null pointer, bad size or mode mix";
+    case MLA_ERR_RECORD_BYTES: return "MLA_ERR_RECORD_BYTES: NVFP4 MLA cache record must be 368 or 432 bytes";
+    case MLA_ERR_ALIGNMENT: return "MLA_ERR_ALIGNMENT: pointer or stride not 16-byte aligned";
+    case MLA_ERR_UNSUPPORTED_DEVICE: return "MLA_ERR_UNSUPPORTED_DEVICE: current device is not sm_103 (GB300)";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: decode workspace missing or too small";
+    case MLA_ERR_LAUNCH: return "MLA_ERR_LAUNCH: CUDA launch failed";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_nvfp4_abi_version(void) { return MLA_NVFP4_ABI_VERSION; }
+
+int mla_nvfp4_global_scale(const void* x, int64_t n, float* gs, void* stream) {
+  if (x == nullptr || gs == nullptr || n < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x)) return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  return mla::launch_global_scale(x, n, gs, static_cast<cudaStream_t>(stream), sms);
+}
+
+int mla_nvfp4_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                          int64_t k_pe_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                          uint8_t* cache, int64_t num_slots, int record_bytes,
+                          const float* global_scale, uint32_t* error_word, void* stream) {
+  if (record_bytes != MLA_RECORD_BF16_ROPE && record_bytes != MLA_RECORD_FP8_ROPE)
+    return MLA_ERR_RECORD_BYTES;
+  if (num_tokens < 0 || num_slots < 0) return MLA_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (kv_c == nullptr || k_pe == nullptr || slot_mapping == nullptr ||
+                         cache == nullptr || global_scale == nullptr))
+    return MLA_ERR_INVALID_ARG;
+  if (kv_c_stride < MLA_D_LATENT || k_pe_stride < MLA_D_ROPE) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(kv_c) || !aligned16(k_pe) || !aligned16(cache) || (kv_c_stride * 2) % 16 ||
+      (k_pe_stride * 2) % 16)
+    return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  return mla::launch_cache_write(kv_c, kv_c_stride, k_pe, k_pe_stride, slot_mapping, num_tokens,
+                                 cache, num_slots, record_bytes, global_scale, error_word,
+                                 static_cast<cudaStream_t>(stream), sms);
+}
+
+size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits) {
+  if (batch < 1 || num_heads < 1) return 0;
+  if (num_splits <= 0) {
+    const int sms = device_sms();
+    num_splits = mla::decode_default_splits(batch, num_heads, sms > 0 ? sms : 152);
+  }
+  return mla::decode_workspace_bytes(batch, num_heads, num_splits);
+}
+
+int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cache,
+                     int64_t num_slots, int record_bytes, const int32_t* page_table,
+                     int64_t page_table_stride, int page_size, const int32_t* seq_lens,
+                     const int32_t* topk_indices, int topk, float softmax_scale,
+                     const float* global_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, int num_splits, uint32_t* error_word, void* stream) {
+  if (record_bytes != MLA_RECORD_BF16_ROPE && record_bytes != MLA_RECORD_FP8_ROPE)
+    return MLA_ERR_RECORD_BYTES;
+  if (batch < 0 || num_heads < 1 || num_slots < 0) return MLA_ERR_INVALID_ARG;
+  const bool paged = page_table != nullptr || seq_lens != nullptr;
+  const bool sparse = topk_indices != nullptr;
+  if (paged == sparse) return MLA_ERR_INVALID_ARG;  // exactly one mode
+  if (paged && (page_table == nullptr || seq_lens == nullptr || page_size < 1 ||
+                page_table_stride < 1))
+    return MLA_ERR_INVALID_ARG;
+  if (sparse && topk < 0) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (q == nullptr || cache == nullptr || global_scale == nullptr || out == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !(softmax_scale < 3.0e38f)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(cache) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  if (num_splits <= 0) num_splits = mla::decode_default_splits(batch, num_heads, sms);
+  if (num_splits > 4096) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla::decode_workspace_bytes(batch, num_heads, num_splits);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MLA_ERR_WORKSPACE;
+  mla::DecodeArgs a{q, batch, num_heads, cache, num_slots, record_bytes, page_table,
+                    page_table_stride, page_size, seq_lens, topk_indices, sparse ? topk : 0,
+                    softmax_scale, global_scale, out, lse, workspace, num_splits, error_word};
+  return mla::launch_decode(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
+                                int64_t q_stride_t, int64_t q_stride_h, int64_t k_stride_t,
+                                int64_t k_stride_h, int64_t v_stride_t, int64_t v_stride_h,
+                                const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
+                                int max_seqlen, int num_heads, float softmax_scale,
+                                const float* global_scale, uint8_t* out_codes,
+                                uint8_t* out_scales, float* lse, uint32_t* error_word,
+                                void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || num_heads < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (total_tokens == 0 || num_seqs == 0) {
+    if (total_tokens != 0) return MLA_ERR_INVALID_ARG;
+    return MLA_OK;
+  }
+  if (max_seqlen < 1 || total_tokens > (int64_t(1) << 31) - 1) return MLA_ERR_INVALID_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || cu_seqlens == nullptr ||
+      global_scale == nullptr || out_codes == nullptr || out_scales == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !(softmax_scale < 3.0e38f)) return MLA_ERR_INVALID_ARG;
+  if (q_stride_h < MLA_D_QK_PREFILL || k_stride_h < MLA_D_QK_PREFILL ||
+      v_stride_h < MLA_D_V_PREFILL || q_stride_t < q_stride_h * (num_heads - 1) + MLA_D_QK_PREFILL ||
+      k_stride_t < k_stride_h * (num_heads - 1) + MLA_D_QK_PREFILL ||
+      v_stride_t < v_stride_h * (num_heads - 1) + MLA_D_V_PREFILL)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_codes) ||
+      (q_stride_t * 2) % 16 || (q_stride_h * 2) % 16 || (k_stride_t * 2) % 16 ||
+      (k_stride_h * 2) % 16 || (v_stride_t * 2) % 16 || (v_stride_h * 2) % 16)
+    return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  mla::PrefillArgs a{q, k, v, q_stride_t, q_stride_h, k_stride_t, k_stride_h, v_stride_t,
+                     v_stride_h, cu_seqlens, num_seqs, total_tokens, max_seqlen, num_heads,
+                     softmax_scale, global_scale, out_codes, out_scales, lse, error_word};
+  return mla::launch_prefill(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+int mla_nvfp4_quantize_rows(const float* x, int64_t M, int64_t N, const float* global_scale,
+                            uint8_t* codes, uint8_t* scales, uint32_t* error_word, void* stream) {
+  if (M < 0 || N < 0 || N % 16 != 0) return MLA_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MLA_OK;
+  if (x == nullptr || global_scale == nullptr || codes == nullptr || scales == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u) != 0) return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  return mla::launch_quantize_rows(x, M, N, global_scale, codes, scales, error_word,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernel files.
+// Arguments are validated by the caller; these functions only launch.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/mla_nvfp4.h"
+
+namespace mla {
+
+int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, int64_t pe_stride,
+                       const int64_t* slot_mapping, int64_t num_tokens, uint8_t* cache,
+                       int64_t num_slots, int record_bytes, const float* gs,
+                       uint32_t* error_word, cudaStream_t stream, int num_sms);
+
+int launch_quantize_rows(const float* x, int64_t M, int64_t N, const float* gs, uint8_t* codes,
+                         uint8_t* scales, uint32_t* error_word, cudaStream_t stream);
+
+int launch_global_scale(const void* x, int64_t n, float* gs, cudaStream_t stream, int num_sms);
+
+struct DecodeArgs {
+  const void* q;
+  int batch;
+  int num_heads;
+  const uint8_t* cache;
+  int64_t num_slots;
+  int record_bytes;
+  const int32_t* page_table;
+  int64_t page_table_stride;
+  int page_size;
+  const int32_t* seq_lens;
+  const int32_t* topk_indices;
+  int topk;
+  float softmax_scale;
+  const float* gs;
+  void* out;
+  float* lse;
+  void* workspace;
+  int num_splits;
+  uint32_t* error_word;
+};
+
+// Decode workspace layout for (batch, heads, splits).
+size_t decode_workspace_bytes(int batch, int num_heads, int num_splits);
+int decode_default_splits(int batch, int num_heads, int num_sms);
+int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms);
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
+  const int32_t* cu_seqlens;
+  int num_seqs;
+  int64_t total_tokens;
+  int max_seqlen;
+  int num_heads;
+  float softmax_scale;
+  const float* gs;
+  uint8_t* out_codes;
+  uint8_t* out_scales;
+  float* lse;
+  uint32_t* error_word;
+};
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms);
+
+}  // namespace mla

@@ -1,0 +1,217 @@
+// Elementwise NVFP4 kernels: latent cache write, the quantise-rows hook and
+// the global-scale reduction.  All three are HBM-bound: no tensor cores,
+// 16-byte vector loads, one pass over the input.
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "nvfp4.cuh"
+
+namespace mla {
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4& v, float* f) {
+  bf16x2_to_f32(v.x, f[0], f[1]);
+  bf16x2_to_f32(v.y, f[2], f[3]);
+  bf16x2_to_f32(v.z, f[4], f[5]);
+  bf16x2_to_f32(v.w, f[6], f[7]);
+}
+
+// ---------------------------------------------------------------------------
+// Cache write.  One warp per token.  Lane l loads latent elements [8l, 8l+8)
+// and [256+8l, 256+8l+8) with two fully coalesced 512-byte warp loads; the
+// block of 16 is shared by lanes 2j and 2j+1, whose amax is combined with one
+// shuffle.  Record stores: 2 x 128 B of codes, 32 B of scales, the RoPE part
+// and the 16-byte zero pad.
+// Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for MLA (vLLM
+// TRITON_MLA) - #2244", second commit message (quantise at cache-write
+// time); "nvfp4 MLA KV cache + per-layer outer-scale + fp8-RoPE KV-cell
+// (sm120) - #33", review of api.py (432 / 368-byte records).
+// ---------------------------------------------------------------------------
+template <bool kFp8Rope>
+__global__ void __launch_bounds__(256) cache_write_kernel(
+    const __nv_bfloat16* __restrict__ kv_c, int64_t kv_stride, const __nv_bfloat16* __restrict__ k_pe,
+    int64_t pe_stride, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
+    uint8_t* __restrict__ cache, int64_t num_slots, const float* __restrict__ gs_ptr,
+    uint32_t* error_word) {
+  constexpr int kRecord = kFp8Rope ? 368 : 432;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const float gs = *gs_ptr;
+  const bool gs_valid = scale_ok(gs);
+  if (!gs_valid && warp == 0 && lane == 0) flag_error(error_word, MLA_DEVERR_SCALE);
+
+  for (int64_t t = warp; t < num_tokens; t += n_warps) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (lane == 0) flag_error(error_word, MLA_DEVERR_BOUNDS);
+      continue;
+    }
+    const __nv_bfloat16* row = kv_c + t * kv_stride;
+    const uint4 va = ldg_stream(row + 8 * lane);
+    const uint4 vb = ldg_stream(row + 256 + 8 * lane);
+    uint4 vr = make_uint4(0, 0, 0, 0);
+    if (lane < 8) vr = ldg_stream(k_pe + t * pe_stride + 8 * lane);
+
+    float xa[8], xb[8];
+    unpack8_bf16(va, xa);
+    unpack8_bf16(vb, xb);
+    float am_a = amax8(xa), am_b = amax8(xb);
+    am_a = fmaxf(am_a, __shfl_xor_sync(0xffffffffu, am_a, 1));
+    am_b = fmaxf(am_b, __shfl_xor_sync(0xffffffffu, am_b, 1));
+    uint32_t code_a = 0, code_b = 0, sb_a = 0, sb_b = 0;
+    if (gs_valid) {
+      float Sa, Sb;
+      sb_a = block_scale(am_a, gs, Sa);
+      sb_b = block_scale(am_b, gs, Sb);
+      code_a = encode8(xa, Sa);
+      code_b = encode8(xb, Sb);
+    }
+    uint8_t* rec = cache + slot * kRecord;
+    reinterpret_cast<uint32_t*>(rec)[lane] = code_a;        // bytes [4l, 4l+4)
+    reinterpret_cast<uint32_t*>(rec + 128)[lane] = code_b;  // bytes [128+4l, ...)
+    if ((lane & 1) == 0) {
+      rec[256 + (lane >> 1)] = static_cast<uint8_t>(sb_a);
+      rec[256 + 16 + (lane >> 1)] = static_cast<uint8_t>(sb_b);
+    }
+    if (lane < 8) {
+      if constexpr (kFp8Rope) {
+        float r[8];
+        unpack8_bf16(vr, r);
+        const uint32_t w0 = cvt_e4m3x2(r[0], r[1]) | (cvt_e4m3x2(r[2], r[3]) << 16);
+        const uint32_t w1 = cvt_e4m3x2(r[4], r[5]) | (cvt_e4m3x2(r[6], r[7]) << 16);
+        reinterpret_cast<uint2*>(rec + 288)[lane] = make_uint2(w0, w1);
+      } else {
+        reinterpret_cast<uint4*>(rec + 288)[lane] = vr;
+      }
+    } else if (lane == 8) {
+      *reinterpret_cast<uint4*>(rec + kRecord - 16) = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, int64_t pe_stride,
+                       const int64_t* slot_mapping, int64_t num_tokens, uint8_t* cache,
+                       int64_t num_slots, int record_bytes, const float* gs,
+                       uint32_t* error_word, cudaStream_t stream, int num_sms) {
+  if (num_tokens == 0) return MLA_OK;
+  const int64_t want = (num_tokens + 7) / 8;  // 8 warps per block, one token each
+  const int64_t cap = static_cast<int64_t>(num_sms) * 64;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  auto kv = static_cast<const __nv_bfloat16*>(kv_c);
+  auto pe = static_cast<const __nv_bfloat16*>(k_pe);
+  if (record_bytes == 368)
+    cache_write_kernel<true><<<grid, 256, 0, stream>>>(kv, kv_stride, pe, pe_stride, slot_mapping,
+                                                       num_tokens, cache, num_slots, gs, error_word);
+  else
+    cache_write_kernel<false><<<grid, 256, 0, stream>>>(kv, kv_stride, pe, pe_stride, slot_mapping,
+                                                        num_tokens, cache, num_slots, gs, error_word);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Quantise rows (fp32 [M, N] -> packed codes + swizzled scales).  One thread
+// per scale slot of the padded [Mp, Kp] scale matrix: real slots quantise a
+// block of 16, padding slots write a zero scale byte.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restrict__ x, int64_t M,
+                                                            int64_t N, const float* __restrict__ gs_ptr,
+                                                            uint8_t* __restrict__ codes,
+                                                            uint8_t* __restrict__ scales,
+                                                            uint32_t* error_word) {
+  const int64_t K = N / 16;
+  const int64_t Kp = (K + 3) & ~int64_t(3);
+  const int64_t Mp = (M + 127) & ~int64_t(127);
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= Mp * Kp) return;
+  const int64_t m = idx / Kp, k = idx % Kp;
+  const float gs = *gs_ptr;
+  const bool gs_valid = scale_ok(gs);
+  if (!gs_valid && idx == 0) flag_error(error_word, MLA_DEVERR_SCALE);
+  uint32_t sb = 0;
+  if (m < M && k < K) {
+    const float4* src = reinterpret_cast<const float4*>(x + m * N + k * 16);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = src[i];
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+    uint32_t lo = 0, hi = 0;
+    if (gs_valid) {
+      float S;
+      sb = block_scale(fmaxf(amax8(v), amax8(v + 8)), gs, S);
+      lo = encode8(v, S);
+      hi = encode8(v + 8, S);
+    }
+    *reinterpret_cast<uint2*>(codes + m * (N / 2) + k * 8) = make_uint2(lo, hi);
+  }
+  scales[sf_offset(m, k, Kp / 4)] = static_cast<uint8_t>(sb);
+}
+
+int launch_quantize_rows(const float* x, int64_t M, int64_t N, const float* gs, uint8_t* codes,
+                         uint8_t* scales, uint32_t* error_word, cudaStream_t stream) {
+  const int64_t K = N / 16;
+  const int64_t total = ((M + 127) / 128 * 128) * ((K + 3) / 4 * 4);
+  if (total == 0) return MLA_OK;
+  const int64_t grid = (total + 255) / 256;
+  if (grid > 0x7fffffff) return MLA_ERR_INVALID_ARG;
+  quantize_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(x, M, N, gs, codes, scales,
+                                                                         error_word);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Global scale: gs = fp32(amax|x| / 2688).  Pass 1 reduces |x| into the
+// output word as an unsigned integer (non-negative floats order like their
+// bit patterns); pass 2 turns the maximum into the scale in place.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t n,
+                                                   uint32_t* __restrict__ out_bits) {
+  float m = 0.f;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t n8 = n / 8;
+  for (int64_t i = tid; i < n8; i += stride) {
+    float f[8];
+    unpack8_bf16(ldg_stream(x + 8 * i), f);
+    m = fmaxf(m, amax8(f));
+  }
+  for (int64_t i = n8 * 8 + tid; i < n; i += stride) m = fmaxf(m, fabsf(__bfloat162float(x[i])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = red[0];
+    for (int i = 1; i < 8; ++i) b = fmaxf(b, red[i]);
+    atomicMax(out_bits, __float_as_uint(b));
+  }
+}
+
+__global__ void finalize_scale_kernel(float* gs) {
+  const float amax = __uint_as_float(*reinterpret_cast<uint32_t*>(gs));
+  *gs = __fdiv_rn(amax, 2688.0f);
+}
+
+int launch_global_scale(const void* x, int64_t n, float* gs, cudaStream_t stream, int num_sms) {
+  if (cudaMemsetAsync(gs, 0, sizeof(float), stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  const int64_t want = (n / 8 + 255) / 256 + 1;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  amax_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), n,
+                                        reinterpret_cast<uint32_t*>(gs));
+  finalize_scale_kernel<<<1, 1, 0, stream>>>(gs);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+}
+
+}  // namespace mla

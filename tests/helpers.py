@@ -1,0 +1,98 @@
+"""Shared test helpers: running the oracle on workload tensors and the
+comparison rules (tolerances from the method's stated acceptance bar)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import attention, cache as ocache, nvfp4, swizzle
+
+# Dequantised attention outputs: max-abs error and mean relative (L1) error
+# against the float64 oracle.
+MAX_ABS = 2e-2
+MEAN_REL = 5e-3
+# Rounding-tie budget for codes where both sides do not see the same input.
+TIE_BUDGET = 1e-4
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def oracle_gs(x: torch.Tensor) -> np.float32:
+    return nvfp4.global_scale(np.abs(f32(x)).max())
+
+
+def oracle_cache(w, gs) -> np.ndarray:
+    c = np.zeros((w.num_slots, w.record_bytes), dtype=np.uint8)
+    ocache.write_cache(c, f32(w.kv_c), f32(w.k_pe), w.slot_mapping.cpu().numpy(), gs, w.record_bytes)
+    return c
+
+
+def oracle_slots(w):
+    if w.paged:
+        return attention.decode_slots_paged(w.page_table.cpu().numpy(), w.seq_lens.cpu().numpy(), 64)
+    return attention.decode_slots_topk(w.topk_indices.cpu().numpy())
+
+
+def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    denom = float(np.abs(ref).sum())
+    mean_rel = float(err.sum() / denom) if denom > 0 else float(err.sum())
+    assert max_abs <= MAX_ABS and mean_rel <= MEAN_REL, \
+        f"{what}: max_abs={max_abs:.3e} (<= {MAX_ABS}), mean_rel={mean_rel:.3e} (<= {MEAN_REL})"
+    return max_abs, mean_rel
+
+
+def assert_lse_close(got, ref, what: str, tol=2e-3):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    inf = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf), f"{what}: -inf pattern differs"
+    d = np.abs(got[~inf] - ref[~inf])
+    assert d.size == 0 or d.max() <= tol, f"{what}: lse max diff {d.max():.3e}"
+
+
+def code_boundary_distance(q: np.ndarray) -> np.ndarray:
+    """Distance of |q| (value / block scale) to the nearest e2m1 rounding
+    midpoint, in code units."""
+    mids = (nvfp4.E2M1_MAGNITUDES[:-1] + nvfp4.E2M1_MAGNITUDES[1:]) / 2
+    return np.min(np.abs(np.abs(q)[..., None] - mids), axis=-1)
+
+
+def check_fused_output(codes_gpu, scales_gpu, o_ref, gs, eps_rel=4e-3):
+    """End-to-end NVFP4 output check where the kernel quantises its own fp32
+    attention output: a scale byte may differ only where the oracle's raw
+    scale is within eps_rel of an e4m3 rounding midpoint, and a code only
+    where the oracle's value/scale is within eps_rel*6 of an e2m1 midpoint
+    (or its block's scale differs).  Returns the mismatch counts."""
+    M, N = o_ref.shape
+    K = N // 16
+    x = o_ref.astype(np.float32)
+    codes_ref, sb_ref = nvfp4.quantize_blocks(x, gs)
+    sf_gpu = swizzle.unswizzle_scales(scales_gpu, M, K)
+    codes_g = nvfp4.unpack_e2m1(codes_gpu.reshape(M, N // 2))
+    sb_ref = sb_ref.reshape(M, K)
+    # scales
+    amax = np.abs(x.reshape(M, K, 16)).max(-1).astype(np.float64)
+    s_raw = amax / 6.0 / float(gs)
+    grid = nvfp4.e4m3_decode(np.arange(127))
+    mids = (grid[:-1] + grid[1:]) / 2
+    near_s = np.min(np.abs(s_raw[..., None] - mids), axis=-1) <= eps_rel * np.maximum(s_raw, 1e-30)
+    bad_s = (sf_gpu != sb_ref)
+    assert not np.any(bad_s & ~near_s), f"{int((bad_s & ~near_s).sum())} scale bytes differ away from a tie"
+    # codes (only in blocks whose scale agrees)
+    S = (nvfp4.e4m3_decode(sb_ref) * float(gs)).repeat(16, axis=1)
+    q = np.where(S > 0, x.astype(np.float64) / np.where(S > 0, S, 1), 0)
+    near_c = code_boundary_distance(q) <= eps_rel * 6
+    same_scale = (~bad_s).repeat(16, axis=1)
+    diff = (codes_g != codes_ref)
+    # a flip of the sign of zero is allowed where the value rounds to zero
+    zero_both = ((codes_g & 7) == 0) & ((codes_ref & 7) == 0)
+    diff &= ~zero_both
+    bad = diff & same_scale & ~near_c
+    assert not np.any(bad), f"{int(bad.sum())} codes differ away from a rounding boundary"
+    return int(bad_s.sum()), int((diff & same_scale).sum())

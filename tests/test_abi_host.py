@@ -1,0 +1,73 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+entry point include/mla_nvfp4.h declares, and rejects bad arguments on the
+host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_attention_nvfp4_gb300 as mla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "mla_nvfp4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_nvfp4_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = mla.load_library()
+    declared = _header_functions()
+    assert len(declared) >= 7
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(mla.abi_symbols()) == declared
+    assert lib.mla_nvfp4_abi_version() == 1
+
+
+def test_status_strings():
+    assert mla.status_string(0) == "MLA_OK"
+    assert "368 or 432" in mla.status_string(2)
+    assert mla.status_string(99) == "MLA_ERR_UNKNOWN"
+
+
+def test_record_width_rejected_before_launch():
+    lib = mla.load_library()
+    for rb in (0, 400, 431, 433, 367, 369, 512):
+        assert lib.mla_nvfp4_cache_write(None, 512, None, 64, None, 1, None, 1, rb, None, None, None) == 2
+        assert lib.mla_nvfp4_decode(None, 1, 1, None, 1, rb, None, 0, 64, None, None, 0, 1.0, None,
+                                    None, None, None, 0, 0, None, None) == 2
+
+
+def test_mode_mix_rejected():
+    lib = mla.load_library()
+    p = ctypes.c_void_p(16)
+    # both paged and top-k
+    assert lib.mla_nvfp4_decode(p, 1, 1, p, 1, 432, p, 1, 64, p, p, 4, 1.0, p, p, None, p, 1 << 20, 1,
+                                None, None) == 1
+    # neither
+    assert lib.mla_nvfp4_decode(p, 1, 1, p, 1, 432, None, 0, 64, None, None, 0, 1.0, p, p, None, p,
+                                1 << 20, 1, None, None) == 1
+
+
+def test_bad_sizes_rejected():
+    lib = mla.load_library()
+    p = ctypes.c_void_p(16)
+    assert lib.mla_nvfp4_quantize_rows(p, 4, 17, p, p, p, None, None) == 1   # N % 16
+    assert lib.mla_nvfp4_quantize_rows(p, 0, 32, p, p, p, None, None) == 0   # empty is a no-op
+    assert lib.mla_nvfp4_cache_write(p, 500, p, 64, p, 1, p, 1, 432, p, None, None) == 1  # stride < 512
+    assert lib.mla_nvfp4_cache_write(p, 516, p, 64, p, 1, p, 1, 432, p, None, None) == 3  # 1032 B stride
+    assert lib.mla_nvfp4_cache_write(ctypes.c_void_p(8), 512, p, 64, p, 1, p, 1, 432, p, None, None) == 3
+    assert lib.mla_nvfp4_decode_workspace_size(0, 128, 4) == 0
+    assert lib.mla_nvfp4_decode_workspace_size(2, 16, 4) > 0
+    # prefill: bad head stride, zero tokens is a no-op
+    assert lib.mla_nvfp4_prefill_fused_out(p, p, p, 192 * 2, 100, 192 * 2, 192, 128 * 2, 128, p, 1, 4, 4,
+                                           2, 1.0, p, p, p, None, None, None) == 1
+    assert lib.mla_nvfp4_prefill_fused_out(p, p, p, 192, 192, 192, 192, 128, 128, p, 1, 0, 0, 1, 1.0, p,
+                                           p, p, None, None, None) == 0
+    # non-positive softmax scale
+    assert lib.mla_nvfp4_prefill_fused_out(p, p, p, 192, 192, 192, 192, 128, 128, p, 1, 4, 4, 1, 0.0, p,
+                                           p, p, None, None, None) == 1
