@@ -30,6 +30,19 @@ DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE = 0x1, 0x2, 0x4
 
 # Kernels each entry point launches (for launch accounting in the benchmark).
 LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 2, "prefill": 1, "global_scale": 2}
+# What bounds each hot kernel as built: "hbm", "tensor" (tcgen05 MMA) or
+# "alu" (CUDA-core arithmetic).
+KERNEL_BOUND = {"cache_write": "hbm", "decode": "tensor", "prefill": "tensor"}
+# Operand type of the tensor-core attention products (fp32 accumulation).
+COMPUTE_DTYPE = "bf16"
+
+
+def kernel_kind(name: str) -> str:
+    return KERNEL_BOUND[name]
+
+
+def compute_dtype() -> str:
+    return COMPUTE_DTYPE
 
 _LIB = None
 

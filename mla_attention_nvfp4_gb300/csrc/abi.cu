@@ -150,6 +150,7 @@ int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
       v_stride_t < v_stride_h * (num_heads - 1) + MLA_D_V_PREFILL)
     return MLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_codes) ||
+      (reinterpret_cast<uintptr_t>(out_scales) & 3u) != 0 ||
       (q_stride_t * 2) % 16 || (q_stride_h * 2) % 16 || (k_stride_t * 2) % 16 ||
       (k_stride_h * 2) % 16 || (v_stride_t * 2) % 16 || (v_stride_h * 2) % 16)
     return MLA_ERR_ALIGNMENT;

@@ -98,13 +98,14 @@ def decode(q, cache, record_bytes, gs, softmax_scale, slots_per_seq):
     return out, lse
 
 
-def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None):
+def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None, with_abs=False):
     """Causal varlen prefill.
 
     q, k [T,H,Dqk], v [T,H,Dv] (bf16 values); cu_seqlens [S+1].  Query i of a
     sequence sees keys 0..i of the same sequence.  ``heads`` restricts the
     computation to a subset of heads (the others are left zero).
-    Returns (o [T,H,Dv], lse [H,T]) in float64.
+    Returns (o [T,H,Dv], lse [H,T]) in float64; with ``with_abs`` also
+    softmax(s) @ |v|, the scale of any rounding of the probabilities.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -113,6 +114,7 @@ def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None):
     Dv = v.shape[2]
     heads = range(H) if heads is None else heads
     o = np.zeros((T, H, Dv))
+    o_abs = np.zeros((T, H, Dv)) if with_abs else None
     lse = np.full((H, T), -np.inf)
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     for s in range(len(cu) - 1):
@@ -128,8 +130,10 @@ def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None):
             p = np.exp(sc - m)
             l = p.sum(axis=1, keepdims=True)
             o[a:e, h] = (p / l) @ v[a:e, h]
+            if with_abs:
+                o_abs[a:e, h] = (p / l) @ np.abs(v[a:e, h])
             lse[h, a:e] = (m + np.log(l))[:, 0]
-    return o, lse
+    return (o, lse, o_abs) if with_abs else (o, lse)
 
 
 def prefill_rows(q, k, v, cu_seqlens, softmax_scale, rows, head):

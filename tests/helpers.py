@@ -47,7 +47,12 @@ def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str):
     return max_abs, mean_rel
 
 
-def assert_lse_close(got, ref, what: str, tol=2e-3):
+# LSE: the partition function to within the mean relative error bar of the
+# outputs, ln(1 + 5e-3).
+LSE_TOL = float(np.log1p(MEAN_REL))
+
+
+def assert_lse_close(got, ref, what: str, tol=LSE_TOL):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     inf = np.isneginf(ref)
@@ -63,34 +68,46 @@ def code_boundary_distance(q: np.ndarray) -> np.ndarray:
     return np.min(np.abs(np.abs(q)[..., None] - mids), axis=-1)
 
 
-def check_fused_output(codes_gpu, scales_gpu, o_ref, gs, eps_rel=4e-3):
+# Bound on the kernel's output error from rounding the probabilities to bf16
+# for the tensor-core P.V product: |dO| <= 2^-9 * sum_j p_j |v_j| / sum_j p_j
+# per element (fp32 accumulation adds ~1e-6 relative); 2^-8 leaves a 2x margin.
+P_ROUNDING = 2.0 ** -8
+
+
+def check_fused_output(codes_gpu, scales_gpu, o_ref, o_abs, gs):
     """End-to-end NVFP4 output check where the kernel quantises its own fp32
-    attention output: a scale byte may differ only where the oracle's raw
-    scale is within eps_rel of an e4m3 rounding midpoint, and a code only
-    where the oracle's value/scale is within eps_rel*6 of an e2m1 midpoint
-    (or its block's scale differs).  Returns the mismatch counts."""
+    attention output.  Each output element may differ from the exact one by
+    err = P_ROUNDING * o_abs (+1e-6 relative).  A scale byte may differ from
+    the oracle's quantisation of the exact output only where the block's raw
+    scale lies within the error of an e4m3 rounding midpoint, and a code only
+    where value/scale lies within err/scale of an e2m1 midpoint (or its
+    block's scale differs).  Returns (scale mismatches, code mismatches)."""
     M, N = o_ref.shape
     K = N // 16
     x = o_ref.astype(np.float32)
+    err = (P_ROUNDING * np.asarray(o_abs, dtype=np.float64) + 1e-6 * np.abs(o_ref)).reshape(M, N) + 1e-30
     codes_ref, sb_ref = nvfp4.quantize_blocks(x, gs)
     sf_gpu = swizzle.unswizzle_scales(scales_gpu, M, K)
     codes_g = nvfp4.unpack_e2m1(codes_gpu.reshape(M, N // 2))
     sb_ref = sb_ref.reshape(M, K)
     # scales
     amax = np.abs(x.reshape(M, K, 16)).max(-1).astype(np.float64)
+    d_amax = err.reshape(M, K, 16).max(-1)
     s_raw = amax / 6.0 / float(gs)
+    ds = d_amax / 6.0 / float(gs)
     grid = nvfp4.e4m3_decode(np.arange(127))
     mids = (grid[:-1] + grid[1:]) / 2
-    near_s = np.min(np.abs(s_raw[..., None] - mids), axis=-1) <= eps_rel * np.maximum(s_raw, 1e-30)
+    near_s = np.min(np.abs(s_raw[..., None] - mids), axis=-1) <= ds
     bad_s = (sf_gpu != sb_ref)
     assert not np.any(bad_s & ~near_s), f"{int((bad_s & ~near_s).sum())} scale bytes differ away from a tie"
     # codes (only in blocks whose scale agrees)
     S = (nvfp4.e4m3_decode(sb_ref) * float(gs)).repeat(16, axis=1)
-    q = np.where(S > 0, x.astype(np.float64) / np.where(S > 0, S, 1), 0)
-    near_c = code_boundary_distance(q) <= eps_rel * 6
+    safe = np.where(S > 0, S, 1.0)
+    q = np.where(S > 0, x.astype(np.float64) / safe, 0)
+    near_c = code_boundary_distance(q) <= err / safe
     same_scale = (~bad_s).repeat(16, axis=1)
     diff = (codes_g != codes_ref)
-    # a flip of the sign of zero is allowed where the value rounds to zero
+    # the sign of a value that rounds to zero may differ
     zero_both = ((codes_g & 7) == 0) & ((codes_ref & 7) == 0)
     diff &= ~zero_both
     bad = diff & same_scale & ~near_c

@@ -35,10 +35,11 @@ def test_prefill_small(lens, heads):
     w = workloads.prefill("small", seq_lens=lens, heads=heads, seed=sum(lens))
     gs = oracle_gs(w.v)
     codes, sf, lse = _run(w, gs)
-    o_ref, l_ref = attention.prefill(f32(w.q), f32(w.k), f32(w.v), w.cu_seqlens.numpy(), w.softmax_scale)
+    o_ref, l_ref, o_abs = attention.prefill(f32(w.q), f32(w.k), f32(w.v), w.cu_seqlens.numpy(),
+                                             w.softmax_scale, with_abs=True)
     T = w.total_tokens
     o2 = o_ref.reshape(T, heads * 128)
-    n_sf, n_codes = check_fused_output(codes, sf, o2, gs)
+    n_sf, n_codes = check_fused_output(codes, sf, o2, o_abs.reshape(T, heads * 128), gs)
     deq = swizzle.dequantize_rows(codes, sf, T, heads * 128, gs)
     ref_deq = swizzle.dequantize_rows(*swizzle.quantize_rows(o2.astype(np.float32), gs), T, heads * 128, gs)
     # codes agree up to boundary flips (checked above), so the dequantised
