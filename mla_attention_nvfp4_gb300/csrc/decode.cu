@@ -56,7 +56,7 @@ constexpr int kThreads = 320;
 constexpr int kRawStride = 224;    // bytes per key in the raw ring (208 used)
 constexpr int kRawStages = 4;
 constexpr int kKvStages = 3;
-constexpr int kXchBufs = 3;
+constexpr int kXchBufs = 4;
 constexpr uint32_t kRawBytes = kTok * kRawStride;         // 7168
 constexpr uint32_t kKvBlock = kTok * 128;                 // one 64-feature column block
 constexpr uint32_t kKvBytes = 5 * kKvBlock;               // 4 latent blocks + RoPE block
@@ -181,6 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
+  __shared__ uint32_t raw_mask[kRawStages];  // valid keys of each raw stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -201,7 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
   if (threadIdx.x == 0) {
     abort_s = 0;
     for (int i = 0; i < kRawStages; ++i) {
-      mbar_init(&bars.raw_full[i], 32);
+      mbar_init(&bars.raw_full[i], 33);  // 32 cp.async arrivals + the mask writer
       mbar_init(&bars.raw_empty[i], 128);
     }
     for (int i = 0; i < kKvStages; ++i) {
@@ -231,13 +232,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Slot ids are fetched two tiles ahead so their latency stays off the
+    // copy-issue path.
     bool bad = false;
+    int64_t slot_a = nt > 0 ? key_slot(p, b, tile0 * kTok + lane, n_keys, bad) : -1;
+    int64_t slot_b = nt > 1 ? key_slot(p, b, (tile0 + 1) * kTok + lane, n_keys, bad) : -1;
     for (int j = 0; j < nt; ++j) {
       const int st = j % kRawStages;
       const uint32_t ph = (j / kRawStages) & 1;
+      const int64_t slot = slot_a;
+      slot_a = slot_b;
+      slot_b = (j + 2 < nt) ? key_slot(p, b, (tile0 + j + 2) * kTok + lane, n_keys, bad) : -1;
       if (!mbar_wait(&bars.raw_empty[st], ph ^ 1, err, &abort_s)) break;
-      const int t = (tile0 + j) * kTok + lane;
-      const int64_t slot = key_slot(p, b, t, n_keys, bad);
+      const unsigned vmask = __ballot_sync(0xffffffffu, slot >= 0);
       if (slot >= 0) {
         const uint8_t* rec = p.cache + slot * kRecord;
         uint8_t* dst = sRaw + st * kRawBytes + lane * kRawStride;
@@ -253,6 +260,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         }
       }
       cp_async_arrive(&bars.raw_full[st]);
+      if (lane == 0) {
+        raw_mask[st] = vmask;
+        mbar_arrive(&bars.raw_full[st]);
+      }
     }
     if (bad && rank == 0) flag_error(err, MLA_DEVERR_BOUNDS);
     cp_async_wait_all();
@@ -276,17 +287,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         mma_commit(&bars.pv_done[pb]);
         return true;
       };
-      for (int j = 0; ok && j < nt; ++j) {
+      // QK runs two tiles ahead of PV: S(i+2) is computed while the softmax
+      // works on tile i.
+      auto issue_qk = [&](int j) -> bool {
         const int ks = j % kKvStages;
         const int sb = j & 1;
-        if (!mbar_wait(&bars.kv_full[ks], (j / kKvStages) & 1, err, &abort_s)) {
-          ok = false;
-          break;
-        }
-        if (j >= 2 && !mbar_wait(&bars.s_free[sb], ((j - 2) >> 1) & 1, err, &abort_s)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&bars.kv_full[ks], (j / kKvStages) & 1, err, &abort_s)) return false;
+        if (j >= 2 && !mbar_wait(&bars.s_free[sb], ((j - 2) >> 1) & 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t kbase = kv_addr + ks * kKvBytes;
 #pragma unroll
@@ -295,9 +302,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
           mma_ts(tmem + col_s(sb), tmem + kTQ + kk * 8, bd, kIdescQK, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.s_full[sb]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      if (ok && nt > 1) ok = issue_qk(1);
+      for (int i = 0; ok && i < nt; ++i) {
+        if (i + 2 < nt && !issue_qk(i + 2)) {
+          ok = false;
+          break;
+        }
+        if (!issue_pv(i)) ok = false;
       }
-      if (ok) issue_pv(nt - 1);
       mma_commit(&bars.o_full);
       mbar_wait(&bars.o_full, 0, err, nullptr);  // every MMA retired
     }
@@ -305,13 +320,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     // ---------------------------------------------------------- dequantise
     const int dt = threadIdx.x - 64;
     const int tok = dt >> 2, part = dt & 3;
-    bool bad = false;
     for (int j = 0; j < nt; ++j) {
       const int st = j % kRawStages, ks = j % kKvStages;
       if (!mbar_wait(&bars.raw_full[st], (j / kRawStages) & 1, err, &abort_s)) break;
       if (!mbar_wait(&bars.kv_empty[ks], ((j / kKvStages) & 1) ^ 1, err, &abort_s)) break;
-      const int t = (tile0 + j) * kTok + tok;
-      const bool valid = key_slot(p, b, t, n_keys, bad) >= 0;
+      const bool valid = (raw_mask[st] >> tok) & 1u;
       uint8_t* kv = sKV + ks * kKvBytes;
       const uint32_t sw = tok & 7;
       uint4 outv[8];
@@ -415,8 +428,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       const uint32_t xch_local = smem_u32(sXch);
       const uint32_t xch_peer = map_peer(xch_local, peer);
       const uint32_t swz = hr & 7;
-      auto fetch = [&](int j, float (&s)[kTok]) -> bool {
+      // fetch(j): read this CTA's partial scores of tile j from TMEM, free
+      // the S buffer, send them to the peer and note which keys are valid.
+      auto fetch = [&](int j, float (&s)[kTok], unsigned& valid) -> bool {
         const int sb = j & 1;
+        const int xb = j % kXchBufs;
+        if (hr == 0) mbar_expect_tx(&bars.xch_full[xb], kXchBytes);
+        bool bad = false;
+        valid = __ballot_sync(0xffffffffu, key_slot(p, b, (tile0 + j) * kTok + lane, n_keys, bad) >= 0);
         if (!mbar_wait(&bars.s_full[sb], (j >> 1) & 1, err, &abort_s)) return false;
         tc_fence_after();
         uint32_t v0[16], v1[16];
@@ -425,15 +444,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&bars.s_free[sb]);
-        const int xb = j % kXchBufs;
         const uint32_t dst = xch_peer + xb * kXchBytes + hr * 128;
         const uint32_t rbar = map_peer(smem_u32(&bars.xch_full[xb]), peer);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          st_async_v4(dst + ((static_cast<uint32_t>(i) ^ swz) << 4), make_uint4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]), rbar);
+          st_async_v4(dst + ((static_cast<uint32_t>(i) ^ swz) << 4),
+                      make_uint4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]), rbar);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          st_async_v4(dst + ((static_cast<uint32_t>(i + 4) ^ swz) << 4), make_uint4(v1[4 * i], v1[4 * i + 1], v1[4 * i + 2], v1[4 * i + 3]), rbar);
+          st_async_v4(dst + ((static_cast<uint32_t>(i + 4) ^ swz) << 4),
+                      make_uint4(v1[4 * i], v1[4 * i + 1], v1[4 * i + 2], v1[4 * i + 3]), rbar);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           s[i] = __uint_as_float(v0[i]);
@@ -442,58 +462,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         return true;
       };
 
-      float s_cur[kTok], s_next[kTok];
-      if (hr == 0) mbar_expect_tx(&bars.xch_full[0], kXchBytes);
-      ok = fetch(0, s_cur);
-      for (int j = 0; ok && j < nt; ++j) {
+      // step(j): combine tile j with the peer's partial, online softmax, P(j)
+      // into TMEM; then fetch tile j+2 into the same registers.
+      auto step = [&](int j, float (&s)[kTok], unsigned& valid) -> bool {
         const int pb = j & 1;
         const int xb = j % kXchBufs;
-        if (j + 1 < nt) {
-          if (hr == 0) mbar_expect_tx(&bars.xch_full[(j + 1) % kXchBufs], kXchBytes);
-          if (!fetch(j + 1, s_next)) {
-            ok = false;
-            break;
-          }
-        }
-        // validity of the 32 keys of this tile (lane t checks key t)
-        bool bad = false;
-        const unsigned valid = __ballot_sync(0xffffffffu, key_slot(p, b, (tile0 + j) * kTok + lane, n_keys, bad) >= 0);
-        if (!mbar_wait(&bars.xch_full[xb], (j / kXchBufs) & 1, err, &abort_s)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&bars.xch_full[xb], (j / kXchBufs) & 1, err, &abort_s)) return false;
         const uint8_t* src = sXch + xb * kXchBytes + hr * 128;
         float x[kTok];
-        float mx = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 f = *reinterpret_cast<const float4*>(src + ((static_cast<uint32_t>(i) ^ swz) << 4));
-          x[4 * i] = s_cur[4 * i] + f.x;
-          x[4 * i + 1] = s_cur[4 * i + 1] + f.y;
-          x[4 * i + 2] = s_cur[4 * i + 2] + f.z;
-          x[4 * i + 3] = s_cur[4 * i + 3] + f.w;
+          x[4 * i] = s[4 * i] + f.x;
+          x[4 * i + 1] = s[4 * i + 1] + f.y;
+          x[4 * i + 2] = s[4 * i + 2] + f.z;
+          x[4 * i + 3] = s[4 * i + 3] + f.w;
         }
+        float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kTok; ++c) {
+        for (int c = 0; c < kTok; c += 2) {
           x[c] = ((valid >> c) & 1u) ? x[c] * score_scale : -INFINITY;
-          mx = fmaxf(mx, x[c]);
+          x[c + 1] = ((valid >> (c + 1)) & 1u) ? x[c + 1] * score_scale : -INFINITY;
+          mxa = fmaxf(mxa, x[c]);
+          mxb = fmaxf(mxb, x[c + 1]);
         }
+        const float mx = fmaxf(mxa, mxb);
         float m_use = m_run, alpha = 1.f;
         const bool raise = mx > m_run + kRescaleThreshold;
         if (raise) {
           m_use = mx;
           alpha = exp2f(m_run - mx);
         }
-        // P(j) reuses the buffer PV(j-2) read; O rescale needs PV(j-1) retired
-        if (j >= 2 && !mbar_wait(&bars.pv_done[pb], ((j - 2) >> 1) & 1, err, &abort_s)) {
-          ok = false;
-          break;
-        }
+        // P(j) reuses the buffer PV(j-2) read; an O rescale needs PV(j-1) retired
+        if (j >= 2 && !mbar_wait(&bars.pv_done[pb], ((j - 2) >> 1) & 1, err, &abort_s)) return false;
         if (__any_sync(0xffffffffu, raise && j > 0)) {
-          if (!mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s)) return false;
           tc_fence_after();
 #pragma unroll 4
           for (int c = 0; c < 256; c += 16) {
@@ -507,23 +510,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
           tmem_st_wait();
         }
         m_run = m_use;
-        const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;  // a tile with no valid key so far
-        float lsum = 0.f;
+        const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;  // no valid key so far
+        float la = 0.f, lb = 0.f;
         uint32_t pv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = exp2f(x[2 * i] - m_ref), p1 = exp2f(x[2 * i + 1] - m_ref);
-          lsum += p0 + p1;
+          la += p0;
+          lb += p1;
           pv[i] = pack_bf16(p0, p1);
         }
-        l_run = l_run * alpha + lsum;
+        l_run = l_run * alpha + (la + lb);
         tc_fence_after();
         tmem_st16(tmem + lane_off + col_p(pb), pv);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars.p_full[pb]);
-#pragma unroll
-        for (int c = 0; c < kTok; ++c) s_cur[c] = s_next[c];
+        if (j + 2 < nt) return fetch(j + 2, s, valid);
+        return true;
+      };
+
+      float s_a[kTok], s_b[kTok];
+      unsigned valid_a = 0, valid_b = 0;
+      ok = fetch(0, s_a, valid_a);
+      if (ok && nt > 1) ok = fetch(1, s_b, valid_b);
+      for (int j = 0; ok && j < nt; j += 2) {
+        ok = step(j, s_a, valid_a);
+        if (ok && j + 1 < nt) ok = step(j + 1, s_b, valid_b);
       }
       if (ok) ok = mbar_wait(&bars.o_full, 0, err, &abort_s);
     }

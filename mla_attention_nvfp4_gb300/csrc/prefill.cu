@@ -18,7 +18,8 @@
 //                 S_j = Q K_j^T       M=128 N=128 K=192, A and B from smem
 //                 O  += P_j V_j       M=128 N=128 K=128, A (P) from TMEM,
 //                                     B = V tile read MN-major
-//   warps 2..5  softmax, O correction and epilogue; thread = query row.
+//   warps 2..9  softmax, O correction and epilogue: two warpgroups, each
+//               thread one query row and one half (64 columns) of S and O.
 // TMEM columns: S double buffer [0,128) [128,256); O [256,384).  P_j (bf16)
 // overwrites the first 64 columns of its S buffer after the row is read.
 // The running max is only raised when a row's max grows by more than 8
@@ -39,7 +40,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128, kBN = 128, kDqk = 192, kDv = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kQBytes = kBM * kDqk * 2;  // 49152
 constexpr uint32_t kKBytes = kBN * kDqk * 2;  // 49152
 constexpr uint32_t kVBytes = kBN * kDv * 2;   // 32768
@@ -76,6 +77,7 @@ struct alignas(8) Barriers {
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, o_full;
+  uint64_t red[2], red_l;  // the two softmax groups exchanging row maxima / sums
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -85,6 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
+  __shared__ float red_s[2][2][kBM];  // per-group row maxima, double-buffered by tile parity
+  __shared__ float red_l[2][kBM];     // per-group row sums
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y, seq = blockIdx.z;
@@ -122,10 +126,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.p_full[s], 128);
+      mbar_init(&bars.p_full[s], 256);
     }
     mbar_init(&bars.pv_done, 1);
     mbar_init(&bars.o_full, 1);
+    mbar_init(&bars.red[0], 256);
+    mbar_init(&bars.red[1], 256);
+    mbar_init(&bars.red_l, 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -216,10 +223,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
+    // Two warpgroups share each row: group g handles score columns
+    // [64g, 64g+64) and output columns [64g, 64g+64).  Row maxima and sums
+    // are combined through shared memory.
+    const int g = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int qi = row0 + r;         // query index within the sequence
+    const int c0 = 64 * g;           // first score / output column of this group
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -230,31 +242,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float x[kBN];
+      float x[64];
 #pragma unroll
-      for (int c = 0; c < kBN; c += 16) {
+      for (int c = 0; c < 64; c += 16) {
         uint32_t v[16];
-        tmem_ld16(tS[b] + lane_off + c, v);
-        tmem_ld_wait();
+        tmem_ld16(tS[b] + lane_off + c0 + c, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
       }
-      const int key0 = j * kBN;
-      float mx = -INFINITY;
-      if (key0 + kBN - 1 > qi) {  // diagonal tile: mask keys after the query
+      tmem_ld_wait();
+      const int key0 = j * kBN + c0;
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (key0 + 63 > qi) {  // diagonal tile: mask keys after the query
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
+        for (int c = 0; c < 64; ++c) {
           x[c] = (key0 + c <= qi) ? x[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
+          mq[c & 3] = fmaxf(mq[c & 3], x[c]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
+        for (int c = 0; c < 64; ++c) {
           x[c] *= p.scale_log2;
-          mx = fmaxf(mx, x[c]);
+          mq[c & 3] = fmaxf(mq[c & 3], x[c]);
         }
       }
-      // lazy reference update
+      // row max over both halves (also orders every S read before any P write)
+      red_s[b][g][r] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      mbar_arrive(&bars.red[b]);
+      if (!mbar_wait(&bars.red[b], ph, err, &abort_s)) {
+        ok = false;
+        break;
+      }
+      const float mx = fmaxf(red_s[b][0][r], red_s[b][1][r]);
+      // lazy reference update (identical in both groups)
       float m_use = m_run, alpha = 1.f;
       const bool raise = mx > m_run + kRescaleThreshold;
       if (raise) {
@@ -270,73 +290,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kDv; c += 16) {
+        for (int c = 0; c < 64; c += 16) {
           uint32_t v[16];
-          tmem_ld16(tO + lane_off + c, v);
+          tmem_ld16(tO + lane_off + c0 + c, v);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st16(tO + lane_off + c, v);
+          tmem_st16(tO + lane_off + c0 + c, v);
         }
         tmem_st_wait();
       }
       m_run = m_use;
-      float lsum = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kBN; c += 32) {  // P as bf16 pairs over the first 64 columns of S
+      for (int c = 0; c < 64; c += 32) {  // P as bf16 pairs: columns [32g, 32g+32) of the S buffer
         uint32_t v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = exp2f(x[c + 2 * i] - m_use), p1 = exp2f(x[c + 2 * i + 1] - m_use);
-          lsum += p0 + p1;
+          ls[i & 3] += p0 + p1;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           v[i] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        tmem_st16(tS[b] + lane_off + c / 2, v);
+        tmem_st16(tS[b] + lane_off + 32 * g + c / 2, v);
       }
-      l_run = l_run * alpha + lsum;
+      l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[b]);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && mbar_wait(&bars.o_full, 0, err, &abort_s)) {
+      red_l[g][r] = l_run;
       tc_fence_after();
-      float o[kDv];
+      float o[64];
 #pragma unroll
-      for (int c = 0; c < kDv; c += 16) {
+      for (int c = 0; c < 64; c += 16) {
         uint32_t v[16];
-        tmem_ld16(tO + lane_off + c, v);
-        tmem_ld_wait();
+        tmem_ld16(tO + lane_off + c0 + c, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[c + i] = __uint_as_float(v[i]);
       }
+      tmem_ld_wait();
+      mbar_arrive(&bars.red_l);
+      mbar_wait(&bars.red_l, 0, err, &abort_s);
+      const float l_tot = red_l[0][r] + red_l[1][r];
       if (qi < n) {
         const int64_t m = seq_begin + qi;
-        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
 #pragma unroll
-        for (int c = 0; c < kDv; ++c) o[c] *= inv_l;
+        for (int c = 0; c < 64; ++c) o[c] *= inv_l;
         const bool gs_ok = scale_ok(gs);
-        uint32_t w[16];
-        uint32_t sb[8];
+        uint32_t w[8];
+        uint32_t sb[4];
 #pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
+        for (int blk = 0; blk < 4; ++blk) {
           float S = 0.f;
           sb[blk] = gs_ok ? block_scale(fmaxf(amax8(o + 16 * blk), amax8(o + 16 * blk + 8)), gs, S) : 0u;
           w[2 * blk] = gs_ok ? encode8(o + 16 * blk, S) : 0u;
           w[2 * blk + 1] = gs_ok ? encode8(o + 16 * blk + 8, S) : 0u;
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + h * 64);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        const int64_t kc = static_cast<int64_t>(h) * 8;
+        uint4* dst = reinterpret_cast<uint4*>(p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + h * 64 + 32 * g);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        const int64_t kc = static_cast<int64_t>(h) * 8 + 4 * g;
         *reinterpret_cast<uint32_t*>(p.scales + sf_offset(m, kc, k_tiles_sf)) =
             sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
-        *reinterpret_cast<uint32_t*>(p.scales + sf_offset(m, kc + 4, k_tiles_sf)) =
-            sb[4] | (sb[5] << 8) | (sb[6] << 16) | (sb[7] << 24);
-        if (p.lse != nullptr)
-          p.lse[static_cast<int64_t>(h) * p.total + m] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-        if (!gs_ok && qi == 0) flag_error(err, MLA_DEVERR_SCALE);
+        if (g == 0 && p.lse != nullptr)
+          p.lse[static_cast<int64_t>(h) * p.total + m] = l_tot > 0.f ? (m_run + log2f(l_tot)) * kLn2 : -INFINITY;
+        if (!gs_ok && qi == 0 && g == 0) flag_error(err, MLA_DEVERR_SCALE);
       }
     }
   }

@@ -232,6 +232,11 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t k, ui
 namespace mla {
 namespace sm100 {
 
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
