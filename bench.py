@@ -162,7 +162,12 @@ def run_ours(args, rank, world):
 
     # --- workload (device-resident), seed 0 -----------------------------
     w = workloads.decode_dsv3(device=dev)
-    p = workloads.prefill_8x4096(device=dev)
+    if args.case == "profile":
+        # the same legs on a prefill of 2 x 4096 tokens (about 1.8 GB on the
+        # device in all), for ncu captures; never a bench value
+        p = workloads.prefill("prefill_2x4096", seq_lens=(4096, 4096), device=dev)
+    else:
+        p = workloads.prefill_8x4096(device=dev)
     gs = mla.mla_nvfp4_global_scale(w.kv_c)
     gsp = mla.mla_nvfp4_global_scale(p.v)
     cache = torch.zeros((w.num_slots, w.record_bytes), dtype=torch.uint8, device=dev)
@@ -387,6 +392,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--case", default="full", choices=["full", "profile"],
+                    help="profile: smaller prefill input for ncu captures (not a bench value)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -409,6 +416,8 @@ def main():
         cpu_line = {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                     "sample": sample}
     line = run_ours(args, rank, world)
+    if args.case != "full":
+        line["config"]["workload"] = "PROFILE CASE (prefill 2x4096), not a bench value: " + WORKLOAD
     if rank == 0:
         line["cpu_baseline"] = cpu_line
         print(json.dumps(line))

@@ -54,7 +54,7 @@ constexpr int kTok = 32;           // keys per tile
 constexpr int kHeads = 128;        // heads per work unit (MMA M)
 constexpr int kThreads = 320;
 constexpr int kRawStride = 224;    // bytes per key in the raw ring (208 used)
-constexpr int kRawStages = 4;
+constexpr int kRawStages = 6;
 constexpr int kKvStages = 3;
 constexpr int kXchBufs = 4;
 constexpr uint32_t kRawBytes = kTok * kRawStride;         // 7168
@@ -110,25 +110,32 @@ struct alignas(8) Barriers {
   uint64_t o_full;
 };
 
-// Slot of key position t of sequence b; -1 if padding or out of range.
-__device__ __forceinline__ int64_t key_slot(const Params& p, int b, int t, int n_keys, bool& bad) {
+// Key addressing in two halves so that the index load can be issued tiles
+// ahead of its use: load_index() performs one unconditional, in-bounds load
+// (the page-table entry or the top-k index of key position t, clamped into
+// its row); key_slot() then turns that value into a slot id, or -1 for
+// padding / positions past the sequence, and notes out-of-range ids.
+__device__ __forceinline__ int32_t load_index(const Params& p, int b, int t) {
+  if (p.topk != nullptr) {
+    const int tc = min(max(t, 0), max(p.topk_n - 1, 0));
+    return p.topk[static_cast<int64_t>(b) * p.topk_n + tc];
+  }
+  const int pi = min(max(t, 0) / p.page_size, static_cast<int>(p.pt_stride) - 1);
+  return p.page_table[static_cast<int64_t>(b) * p.pt_stride + pi];
+}
+
+__device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t, int n_keys, bool& bad) {
   if (t >= n_keys) return -1;
   int64_t slot;
   if (p.topk != nullptr) {
-    slot = p.topk[static_cast<int64_t>(b) * p.topk_n + t];
-    if (slot < 0) return -1;
+    if (idx < 0) return -1;  // padding entry
+    slot = idx;
   } else {
-    const int pi = t / p.page_size;
-    if (pi >= p.pt_stride) {
+    if (t / p.page_size >= p.pt_stride || idx < 0) {
       bad = true;
       return -1;
     }
-    const int page = p.page_table[static_cast<int64_t>(b) * p.pt_stride + pi];
-    if (page < 0) {
-      bad = true;
-      return -1;
-    }
-    slot = static_cast<int64_t>(page) * p.page_size + t % p.page_size;
+    slot = static_cast<int64_t>(idx) * p.page_size + t % p.page_size;
   }
   if (slot >= p.num_slots) {
     bad = true;
@@ -232,17 +239,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Slot ids are fetched two tiles ahead so their latency stays off the
-    // copy-issue path.
+    // Index loads run two tiles ahead of their use.
     bool bad = false;
-    int64_t slot_a = nt > 0 ? key_slot(p, b, tile0 * kTok + lane, n_keys, bad) : -1;
-    int64_t slot_b = nt > 1 ? key_slot(p, b, (tile0 + 1) * kTok + lane, n_keys, bad) : -1;
+    int32_t idx_a = nt > 0 ? load_index(p, b, tile0 * kTok + lane) : -1;
+    int32_t idx_b = nt > 1 ? load_index(p, b, (tile0 + 1) * kTok + lane) : -1;
     for (int j = 0; j < nt; ++j) {
       const int st = j % kRawStages;
       const uint32_t ph = (j / kRawStages) & 1;
-      const int64_t slot = slot_a;
-      slot_a = slot_b;
-      slot_b = (j + 2 < nt) ? key_slot(p, b, (tile0 + j + 2) * kTok + lane, n_keys, bad) : -1;
+      const int32_t idx = idx_a;
+      idx_a = idx_b;
+      if (j + 2 < nt) idx_b = load_index(p, b, (tile0 + j + 2) * kTok + lane);
+      const int64_t slot = key_slot(p, idx, (tile0 + j) * kTok + lane, n_keys, bad);
       if (!mbar_wait(&bars.raw_empty[st], ph ^ 1, err, &abort_s)) break;
       const unsigned vmask = __ballot_sync(0xffffffffu, slot >= 0);
       if (slot >= 0) {
@@ -430,12 +437,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       const uint32_t swz = hr & 7;
       // fetch(j): read this CTA's partial scores of tile j from TMEM, free
       // the S buffer, send them to the peer and note which keys are valid.
-      auto fetch = [&](int j, float (&s)[kTok], unsigned& valid) -> bool {
+      auto fetch = [&](int j, float (&s)[kTok], int32_t& idx) -> bool {
         const int sb = j & 1;
         const int xb = j % kXchBufs;
         if (hr == 0) mbar_expect_tx(&bars.xch_full[xb], kXchBytes);
-        bool bad = false;
-        valid = __ballot_sync(0xffffffffu, key_slot(p, b, (tile0 + j) * kTok + lane, n_keys, bad) >= 0);
+        idx = load_index(p, b, (tile0 + j) * kTok + lane);  // consumed two steps later
         if (!mbar_wait(&bars.s_full[sb], (j >> 1) & 1, err, &abort_s)) return false;
         tc_fence_after();
         uint32_t v0[16], v1[16];
@@ -464,9 +470,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 
       // step(j): combine tile j with the peer's partial, online softmax, P(j)
       // into TMEM; then fetch tile j+2 into the same registers.
-      auto step = [&](int j, float (&s)[kTok], unsigned& valid) -> bool {
+      auto step = [&](int j, float (&s)[kTok], int32_t& idx) -> bool {
         const int pb = j & 1;
         const int xb = j % kXchBufs;
+        bool bad = false;
+        const unsigned valid = __ballot_sync(0xffffffffu, key_slot(p, idx, (tile0 + j) * kTok + lane, n_keys, bad) >= 0);
         if (!mbar_wait(&bars.xch_full[xb], (j / kXchBufs) & 1, err, &abort_s)) return false;
         const uint8_t* src = sXch + xb * kXchBytes + hr * 128;
         float x[kTok];
@@ -526,17 +534,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars.p_full[pb]);
-        if (j + 2 < nt) return fetch(j + 2, s, valid);
+        if (j + 2 < nt) return fetch(j + 2, s, idx);
         return true;
       };
 
       float s_a[kTok], s_b[kTok];
-      unsigned valid_a = 0, valid_b = 0;
-      ok = fetch(0, s_a, valid_a);
-      if (ok && nt > 1) ok = fetch(1, s_b, valid_b);
+      int32_t idx_a = -1, idx_b = -1;
+      ok = fetch(0, s_a, idx_a);
+      if (ok && nt > 1) ok = fetch(1, s_b, idx_b);
       for (int j = 0; ok && j < nt; j += 2) {
-        ok = step(j, s_a, valid_a);
-        if (ok && j + 1 < nt) ok = step(j + 1, s_b, valid_b);
+        ok = step(j, s_a, idx_a);
+        if (ok && j + 1 < nt) ok = step(j + 1, s_b, idx_b);
       }
       if (ok) ok = mbar_wait(&bars.o_full, 0, err, &abort_s);
     }
