@@ -14,8 +14,10 @@
 //   x_hat = e2m1(code) * e4m3(scale) * gs,   out = sum_j softmax(s)_j x_hat_j.
 //
 // The global scale gs is folded out of the tensor-core operands: the key
-// tile holds c*s (exact in bf16), the query tile holds [q_lat, q_pe / gs],
-// the product is multiplied by softmax_scale * gs, and the output by gs.
+// tile holds c*s (exact in f16) and k_pe (bf16), the query tile holds
+// [sigma*q_lat (f16), sigma*q_pe/gs (bf16)] with sigma a per-head power of
+// two keeping sigma*q_lat inside the f16 range, the product is multiplied by
+// softmax_scale*gs/sigma, and the output by gs.
 //
 // Work unit = (sequence b, split, group of up to 128 heads), run by a
 // cluster of two CTAs.  CTA r owns latent features [256r, 256r+256) and RoPE
@@ -34,7 +36,8 @@
 //                 S_j  = Q_half . K_j^T   M=128 N=32 K=288, Q from TMEM
 //                 O   += P_j . V_j        M=128 N=256 K=32, P from TMEM,
 //                                         V = the latent tile read MN-major
-//   warps 2..5  dequantise raw records into 128-byte-swizzled bf16 tiles.
+//   warps 2..5  dequantise raw records into 128-byte-swizzled tiles: latent
+//               c*s in f16 (one cvt + one multiply per pair), RoPE in bf16.
 //   warps 6..9  Q staging, partial-score exchange, online softmax, O
 //               correction and the partial-output epilogue; thread = head.
 #include <cuda_runtime.h>
@@ -74,8 +77,12 @@ __host__ __device__ constexpr uint32_t col_s(int buf) { return 160u + 32u * buf;
 __host__ __device__ constexpr uint32_t col_p(int buf) { return 224u + 16u * buf; }  // P bf16 pairs, 16 cols
 constexpr uint32_t kTO = 256;                // O half, 256 columns
 
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTok, false, false);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
+// Latent products run on f16 operands (c*s is exact in f16; Q is scaled per
+// row by a power of two so that it cannot overflow f16); the RoPE K-steps
+// run as separate bf16 MMAs into the same accumulator.
+constexpr uint32_t kIdescQKLat = idesc_f16_f32(128, kTok, false, false);
+constexpr uint32_t kIdescQKRope = idesc_bf16_f32(128, kTok, false, false);
+constexpr uint32_t kIdescPV = idesc_f16_f32(128, 256, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -168,7 +175,7 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&z);
 }
 
-// f16x2 -> bf16x2; exact for the values used here (at most 8 significant bits).
+// f16x2 -> bf16x2; exact for e4m3 values (4 significant bits).
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
   const __half2 x = *reinterpret_cast<const __half2*>(&h);
   const float2 f = __half22float2(x);
@@ -306,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 #pragma unroll
         for (int kk = 0; kk < 18; ++kk) {
           const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * kKvBlock + (kk & 3) * 32, 0, 1024);
-          mma_ts(tmem + col_s(sb), tmem + kTQ + kk * 8, bd, kIdescQK, kk > 0 ? 1u : 0u);
+          mma_ts(tmem + col_s(sb), tmem + kTQ + kk * 8, bd, kk < 16 ? kIdescQKLat : kIdescQKRope, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.s_full[sb]);
         return true;
@@ -352,7 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
             e2m1x8_to_f16x8(words[2 * blk + hw], h);
             uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = f16x2_to_bf16x2(hmul2_u32(h[i], s2));
+            for (int i = 0; i < 4; ++i) o[i] = hmul2_u32(h[i], s2);  // c*s, exact in f16
             outv[2 * blk + hw] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
@@ -390,13 +397,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float gs = *p.gs;
     const bool gs_ok = scale_ok(gs);
-    const float score_scale = p.softmax_scale * gs * kLog2e;
+    float score_scale = p.softmax_scale * gs * kLog2e;
     bool ok = true;
     float m_run = -INFINITY, l_run = 0.f;
     if (nt > 0) {
-      // Q half -> TMEM: [q_lat[256r : 256r+256], q_pe[32r : 32r+32] / gs] as bf16 pairs
+      // Q half -> TMEM: [sigma*q_lat[256r : 256r+256] as f16 pairs,
+      //                  sigma*q_pe[32r : 32r+32]/gs as bf16 pairs]
       const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(b) * p.num_heads + head) * 576;
       const float inv_gs = gs_ok ? 1.f / gs : 0.f;
+      float qmax = 0.f;  // over the whole latent row, so both CTAs pick the same sigma
+      if (head_ok) {
+#pragma unroll 4
+        for (int i = 0; i < 64; ++i) {
+          const uint4 w = reinterpret_cast<const uint4*>(qrow)[i];
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float lo, hi;
+            bf16x2_to_f32(ws[k], lo, hi);
+            qmax = fmaxf(qmax, fmaxf(fabsf(lo), fabsf(hi)));
+          }
+        }
+      }
+      // sigma = 2^-a with sigma*qmax < 2^16 (f16 max 65504)
+      const int qexp = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFFu) - 127;
+      const int a_sh = max(0, min(qexp - 14, 100));
+      const float sigma = __uint_as_float(static_cast<uint32_t>(127 - a_sh) << 23);
+      score_scale *= __uint_as_float(static_cast<uint32_t>(127 + a_sh) << 23);
 #pragma unroll
       for (int c = 0; c < 144; c += 16) {
         uint32_t v[16];
@@ -406,10 +433,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const uint4 w = src[i];
-              v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float lo, hi;
+                bf16x2_to_f32(ws[k], lo, hi);
+                __half2 h2 = __floats2half2_rn(lo * sigma, hi * sigma);
+                v[4 * i + k] = *reinterpret_cast<uint32_t*>(&h2);
+              }
             }
           } else {
             const uint4* src = reinterpret_cast<const uint4*>(qrow + 512 + 32 * rank);
+            const float f = inv_gs * sigma;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const uint4 w = src[i];
@@ -418,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
               for (int k = 0; k < 4; ++k) {
                 float lo, hi;
                 bf16x2_to_f32(ws[k], lo, hi);
-                v[4 * i + k] = pack_bf16(lo * inv_gs, hi * inv_gs);
+                v[4 * i + k] = pack_bf16(lo * f, hi * f);
               }
             }
           }
@@ -486,20 +521,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
           x[4 * i + 2] = s[4 * i + 2] + f.z;
           x[4 * i + 3] = s[4 * i + 3] + f.w;
         }
-        float mxa = -INFINITY, mxb = -INFINITY;
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (valid == 0xffffffffu) {
 #pragma unroll
-        for (int c = 0; c < kTok; c += 2) {
-          x[c] = ((valid >> c) & 1u) ? x[c] * score_scale : -INFINITY;
-          x[c + 1] = ((valid >> (c + 1)) & 1u) ? x[c + 1] * score_scale : -INFINITY;
-          mxa = fmaxf(mxa, x[c]);
-          mxb = fmaxf(mxb, x[c + 1]);
+          for (int c = 0; c < kTok; ++c) {
+            x[c] *= score_scale;
+            mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTok; ++c) {
+            x[c] = ((valid >> c) & 1u) ? x[c] * score_scale : -INFINITY;
+            mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+          }
         }
-        const float mx = fmaxf(mxa, mxb);
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         float m_use = m_run, alpha = 1.f;
         const bool raise = mx > m_run + kRescaleThreshold;
         if (raise) {
           m_use = mx;
-          alpha = exp2f(m_run - mx);
+          alpha = ex2_approx(m_run - mx);
         }
         // P(j) reuses the buffer PV(j-2) read; an O rescale needs PV(j-1) retired
         if (j >= 2 && !mbar_wait(&bars.pv_done[pb], ((j - 2) >> 1) & 1, err, &abort_s)) return false;
@@ -519,16 +560,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         }
         m_run = m_use;
         const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;  // no valid key so far
-        float la = 0.f, lb = 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = exp2f(x[2 * i] - m_ref), p1 = exp2f(x[2 * i + 1] - m_ref);
-          la += p0;
-          lb += p1;
-          pv[i] = pack_bf16(p0, p1);
+          const float p0 = ex2_approx(x[2 * i] - m_ref), p1 = ex2_approx(x[2 * i + 1] - m_ref);
+          ls[i & 3] += p0 + p1;
+          __half2 h2 = __floats2half2_rn(p0, p1);  // P <= 2^8 (lazy reference), f16 operand
+          pv[i] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        l_run = l_run * alpha + (la + lb);
+        l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         tc_fence_after();
         tmem_st16(tmem + lane_off + col_p(pb), pv);
         tmem_st_wait();

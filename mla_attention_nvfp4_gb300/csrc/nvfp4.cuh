@@ -8,11 +8,14 @@
 // global amax/(6*448)).
 //
 // Float32 operation order of one block (every op IEEE round-to-nearest, no
-// contraction):
-//     s_raw = (amax16 / 6) / gs
+// contraction; reciprocals instead of divisions, as NVFP4 quantisers
+// usually do):
+//     k     = 1 / (6 * gs)                       once per tensor
+//     s_raw = amax16 * k
 //     sb    = e4m3 RNE-satfinite(s_raw)
 //     S     = e4m3(sb) * gs
-//     code  = e2m1 RNE-satfinite(x / S), all codes 0 when S is 0 or not finite
+//     code  = e2m1 RNE-satfinite(x * (1 / S)), all codes 0 when S is 0
+// A global scale outside [2^-100, 2^100] is invalid (codes and scales 0).
 // The conversions use the sm_100-family cvt instructions, which round to
 // nearest even and clamp to the largest finite value (448, 6).
 #pragma once
@@ -68,25 +71,30 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
-__device__ __forceinline__ bool scale_ok(float gs) { return gs > 0.f && gs <= 3.0e38f; }
+__device__ __forceinline__ bool scale_ok(float gs) {
+  return gs >= 7.888609052210118e-31f && gs <= 1.2676506002282294e30f;  // [2^-100, 2^100]
+}
 
-// Block scale from the block's amax (amax is exact in any reduction order).
-// Returns the scale byte sb and sets S = e4m3(sb) * gs, or S = 0 when that
-// product is 0 or not finite (the block then encodes as all-zero codes).
-__device__ __forceinline__ uint32_t block_scale(float amax, float gs, float& S) {
-  const float s_raw = __fdiv_rn(__fdiv_rn(amax, 6.0f), gs);
-  const uint32_t sb = cvt_e4m3(s_raw);
-  S = __fmul_rn(e4m3_to_f32(sb), gs);
-  if (!(S > 0.f) || !(S <= 3.0e38f)) S = 0.f;
+// k = 1 / (6 * gs): the per-tensor factor of the raw block scale.
+__device__ __forceinline__ float scale_factor(float gs) { return __frcp_rn(__fmul_rn(6.0f, gs)); }
+
+// Block scale from the block's amax (amax is exact in any reduction order)
+// and k = scale_factor(gs).  Returns the scale byte sb and sets R = 1 / S
+// with S = e4m3(sb) * gs, or R = 0 when S is 0 (the block then encodes as
+// all-zero codes).
+__device__ __forceinline__ uint32_t block_scale(float amax, float k, float gs, float& R) {
+  const uint32_t sb = cvt_e4m3(__fmul_rn(amax, k));
+  const float S = __fmul_rn(e4m3_to_f32(sb), gs);
+  R = (S > 0.f) ? __frcp_rn(S) : 0.f;
   return sb;
 }
 
-// Eight codes of x / S (element i in nibble i); all zero when S == 0.
-__device__ __forceinline__ uint32_t encode8(const float* x, float S) {
-  if (S == 0.f) return 0u;
+// Eight codes of x * R (element i in nibble i); all zero when R == 0.
+__device__ __forceinline__ uint32_t encode8(const float* x, float R) {
+  if (R == 0.f) return 0u;
   float q[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], S);
+  for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], R);
   return cvt_e2m1x8(q);
 }
 

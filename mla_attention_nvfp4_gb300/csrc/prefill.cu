@@ -341,14 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) o[c] *= inv_l;
         const bool gs_ok = scale_ok(gs);
+        const float kf = scale_factor(gs);
         uint32_t w[8];
         uint32_t sb[4];
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-          float S = 0.f;
-          sb[blk] = gs_ok ? block_scale(fmaxf(amax8(o + 16 * blk), amax8(o + 16 * blk + 8)), gs, S) : 0u;
-          w[2 * blk] = gs_ok ? encode8(o + 16 * blk, S) : 0u;
-          w[2 * blk + 1] = gs_ok ? encode8(o + 16 * blk + 8, S) : 0u;
+          float R = 0.f;
+          sb[blk] = gs_ok ? block_scale(fmaxf(amax8(o + 16 * blk), amax8(o + 16 * blk + 8)), kf, gs, R) : 0u;
+          w[2 * blk] = gs_ok ? encode8(o + 16 * blk, R) : 0u;
+          w[2 * blk + 1] = gs_ok ? encode8(o + 16 * blk + 8, R) : 0u;
         }
         uint4* dst = reinterpret_cast<uint4*>(p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + h * 64 + 32 * g);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const float gs = *gs_ptr;
   const bool gs_valid = scale_ok(gs);
+  const float k = scale_factor(gs);
   if (!gs_valid && warp == 0 && lane == 0) flag_error(error_word, MLA_DEVERR_SCALE);
 
   for (int64_t t = warp; t < num_tokens; t += n_warps) {
@@ -69,11 +70,11 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     am_b = fmaxf(am_b, __shfl_xor_sync(0xffffffffu, am_b, 1));
     uint32_t code_a = 0, code_b = 0, sb_a = 0, sb_b = 0;
     if (gs_valid) {
-      float Sa, Sb;
-      sb_a = block_scale(am_a, gs, Sa);
-      sb_b = block_scale(am_b, gs, Sb);
-      code_a = encode8(xa, Sa);
-      code_b = encode8(xb, Sb);
+      float Ra, Rb;
+      sb_a = block_scale(am_a, k, gs, Ra);
+      sb_b = block_scale(am_b, k, gs, Rb);
+      code_a = encode8(xa, Ra);
+      code_b = encode8(xb, Rb);
     }
     uint8_t* rec = cache + slot * kRecord;
     reinterpret_cast<uint32_t*>(rec)[lane] = code_a;        // bytes [4l, 4l+4)
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restr
   const int64_t m = idx / Kp, k = idx % Kp;
   const float gs = *gs_ptr;
   const bool gs_valid = scale_ok(gs);
+  const float kf = scale_factor(gs);
   if (!gs_valid && idx == 0) flag_error(error_word, MLA_DEVERR_SCALE);
   uint32_t sb = 0;
   if (m < M && k < K) {
@@ -147,10 +149,10 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restr
     }
     uint32_t lo = 0, hi = 0;
     if (gs_valid) {
-      float S;
-      sb = block_scale(fmaxf(amax8(v), amax8(v + 8)), gs, S);
-      lo = encode8(v, S);
-      hi = encode8(v + 8, S);
+      float R;
+      sb = block_scale(fmaxf(amax8(v), amax8(v + 8)), kf, gs, R);
+      lo = encode8(v, R);
+      hi = encode8(v + 8, R);
     }
     *reinterpret_cast<uint2*>(codes + m * (N / 2) + k * 8) = make_uint2(lo, hi);
   }

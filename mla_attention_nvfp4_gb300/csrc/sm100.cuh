@@ -152,14 +152,27 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and an fp32
-// accumulator: D format in bits 4..5 (1 = f32), A format 7..9 and B format
-// 10..12 (1 = bf16), A / B major-ness in bits 15 / 16 (1 = MN-major),
-// N >> 3 in 17..22, M >> 4 in 24..28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+// Instruction descriptor of kind::f16 with an fp32 accumulator: D format in
+// bits 4..5 (1 = f32), A format 7..9 and B format 10..12 (0 = f16, 1 = bf16;
+// A and B always the same type), A / B major-ness in bits 15 / 16
+// (1 = MN-major), N >> 3 in 17..22, M >> 4 in 24..28.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, uint32_t ab_type, bool a_mn, bool b_mn) {
+  return (1u << 4) | (ab_type << 7) | (ab_type << 10) | (static_cast<uint32_t>(a_mn) << 15) |
          (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f32acc(M, N, 1u, a_mn, b_mn);
+}
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f32acc(M, N, 0u, a_mn, b_mn);
+}
+
+// 2^x (approximate, flushes subnormal results to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ------------------------------------------------------------------- MMA

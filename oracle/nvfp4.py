@@ -6,12 +6,18 @@ block scale per 16 elements along the contraction axis, with the global
 scale amax/(6*448).  Codes are e2m1 with magnitudes {0, .5, 1, 1.5, 2, 3, 4,
 6}; the block scale is e4m3(amax16 / 6 / global).
 
-Float32 decision steps (the pages give no precision; the kernels' is used):
+Float32 decision steps (the pages give no precision or evaluation order; the
+kernels' is used, with reciprocals as NVFP4 quantisers usually do):
 
-    s_raw = f32( f32(amax16 / 6) / gs )
+    k     = f32( 1 / f32(6 * gs) )                (once per tensor)
+    s_raw = f32( amax16 * k )
     sb    = e4m3_rne_satfinite(s_raw)
     S     = f32( e4m3(sb) * gs )
-    code  = e2m1_rne_satfinite( f32(x / S) )      (all codes 0 when S == 0)
+    r     = f32( 1 / S )
+    code  = e2m1_rne_satfinite( f32(x * r) )      (all codes 0 when S == 0)
+
+A global scale outside [2^-100, 2^100] (or not finite) is invalid: codes
+and scale bytes are then 0.
 
 Both roundings onto the 8-bit / 4-bit grids are exact round-to-nearest-even
 of the float32 value, computed here in float64, where they are exact.
@@ -105,6 +111,14 @@ def global_scale(amax) -> np.float32:
     return np.float32(np.float32(amax) / np.float32(GLOBAL_SCALE_DIVISOR))
 
 
+GS_MIN, GS_MAX = 2.0 ** -100, 2.0 ** 100
+
+
+def scale_valid(gs) -> bool:
+    g = float(np.float32(gs))
+    return GS_MIN <= g <= GS_MAX
+
+
 def quantize_blocks(x, gs):
     """Quantise rows of 16 float32 values.
 
@@ -116,13 +130,16 @@ def quantize_blocks(x, gs):
     gs = np.float32(gs)
     assert x.shape[-1] % BLOCK == 0
     blocks = x.reshape(x.shape[:-1] + (x.shape[-1] // BLOCK, BLOCK))
+    if not scale_valid(gs):
+        return np.zeros(x.shape, dtype=np.uint8), np.zeros(blocks.shape[:-1], dtype=np.uint8)
+    k = np.float32(np.float32(1.0) / np.float32(np.float32(6.0) * gs))  # IEEE float32 ops
     amax = np.max(np.abs(blocks), axis=-1)  # exact in float32
-    s_raw = (amax / np.float32(6.0)) / gs  # two IEEE float32 divisions
+    s_raw = (amax * k).astype(np.float32)
     sb = e4m3_encode(s_raw.astype(np.float64))
     S = (e4m3_decode(sb).astype(np.float32) * gs).astype(np.float32)
     ok = (S > 0) & np.isfinite(S)
-    safe_S = np.where(ok, S, np.float32(1.0)).astype(np.float32)
-    q = (blocks / safe_S[..., None]).astype(np.float32)  # IEEE float32 division
+    r = (np.float32(1.0) / np.where(ok, S, np.float32(1.0))).astype(np.float32)
+    q = (blocks * r[..., None]).astype(np.float32)
     codes = e2m1_encode(q.astype(np.float64))
     codes = np.where(ok[..., None], codes, np.uint8(0)).astype(np.uint8)
     return codes.reshape(x.shape), sb.astype(np.uint8)
