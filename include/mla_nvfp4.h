@@ -66,6 +66,10 @@ const char* mla_nvfp4_status_string(int status);
 /* MLA_NVFP4_ABI_VERSION of the loaded library. */
 int mla_nvfp4_abi_version(void);
 
+/* The CUDA runtime's message for the last failed launch or attribute call
+ * behind an MLA_ERR_LAUNCH return on the calling host thread ("" if none). */
+const char* mla_nvfp4_last_error(void);
+
 /*
  * Global (outer) scale of a bf16 tensor: *gs = fp32(amax|x| / 2688).
  * Source: "#2244" PR description, "Contract notes" (amax/(6*448)); the

@@ -50,6 +50,7 @@ _c_i64, _c_int, _c_vp, _c_f = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, cty
 _SIGS = {
     "mla_nvfp4_status_string": (ctypes.c_char_p, [_c_int]),
     "mla_nvfp4_abi_version": (_c_int, []),
+    "mla_nvfp4_last_error": (ctypes.c_char_p, []),
     "mla_nvfp4_global_scale": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp]),
     "mla_nvfp4_cache_write": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64,
                                        _c_int, _c_vp, _c_vp, _c_vp]),
@@ -72,7 +73,10 @@ def abi_symbols():
 class MLAError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
-        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        detail = ""
+        if status == 6:  # MLA_ERR_LAUNCH: add the CUDA runtime's message
+            detail = ": " + load_library().mla_nvfp4_last_error().decode()
+        super().__init__(f"{fn}: {status_string(status)} (status {status}){detail}")
 
 
 def load_library(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:

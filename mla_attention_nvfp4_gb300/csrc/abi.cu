@@ -33,7 +33,18 @@ int device_sms() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+thread_local const char* t_last_error = "";
+
 }  // namespace
+
+namespace mla {
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_OK;
+  t_last_error = cudaGetErrorString(e);
+  return MLA_ERR_LAUNCH;
+}
+int launch_status() { return cuda_status(cudaGetLastError()); }
+}  // namespace mla
 
 extern "C" {
 
@@ -51,6 +62,8 @@ const char* mla_nvfp4_status_string(int status) {
 }
 
 int mla_nvfp4_abi_version(void) { return MLA_NVFP4_ABI_VERSION; }
+
+const char* mla_nvfp4_last_error(void) { return t_last_error; }
 
 int mla_nvfp4_global_scale(const void* x, int64_t n, float* gs, void* stream) {
   if (x == nullptr || gs == nullptr || n < 1) return MLA_ERR_INVALID_ARG;

@@ -702,20 +702,18 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int /*num_sms*/) {
   dim3 grid(2 * a.num_splits, a.batch, (a.num_heads + kHeads - 1) / kHeads);
   if (grid.y > 65535u || grid.z > 65535u) return MLA_ERR_INVALID_ARG;
   if (a.record_bytes == 432) {
-    if (cudaFuncSetAttribute(decode_tc_kernel<432>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmAlloc)) != cudaSuccess)
-      return MLA_ERR_LAUNCH;
+    if (const int st = cuda_status(cudaFuncSetAttribute(decode_tc_kernel<432>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmAlloc)))) return st;
     decode_tc_kernel<432><<<grid, kThreads, kSmAlloc, stream>>>(p);
   } else {
-    if (cudaFuncSetAttribute(decode_tc_kernel<368>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmAlloc)) != cudaSuccess)
-      return MLA_ERR_LAUNCH;
+    if (const int st = cuda_status(cudaFuncSetAttribute(decode_tc_kernel<368>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmAlloc)))) return st;
     decode_tc_kernel<368><<<grid, kThreads, kSmAlloc, stream>>>(p);
   }
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (const int st = launch_status()) return st;
   decode_merge_kernel<<<a.batch * a.num_heads, 128, 0, stream>>>(
       p.part_o, p.part_lse, a.num_splits, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+  return launch_status();
 }
 
 }  // namespace mla

@@ -10,6 +10,11 @@
 
 namespace mla {
 
+// Record a CUDA failure for mla_nvfp4_last_error() and map it to a status.
+int cuda_status(cudaError_t e);
+// MLA_OK after a successful launch sequence, else the recorded failure.
+int launch_status();
+
 int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, int64_t pe_stride,
                        const int64_t* slot_mapping, int64_t num_tokens, uint8_t* cache,
                        int64_t num_slots, int record_bytes, const float* gs,

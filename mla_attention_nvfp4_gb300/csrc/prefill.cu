@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tS0 = tmem, tS1 = tmem + 128;
   const uint32_t tO = tmem + 256;
   uint32_t* err = p.error_word;
 
@@ -180,7 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
+      // Descriptors are built once; a K-step only adds its byte offset >> 4
+      // to the start-address field (addresses stay below 256 KB, no carry).
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      const uint64_t dq = smem_desc_sw128(q_addr, 0, 1024);
+      const uint64_t dk0 = smem_desc_sw128(k_addr, 0, 1024), dk1 = smem_desc_sw128(k_addr + kKBytes, 0, 1024);
+      const uint64_t dv0 = smem_desc_sw128(v_addr, 16384, 1024), dv1 = smem_desc_sw128(v_addr + kVBytes, 16384, 1024);
       bool ok = mbar_wait(&bars.q_full, 0, err, &abort_s);
       auto issue_pv = [&](int i) -> bool {
         const int b = i & 1;
@@ -188,12 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars.p_full[b], ph, err, &abort_s)) return false;
         if (!mbar_wait(&bars.v_full[b], ph, err, &abort_s)) return false;
         tc_fence_after();
-        const uint32_t vbase = v_addr + b * kVBytes;
+        const uint64_t vd = b ? dv1 : dv0;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, 16384, 1024);
-          mma_ts(tO, tS[b] + kk * 8, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tO, (b ? tS1 : tS0) + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.v_empty[b]);
         mma_commit(&bars.pv_done);
         return true;
@@ -206,12 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = k_addr + s * kKBytes;
+        const uint64_t kd = s ? dk1 : dk0;
 #pragma unroll
         for (int kk = 0; kk < kDqk / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS[s], smem_desc_sw128(q_addr + off, 0, 1024), smem_desc_sw128(kbase + off, 0, 1024), kIdescS,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(s ? tS1 : tS0, dq + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.s_full[s]);
         mma_commit(&bars.k_empty[s]);
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 64; c += 16) {
         uint32_t v[16];
-        tmem_ld16(tS[b] + lane_off + c0 + c, v);
+        tmem_ld16((b ? tS1 : tS0) + lane_off + c0 + c, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
       }
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           v[i] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        tmem_st16(tS[b] + lane_off + 32 * g + c / 2, v);
+        tmem_st16((b ? tS1 : tS0) + lane_off + 32 * g + c / 2, v);
       }
       l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       tmem_st_wait();
@@ -423,13 +425,12 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int /*num_sms*/) {
   p.scales = a.out_scales;
   p.lse = a.lse;
   p.error_word = a.error_word;
-  if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemAlloc)) != cudaSuccess)
-    return MLA_ERR_LAUNCH;
+  if (const int st = cuda_status(cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemAlloc)))) return st;
   dim3 grid(p.q_tiles, a.num_heads, a.num_seqs);
   if (grid.y > 65535u || grid.z > 65535u) return MLA_ERR_INVALID_ARG;
   prefill_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+  return launch_status();
 }
 
 }  // namespace mla

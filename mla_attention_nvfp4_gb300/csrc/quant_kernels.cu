@@ -115,7 +115,7 @@ int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, in
   else
     cache_write_kernel<false><<<grid, 256, 0, stream>>>(kv, kv_stride, pe, pe_stride, slot_mapping,
                                                         num_tokens, cache, num_slots, gs, error_word);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+  return launch_status();
 }
 
 // ---------------------------------------------------------------------------
@@ -168,7 +168,7 @@ int launch_quantize_rows(const float* x, int64_t M, int64_t N, const float* gs, 
   if (grid > 0x7fffffff) return MLA_ERR_INVALID_ARG;
   quantize_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(x, M, N, gs, codes, scales,
                                                                          error_word);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+  return launch_status();
 }
 
 // ---------------------------------------------------------------------------
@@ -206,14 +206,14 @@ __global__ void finalize_scale_kernel(float* gs) {
 }
 
 int launch_global_scale(const void* x, int64_t n, float* gs, cudaStream_t stream, int num_sms) {
-  if (cudaMemsetAsync(gs, 0, sizeof(float), stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (const int st = cuda_status(cudaMemsetAsync(gs, 0, sizeof(float), stream))) return st;
   const int64_t want = (n / 8 + 255) / 256 + 1;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   const int grid = static_cast<int>(want < cap ? want : cap);
   amax_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), n,
                                         reinterpret_cast<uint32_t*>(gs));
   finalize_scale_kernel<<<1, 1, 0, stream>>>(gs);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_LAUNCH;
+  return launch_status();
 }
 
 }  // namespace mla
