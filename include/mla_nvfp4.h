@@ -12,7 +12,9 @@
  * Conventions for every entry point:
  *  - All pointers are DEVICE pointers unless stated otherwise.  The caller
  *    owns every buffer (including decode workspace); the library allocates
- *    nothing and keeps no state between calls.
+ *    nothing and keeps no state between calls, except that
+ *    mla_nvfp4_decode_noalloc uses a fixed scratch area compiled into the
+ *    library (see there).
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
  *    enqueued asynchronously; the return value covers host-side argument
  *    checks and the launch only.
@@ -142,6 +144,53 @@ int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cac
                      const int32_t* topk_indices, int topk, float softmax_scale,
                      const float* global_scale, void* out, float* lse, void* workspace,
                      size_t workspace_bytes, int num_splits, uint32_t* error_word, void* stream);
+
+/* Largest decode the library's built-in scratch holds: batch * splits *
+ * num_heads partial rows, and the bytes those rows take (the value of
+ * mla_nvfp4_decode_workspace_size for that many rows). */
+#define MLA_DECODE_STATIC_ROWS 16384
+#define MLA_DECODE_STATIC_WORKSPACE_BYTES 33619968u /* 16384*2048 + 65536 */
+
+/*
+ * mla_nvfp4_decode without a caller workspace.  The pages describe no such
+ * entry point; it exists for callers that cannot hand the library device
+ * memory for each call: a serving engine that has given all free device
+ * memory to its paged KV-cache pool at start-up, a host program in another
+ * language with no device allocator of its own, or a decode step that must
+ * not call cudaMalloc/cudaFree because those calls synchronise the device.
+ * It takes the same arguments as mla_nvfp4_decode minus workspace and
+ * workspace_bytes, and computes the same result with the same kernels.
+ *
+ *   Scratch      : the split partials live in a file-scope __device__ array
+ *                  of MLA_DECODE_STATIC_WORKSPACE_BYTES bytes (one copy per
+ *                  device, 256-byte aligned).  The call allocates nothing:
+ *                  no cudaMalloc, no cudaFree, no allocating library call.
+ *                  Nothing in the scratch needs to start at zero: every
+ *                  call writes each partial row before its merge reads it.
+ *   Limit        : batch * num_splits * num_heads (num_splits after the
+ *                  default for <= 0 is applied) must not exceed
+ *                  MLA_DECODE_STATIC_ROWS; larger calls return
+ *                  MLA_ERR_WORKSPACE without launching, and
+ *                  mla_nvfp4_last_error() names the row count and the limit.
+ *                  Pass fewer splits or use mla_nvfp4_decode.
+ *   First call   : the first call on a device, with that device current,
+ *                  looks up the scratch's device address
+ *                  (cudaGetSymbolAddress, which may load the library's
+ *                  device code) and keeps it for later calls on that
+ *                  device; make that first call before any stream capture
+ *                  begins.  A failed lookup returns MLA_ERR_LAUNCH.
+ *   Concurrency  : all calls on one device share the one scratch, so calls
+ *                  whose work may overlap on the device (different
+ *                  streams, or several host threads without ordering) race
+ *                  and give wrong results.  Calls enqueued on one stream
+ *                  run in order and are safe.
+ */
+int mla_nvfp4_decode_noalloc(const void* q, int batch, int num_heads, const uint8_t* cache,
+                             int64_t num_slots, int record_bytes, const int32_t* page_table,
+                             int64_t page_table_stride, int page_size, const int32_t* seq_lens,
+                             const int32_t* topk_indices, int topk, float softmax_scale,
+                             const float* global_scale, void* out, float* lse, int num_splits,
+                             uint32_t* error_word, void* stream);
 
 /*
  * Causal varlen MLA prefill whose epilogue writes NVFP4 directly.

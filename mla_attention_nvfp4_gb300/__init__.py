@@ -58,6 +58,9 @@ _SIGS = {
     "mla_nvfp4_decode": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64, _c_int,
                                   _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp, _c_vp,
                                   ctypes.c_size_t, _c_int, _c_vp, _c_vp]),
+    "mla_nvfp4_decode_noalloc": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64,
+                                          _c_int, _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp,
+                                          _c_int, _c_vp, _c_vp]),
     "mla_nvfp4_prefill_fused_out": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
                                              _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_int, _c_int,
                                              _c_f, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
@@ -71,11 +74,14 @@ def abi_symbols():
 
 
 class MLAError(RuntimeError):
-    def __init__(self, fn, status):
+    def __init__(self, fn, status, detail=None):
         self.status = status
-        detail = ""
-        if status == 6:  # MLA_ERR_LAUNCH: add the CUDA runtime's message
-            detail = ": " + load_library().mla_nvfp4_last_error().decode()
+        if detail is not None:
+            detail = ": " + detail
+        else:
+            detail = ""
+            if status == 6:  # MLA_ERR_LAUNCH: add the CUDA runtime's message
+                detail = ": " + load_library().mla_nvfp4_last_error().decode()
         super().__init__(f"{fn}: {status_string(status)} (status {status}){detail}")
 
 
@@ -205,6 +211,47 @@ def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, 
             _ptr(global_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
             num_splits, _ptr(error_word), _stream(q)))
     return (out, lse) if return_lse else out
+
+
+def mla_nvfp4_decode_noalloc(q, cache, global_scale, softmax_scale, out, *, page_table=None,
+                             seq_lens=None, page_size=64, topk_indices=None, lse=None, num_splits=0,
+                             error_word=None):
+    """mla_nvfp4_decode with the library's built-in scratch instead of a
+    workspace; the caller passes ``out`` (and ``lse`` if wanted), so nothing
+    is allocated.  Returns ``out``."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16)
+    _need(cache, "cache", torch.uint8, dev)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    _need(page_table, "page_table", torch.int32, dev)
+    _need(seq_lens, "seq_lens", torch.int32, dev)
+    _need(topk_indices, "topk_indices", torch.int32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    if out is None:
+        raise ValueError("out must be given: this entry point allocates nothing")
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if q.dim() != 3 or q.shape[2] != 576 or not q.is_contiguous():
+        raise ValueError("q must be contiguous [B, H, 576]")
+    B, H, _ = q.shape
+    if out.shape != (B, H, 512) or not out.is_contiguous():
+        raise ValueError("out must be contiguous [B, H, 512]")
+    if lse is not None and (lse.shape != (B, H) or not lse.is_contiguous()):
+        raise ValueError("lse must be contiguous [B, H]")
+    if topk_indices is not None and topk_indices.stride(1) != 1:
+        raise ValueError("topk_indices rows must be contiguous")
+    lib = load_library()
+    pt_stride = page_table.stride(0) if page_table is not None else 0
+    topk = topk_indices.shape[1] if topk_indices is not None else 0
+    with torch.cuda.device(dev):
+        st = lib.mla_nvfp4_decode_noalloc(
+            _ptr(q), B, H, _ptr(cache), cache.shape[0], cache.shape[1], _ptr(page_table), pt_stride,
+            page_size, _ptr(seq_lens), _ptr(topk_indices), topk, float(softmax_scale),
+            _ptr(global_scale), _ptr(out), _ptr(lse), num_splits, _ptr(error_word), _stream(q))
+    if st != 0:
+        detail = lib.mla_nvfp4_last_error().decode() if st in (5, 6) else None
+        raise MLAError("mla_nvfp4_decode_noalloc", st, detail)
+    return out
 
 
 def prefill_scale_bytes(total_tokens: int, num_heads: int) -> int:

@@ -44,6 +44,8 @@ int cuda_status(cudaError_t e) {
   return MLA_ERR_LAUNCH;
 }
 int launch_status() { return cuda_status(cudaGetLastError()); }
+void set_last_error(const char* message) { t_last_error = message; }
+int current_device_sms() { return device_sms(); }
 }  // namespace mla
 
 extern "C" {

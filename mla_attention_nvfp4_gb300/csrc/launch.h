@@ -14,6 +14,12 @@ namespace mla {
 int cuda_status(cudaError_t e);
 // MLA_OK after a successful launch sequence, else the recorded failure.
 int launch_status();
+// Make mla_nvfp4_last_error() return `message` (which must outlive the
+// calling thread's next library call) on this thread.
+void set_last_error(const char* message);
+// SM count of the current device, or -MLA_ERR_UNSUPPORTED_DEVICE when it
+// is not sm_103.
+int current_device_sms();
 
 int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, int64_t pe_stride,
                        const int64_t* slot_mapping, int64_t num_tokens, uint8_t* cache,
