@@ -14,32 +14,39 @@
 //   x_hat = e2m1(code) * e4m3(scale) * gs,   out = sum_j softmax(s)_j x_hat_j.
 //
 // The global scale gs is folded out of the tensor-core operands: the key
-// tile holds c*s (exact in f16) and k_pe (bf16), the query tile holds
-// [sigma*q_lat (f16), sigma*q_pe/gs (bf16)] with sigma a per-head power of
-// two keeping sigma*q_lat inside the f16 range, the product is multiplied by
-// softmax_scale*gs/sigma, and the output by gs.
+// tile holds c*s and k_pe, both exact in f16 (k_pe inside the f16 range),
+// the query holds sigma*[q_lat, q_pe/gs] in f16 with sigma a per-head power
+// of two keeping both parts inside the f16 range (q_lat then stays exact;
+// q_pe/gs is rounded once, to 11 bits), the product is multiplied by
+// softmax_scale*gs/sigma, and the output by gs.  All score MMAs are f16.
 //
-// Work unit = (sequence b, split, group of up to 128 heads), run by a
-// cluster of two CTAs.  CTA r owns latent features [256r, 256r+256) and RoPE
-// features [32r, 32r+32): it stages and dequantises only its half of every
-// record, keeps its half of Q in TMEM, computes a partial score tile over
-// its 288 dims, and accumulates its 256-column half of O.  The partial score
-// tiles (128 heads x 32 keys, fp32) are exchanged through distributed shared
-// memory, so both CTAs run the same softmax on the full scores.  This keeps
-// the 128 x 512 fp32 output within one SM's 512 TMEM columns per CTA and
-// does no tensor-core work twice.
+// Work unit = (sequence b, split, group of up to 128 heads), run by two
+// independent CTAs.  Both compute the full 576-feature scores of every
+// 64-key tile; CTA r accumulates only output features [256r, 256r+256).  The
+// 128 x 512 fp32 output does not fit one SM's 512 TMEM columns next to the
+// scores and the query, and exchanging partial scores between two SMs costs
+// more than computing them twice, so the score product is duplicated and
+// nothing crosses SMs.
 //
-// Warp roles per CTA (320 threads):
-//   warp 0      producer: slot ids, cp.async of the CTA's record halves
-//               into a 4-stage raw ring (16-byte chunks).
-//   warp 1      TMEM owner and MMA issuer (one thread):
-//                 S_j  = Q_half . K_j^T   M=128 N=32 K=288, Q from TMEM
-//                 O   += P_j . V_j        M=128 N=256 K=32, P from TMEM,
-//                                         V = the latent tile read MN-major
-//   warps 2..5  dequantise raw records into 128-byte-swizzled tiles: latent
-//               c*s in f16 (one cvt + one multiply per pair), RoPE in bf16.
-//   warps 6..9  Q staging, partial-score exchange, online softmax, O
-//               correction and the partial-output epilogue; thread = head.
+// Per CTA:
+//   TMEM   O half [0,256), scores/P for two tiles [256,384), Q RoPE part and
+//          latent features [0,192) [384,512) as MMA A operands.
+//   SMEM   Q latent features [192,512) (f16, 128-byte swizzled, 80 KB), and
+//          for two tiles: the "V part" (this CTA's 256 latent features, read
+//          by both products) and the "T part" (the other 256 latent features
+//          and the RoPE features, read by the score product only).
+//   The MMA order per tile is  QK_T(t+1), PV(t), QK_V(t+1): the softmax of
+//   tile t overlaps QK_T(t+1), and the V part of tile t+1 may be written
+//   while PV(t-1)..QK_T(t+1) run, so two buffers of each part suffice.
+//
+// Warp roles (352 threads):
+//   warps 0..3   Q staging, online softmax (thread = head), lazy O rescale,
+//                partial-output epilogue.
+//   warp 4       TMEM owner and MMA issuer (one thread).
+//   warps 5..10  dequantisation: thread = (key, third of the record), 16-byte
+//                loads straight from global memory (L2-prefetched a tile
+//                ahead), e2m1 -> f16 conversion times the block scale, stores
+//                into the swizzled operand tiles.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -53,35 +60,29 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTok = 32;           // keys per tile
+constexpr int kTok = 64;           // keys per tile (MMA N of the score product)
 constexpr int kHeads = 128;        // heads per work unit (MMA M)
-constexpr int kThreads = 320;
-constexpr int kRawStride = 224;    // bytes per key in the raw ring (208 used)
-constexpr int kRawStages = 6;
-constexpr int kKvStages = 3;
-constexpr int kXchBufs = 4;
-constexpr uint32_t kRawBytes = kTok * kRawStride;         // 7168
-constexpr uint32_t kKvBlock = kTok * 128;                 // one 64-feature column block
-constexpr uint32_t kKvBytes = 5 * kKvBlock;               // 4 latent blocks + RoPE block
-constexpr uint32_t kXchBytes = kHeads * kTok * 4;         // 16384
-constexpr uint32_t kSmKv = 0;
-constexpr uint32_t kSmRaw = kSmKv + kKvStages * kKvBytes;
-constexpr uint32_t kSmXch = kSmRaw + kRawStages * kRawBytes;
-constexpr uint32_t kSmBytes = kSmXch + kXchBufs * kXchBytes;
+constexpr int kThreads = 352;
+constexpr int kMmaWarp = 4;
+constexpr int kDeqWarp0 = 5;
+constexpr uint32_t kChunk = kTok * 128;      // 64 keys x 64 features, f16
+constexpr uint32_t kQChunk = kHeads * 128;   // 128 heads x 64 features, f16
+constexpr uint32_t kVBytes = 4 * kChunk;     // V part: 4 latent chunks
+constexpr uint32_t kTBytes = 5 * kChunk;     // T part: 4 latent chunks + RoPE
+constexpr uint32_t kSmQ = 0;                 // Q latent chunks 3..7
+constexpr uint32_t kSmV = kSmQ + 5 * kQChunk;
+constexpr uint32_t kSmT = kSmV + 2 * kVBytes;
+constexpr uint32_t kSmBytes = kSmT + 2 * kTBytes;
 constexpr uint32_t kSmAlloc = kSmBytes + 1024;
-static_assert(kSmAlloc <= 232448, "shared memory budget");
+static_assert(kSmAlloc + 512 <= 232448, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t kTQ = 0;                  // Q half: 288 bf16 = 144 columns
-__host__ __device__ constexpr uint32_t col_s(int buf) { return 160u + 32u * buf; }  // scores, 32 cols
-__host__ __device__ constexpr uint32_t col_p(int buf) { return 224u + 16u * buf; }  // P bf16 pairs, 16 cols
-constexpr uint32_t kTO = 256;                // O half, 256 columns
+constexpr uint32_t kTO = 0;                  // O half, 256 columns
+__host__ __device__ constexpr uint32_t col_s(int buf) { return 256u + 64u * buf; }  // scores / P
+constexpr uint32_t kTQRope = 384;            // sigma*q_pe/gs, f16 pairs, 32 columns
+constexpr uint32_t kTQLat = 416;             // sigma*q_lat[0:192], f16 pairs, 96 columns
 
-// Latent products run on f16 operands (c*s is exact in f16; Q is scaled per
-// row by a power of two so that it cannot overflow f16); the RoPE K-steps
-// run as separate bf16 MMAs into the same accumulator.
-constexpr uint32_t kIdescQKLat = idesc_f16_f32(128, kTok, false, false);
-constexpr uint32_t kIdescQKRope = idesc_bf16_f32(128, kTok, false, false);
+constexpr uint32_t kIdescQK = idesc_f16_f32(128, kTok, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 256, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -108,16 +109,14 @@ struct Params {
 };
 
 struct alignas(8) Barriers {
-  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-  uint64_t kv_full[kKvStages], kv_empty[kKvStages];
   uint64_t q_ready;
-  uint64_t s_full[2], s_free[2];
-  uint64_t xch_full[kXchBufs];
-  uint64_t p_full[2], pv_done[2];
+  uint64_t t_full[2], t_empty[2];
+  uint64_t v_full[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_full;
 };
 
-// Key addressing in two halves so that the index load can be issued tiles
+// Key addressing in two halves so that the index load can be issued a tile
 // ahead of its use: load_index() performs one unconditional, in-bounds load
 // (the page-table entry or the top-k index of key position t, clamped into
 // its row); key_slot() then turns that value into a slot id, or -1 for
@@ -151,6 +150,12 @@ __device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t,
   return slot;
 }
 
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
       "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
@@ -175,31 +180,57 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&z);
 }
 
-// f16x2 -> bf16x2; exact for e4m3 values (4 significant bits).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
-  const __half2 x = *reinterpret_cast<const __half2*>(&h);
-  const float2 f = __half22float2(x);
-  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-  return *reinterpret_cast<uint32_t*>(&b);
+// bf16x2 -> f16x2; exact inside the f16 range (8 <= 11 significant bits).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  float lo, hi;
+  bf16x2_to_f32(v, lo, hi);
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&b);
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t byte_of(const uint4& v, int i) {
+  const uint32_t w = (i < 4) ? v.x : (i < 8) ? v.y : (i < 12) ? v.z : v.w;
+  return (w >> (8 * (i & 3))) & 0xFFu;
+}
+
+// One 16-byte code segment (32 features, two 16-feature blocks with scale
+// bytes s0, s1) -> four 16-byte units of c*s in f16, stored at feature units
+// u0..u0+3 of a 128-byte-swizzled row (unit u of row `row` in chunk u/8).
+__device__ __forceinline__ void dequant_segment(const uint4& c, uint32_t s0, uint32_t s1, uint32_t tile,
+                                                int u0, int row) {
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+  const uint32_t f0 = e4m3x2_to_f16x2(s0 | (s0 << 8)), f1 = e4m3x2_to_f16x2(s1 | (s1 << 8));
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t h[4];
+    e2m1x8_to_f16x8(words[w], h);
+    const uint32_t f = (w < 2) ? f0 : f1;
+    const int u = u0 + w;
+    const uint32_t addr = tile + (u >> 3) * kChunk + row * 128 + (((u & 7) ^ (row & 7)) << 4);
+    sts128(addr, make_uint4(hmul2_u32(h[0], f), hmul2_u32(h[1], f), hmul2_u32(h[2], f), hmul2_u32(h[3], f)));
+  }
+}
+
+__device__ __forceinline__ void zero_units(uint32_t tile, int u0, int n, int row) {
+  for (int u = u0; u < u0 + n; ++u)
+    sts128(tile + (u >> 3) * kChunk + row * 128 + (((u & 7) ^ (row & 7)) << 4), make_uint4(0, 0, 0, 0));
 }
 
 template <int kRecord>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
   constexpr bool kFp8Rope = (kRecord == 368);
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
-  __shared__ uint32_t raw_mask[kRawStages];  // valid keys of each raw stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
-  const uint32_t peer = rank ^ 1u;
+  const int rank = blockIdx.x & 1;
   const int split = blockIdx.x >> 1, b = blockIdx.y, hg = blockIdx.z;
   const int n_keys = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
   const int n_tiles_all = (n_keys + kTok - 1) / kTok;
@@ -209,213 +240,256 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
   uint32_t* err = p.error_word;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sKV = smem + kSmKv;
-  uint8_t* sRaw = smem + kSmRaw;
-  uint8_t* sXch = smem + kSmXch;
+  const uint32_t sQ = smem_u32(smem + kSmQ), sV = smem_u32(smem + kSmV), sT = smem_u32(smem + kSmT);
 
   if (threadIdx.x == 0) {
     abort_s = 0;
-    for (int i = 0; i < kRawStages; ++i) {
-      mbar_init(&bars.raw_full[i], 33);  // 32 cp.async arrivals + the mask writer
-      mbar_init(&bars.raw_empty[i], 128);
-    }
-    for (int i = 0; i < kKvStages; ++i) {
-      mbar_init(&bars.kv_full[i], 128);
-      mbar_init(&bars.kv_empty[i], 1);
-    }
     mbar_init(&bars.q_ready, 128);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.t_full[i], 128);
+      mbar_init(&bars.t_empty[i], 1);
+      mbar_init(&bars.v_full[i], 128);
+      mbar_init(&bars.v_empty[i], 1);
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_free[i], 128);
       mbar_init(&bars.p_full[i], 128);
       mbar_init(&bars.pv_done[i], 1);
     }
-    for (int i = 0; i < kXchBufs; ++i) mbar_init(&bars.xch_full[i], 1);
     mbar_init(&bars.o_full, 1);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&tmem_base_s, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // both CTAs' barriers exist before any remote store
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Index loads run two tiles ahead of their use.
-    bool bad = false;
-    int32_t idx_a = nt > 0 ? load_index(p, b, tile0 * kTok + lane) : -1;
-    int32_t idx_b = nt > 1 ? load_index(p, b, (tile0 + 1) * kTok + lane) : -1;
-    for (int j = 0; j < nt; ++j) {
-      const int st = j % kRawStages;
-      const uint32_t ph = (j / kRawStages) & 1;
-      const int32_t idx = idx_a;
-      idx_a = idx_b;
-      if (j + 2 < nt) idx_b = load_index(p, b, (tile0 + j + 2) * kTok + lane);
-      const int64_t slot = key_slot(p, idx, (tile0 + j) * kTok + lane, n_keys, bad);
-      if (!mbar_wait(&bars.raw_empty[st], ph ^ 1, err, &abort_s)) break;
-      const unsigned vmask = __ballot_sync(0xffffffffu, slot >= 0);
-      if (slot >= 0) {
-        const uint8_t* rec = p.cache + slot * kRecord;
-        uint8_t* dst = sRaw + st * kRawBytes + lane * kRawStride;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cp_async16(dst + 16 * i, rec + 128 * rank + 16 * i);
-        cp_async16(dst + 128, rec + 256 + 16 * rank);
-        if constexpr (kFp8Rope) {
-#pragma unroll
-          for (int i = 0; i < 2; ++i) cp_async16(dst + 144 + 16 * i, rec + 288 + 32 * rank + 16 * i);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) cp_async16(dst + 144 + 16 * i, rec + 288 + 64 * rank + 16 * i);
-        }
-      }
-      cp_async_arrive(&bars.raw_full[st]);
-      if (lane == 0) {
-        raw_mask[st] = vmask;
-        mbar_arrive(&bars.raw_full[st]);
-      }
-    }
-    if (bad && rank == 0) flag_error(err, MLA_DEVERR_BOUNDS);
-    cp_async_wait_all();
-  } else if (warp == 1) {
+  if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && nt > 0) {
-      const uint32_t kv_addr = smem_u32(sKV);
+      // Descriptors are formed once; a tile, chunk or K-step offset is added
+      // to the start-address field (16-byte units, no carry: shared
+      // addresses stay below 256 KB).
+      const uint64_t dq = smem_desc_sw128(sQ, 0, 1024);
+      const uint64_t dv = smem_desc_sw128(sV, 0, 1024);
+      const uint64_t dt = smem_desc_sw128(sT, 0, 1024);
+      const uint64_t dpv = smem_desc_sw128(sV, kChunk, 1024);
       bool ok = mbar_wait(&bars.q_ready, 0, err, &abort_s);
       tc_fence_after();
-      auto issue_pv = [&](int i) -> bool {
-        const int pb = i & 1;
-        if (!mbar_wait(&bars.p_full[pb], (i >> 1) & 1, err, &abort_s)) return false;
-        tc_fence_after();
-        const uint32_t vbase = kv_addr + (i % kKvStages) * kKvBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTok / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kKvBlock, 1024);
-          mma_ts(tmem + kTO, tmem + col_p(pb) + kk * 8, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+      // latent chunk c of Q (TMEM for c < 3, shared memory otherwise) times
+      // the K chunk at descriptor kd, into scores d.  The operand-form test
+      // stays outside the K-steps: with it inside an unrolled K-step loop,
+      // one K-step was observed to run with the previous step's A operand.
+      auto latent = [&](int c, uint64_t kd, uint32_t d) {
+        if (c < 3) {
+          const uint32_t a0 = tmem + kTQLat + 32 * c;
+          mma_ts(d, a0, kd, kIdescQK, 1u);
+          mma_ts(d, a0 + 8, kd + 2, kIdescQK, 1u);
+          mma_ts(d, a0 + 16, kd + 4, kIdescQK, 1u);
+          mma_ts(d, a0 + 24, kd + 6, kIdescQK, 1u);
+        } else {
+          const uint64_t a0 = dq + static_cast<uint64_t>((c - 3) * (kQChunk / 16));
+          mma_ss(d, a0, kd, kIdescQK, 1u);
+          mma_ss(d, a0 + 2, kd + 2, kIdescQK, 1u);
+          mma_ss(d, a0 + 4, kd + 4, kIdescQK, 1u);
+          mma_ss(d, a0 + 6, kd + 6, kIdescQK, 1u);
         }
-        mma_commit(&bars.kv_empty[i % kKvStages]);
+      };
+      auto issue_qk_t = [&](int j) -> bool {
+        const int tb = j & 1;
+        if (!mbar_wait(&bars.t_full[tb], (j >> 1) & 1, err, &abort_s)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + col_s(tb);
+        const uint64_t td = dt + tb * (kTBytes / 16);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(d, tmem + kTQRope + 8 * kk, td + (4 * kChunk + 32 * kk) / 16, kIdescQK, kk > 0 ? 1u : 0u);
+        for (int i = 0; i < 4; ++i) latent(4 * (1 - rank) + i, td + i * (kChunk / 16), d);
+        mma_commit(&bars.t_empty[tb]);
+        return true;
+      };
+      auto issue_qk_v = [&](int j) -> bool {
+        const int vb = j & 1;
+        if (!mbar_wait(&bars.v_full[vb], (j >> 1) & 1, err, &abort_s)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + col_s(vb);
+        const uint64_t vd = dv + vb * (kVBytes / 16);
+        for (int i = 0; i < 4; ++i) latent(4 * rank + i, vd + i * (kChunk / 16), d);
+        mma_commit(&bars.s_full[vb]);
+        return true;
+      };
+      auto issue_pv = [&](int t) -> bool {
+        const int pb = t & 1;
+        if (!mbar_wait(&bars.p_full[pb], (t >> 1) & 1, err, &abort_s)) return false;
+        tc_fence_after();
+        const uint64_t vd = dpv + pb * (kVBytes / 16);
+#pragma unroll
+        for (int kk = 0; kk < kTok / 16; ++kk)
+          mma_ts(tmem + kTO, tmem + col_s(pb) + 8 * kk, vd + (2048 * kk) / 16, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.v_empty[pb]);
         mma_commit(&bars.pv_done[pb]);
         return true;
       };
-      // QK runs two tiles ahead of PV: S(i+2) is computed while the softmax
-      // works on tile i.
-      auto issue_qk = [&](int j) -> bool {
-        const int ks = j % kKvStages;
-        const int sb = j & 1;
-        if (!mbar_wait(&bars.kv_full[ks], (j / kKvStages) & 1, err, &abort_s)) return false;
-        if (j >= 2 && !mbar_wait(&bars.s_free[sb], ((j - 2) >> 1) & 1, err, &abort_s)) return false;
-        tc_fence_after();
-        const uint32_t kbase = kv_addr + ks * kKvBytes;
-#pragma unroll
-        for (int kk = 0; kk < 18; ++kk) {
-          const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * kKvBlock + (kk & 3) * 32, 0, 1024);
-          mma_ts(tmem + col_s(sb), tmem + kTQ + kk * 8, bd, kk < 16 ? kIdescQKLat : kIdescQKRope, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars.s_full[sb]);
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      if (ok && nt > 1) ok = issue_qk(1);
-      for (int i = 0; ok && i < nt; ++i) {
-        if (i + 2 < nt && !issue_qk(i + 2)) {
-          ok = false;
-          break;
-        }
-        if (!issue_pv(i)) ok = false;
+      if (ok) ok = issue_qk_t(0);
+      if (ok) ok = issue_qk_v(0);
+      for (int t = 0; ok && t < nt; ++t) {
+        if (t + 1 < nt && !issue_qk_t(t + 1)) break;
+        if (!issue_pv(t)) break;
+        if (t + 1 < nt && !issue_qk_v(t + 1)) break;
       }
       mma_commit(&bars.o_full);
       mbar_wait(&bars.o_full, 0, err, nullptr);  // every MMA retired
     }
-  } else if (warp < 6) {
+  } else if (warp >= kDeqWarp0) {
     // ---------------------------------------------------------- dequantise
-    const int dt = threadIdx.x - 64;
-    const int tok = dt >> 2, part = dt & 3;
-    for (int j = 0; j < nt; ++j) {
-      const int st = j % kRawStages, ks = j % kKvStages;
-      if (!mbar_wait(&bars.raw_full[st], (j / kRawStages) & 1, err, &abort_s)) break;
-      if (!mbar_wait(&bars.kv_empty[ks], ((j / kKvStages) & 1) ^ 1, err, &abort_s)) break;
-      const bool valid = (raw_mask[st] >> tok) & 1u;
-      uint8_t* kv = sKV + ks * kKvBytes;
-      const uint32_t sw = tok & 7;
-      uint4 outv[8];
-      uint4 rope_out = make_uint4(0, 0, 0, 0);
-      if (valid) {
-        const uint8_t* raw = sRaw + st * kRawBytes + tok * kRawStride;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(raw + 32 * part);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(raw + 32 * part + 16);
-        const uint32_t sc = *reinterpret_cast<const uint32_t*>(raw + 128 + 4 * part);
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          const uint32_t sbyte = (sc >> (8 * blk)) & 0xFFu;
-          const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));
-#pragma unroll
-          for (int hw = 0; hw < 2; ++hw) {  // 8 codes per word
-            uint32_t h[4];
-            e2m1x8_to_f16x8(words[2 * blk + hw], h);
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = hmul2_u32(h[i], s2);  // c*s, exact in f16
-            outv[2 * blk + hw] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        }
-        if constexpr (kFp8Rope) {
-          const uint2 r = *reinterpret_cast<const uint2*>(raw + 144 + 8 * part);
-          uint32_t o[4];
-          o[0] = f16x2_to_bf16x2(e4m3x2_to_f16x2(r.x & 0xFFFFu));
-          o[1] = f16x2_to_bf16x2(e4m3x2_to_f16x2(r.x >> 16));
-          o[2] = f16x2_to_bf16x2(e4m3x2_to_f16x2(r.y & 0xFFFFu));
-          o[3] = f16x2_to_bf16x2(e4m3x2_to_f16x2(r.y >> 16));
-          rope_out = make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-          rope_out = *reinterpret_cast<const uint4*>(raw + 144 + 16 * part);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) outv[i] = make_uint4(0, 0, 0, 0);
-      }
-      // latent features [64 part, 64 part + 64): column block `part`, 8 chunks
-      uint8_t* row = kv + part * kKvBlock + tok * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = outv[c];
-      // RoPE features [8 part, 8 part + 8) of this CTA's 32: column block 4
-      *reinterpret_cast<uint4*>(kv + 4 * kKvBlock + tok * 128 + ((part ^ sw) << 4)) = rope_out;
-      fence_async_smem();
-      mbar_arrive(&bars.kv_full[ks]);
-      mbar_arrive(&bars.raw_empty[st]);
+    // thread = (key k of the tile, part q): q = 0 writes V units 0..23, q = 1
+    // V units 24..31 and T units 0..15, q = 2 T units 16..31 and the RoPE
+    // chunk.  V = latent features [256 rank, +256), T = the other 256.
+    const int di = threadIdx.x - 32 * kDeqWarp0;
+    const int k = di & 63, q = di >> 6;
+    const int other = 1 - rank;
+    bool bad = false;
+    int32_t idx0 = nt > 0 ? load_index(p, b, tile0 * kTok + k) : -1;
+    int32_t idx1 = nt > 1 ? load_index(p, b, (tile0 + 1) * kTok + k) : -1;
+    if (q == 0 && nt > 0) {
+      bool dummy = false;
+      const int64_t s0 = key_slot(p, idx0, tile0 * kTok + k, n_keys, dummy);
+      if (s0 >= 0) prefetch_l2(p.cache + s0 * kRecord, kRecord);
     }
+    for (int j = 0; j < nt; ++j) {
+      const int key = (tile0 + j) * kTok + k;
+      const int64_t slot = key_slot(p, idx0, key, n_keys, bad);
+      idx0 = idx1;
+      if (j + 2 < nt) idx1 = load_index(p, b, key + 2 * kTok);
+      if (q == 0 && j + 1 < nt) {
+        bool dummy = false;
+        const int64_t sn = key_slot(p, idx0, key + kTok, n_keys, dummy);
+        if (sn >= 0) prefetch_l2(p.cache + sn * kRecord, kRecord);
+      }
+      const bool valid = slot >= 0;
+      const uint8_t* rec = p.cache + (valid ? slot : 0) * kRecord;
+      const uint32_t tV = sV + (j & 1) * kVBytes, tT = sT + (j & 1) * kTBytes;
+      const uint32_t ph_empty = ((j >> 1) & 1) ^ 1;
+      if (q == 0) {
+        uint4 c[6], sc = make_uint4(0, 0, 0, 0);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 6; ++i) c[i] = ldg16(rec + 128 * rank + 16 * i);
+          sc = ldg16(rec + 256 + 16 * rank);
+        }
+        if (!mbar_wait(&bars.v_empty[j & 1], ph_empty, err, &abort_s)) break;
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 6; ++i) dequant_segment(c[i], byte_of(sc, 2 * i), byte_of(sc, 2 * i + 1), tV, 4 * i, k);
+        } else {
+          zero_units(tV, 0, 24, k);
+        }
+        fence_async_smem();
+        mbar_arrive(&bars.v_full[j & 1]);
+      } else if (q == 1) {
+        uint4 cv[2], ct[4], scv = make_uint4(0, 0, 0, 0), sct = make_uint4(0, 0, 0, 0);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ct[i] = ldg16(rec + 128 * other + 16 * i);
+          sct = ldg16(rec + 256 + 16 * other);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) cv[i] = ldg16(rec + 128 * rank + 96 + 16 * i);
+          scv = ldg16(rec + 256 + 16 * rank);
+        }
+        if (!mbar_wait(&bars.t_empty[j & 1], ph_empty, err, &abort_s)) break;
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dequant_segment(ct[i], byte_of(sct, 2 * i), byte_of(sct, 2 * i + 1), tT, 4 * i, k);
+        } else {
+          zero_units(tT, 0, 16, k);
+        }
+        fence_async_smem();
+        mbar_arrive(&bars.t_full[j & 1]);
+        if (!mbar_wait(&bars.v_empty[j & 1], ph_empty, err, &abort_s)) break;
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            dequant_segment(cv[i], byte_of(scv, 12 + 2 * i), byte_of(scv, 13 + 2 * i), tV, 24 + 4 * i, k);
+        } else {
+          zero_units(tV, 24, 8, k);
+        }
+        fence_async_smem();
+        mbar_arrive(&bars.v_full[j & 1]);
+      } else {
+        constexpr int kRopeSegs = kFp8Rope ? 4 : 8;
+        uint4 ct[4], r[kRopeSegs], sct = make_uint4(0, 0, 0, 0);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ct[i] = ldg16(rec + 128 * other + 64 + 16 * i);
+          sct = ldg16(rec + 256 + 16 * other);
+#pragma unroll
+          for (int i = 0; i < kRopeSegs; ++i) r[i] = ldg16(rec + 288 + 16 * i);
+        }
+        if (!mbar_wait(&bars.t_empty[j & 1], ph_empty, err, &abort_s)) break;
+        const uint32_t rope_row = tT + 4 * kChunk + k * 128;
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dequant_segment(ct[i], byte_of(sct, 8 + 2 * i), byte_of(sct, 9 + 2 * i), tT, 16 + 4 * i, k);
+          if constexpr (kFp8Rope) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint4 o = make_uint4(e4m3x2_to_f16x2(w[2 * h] & 0xFFFFu), e4m3x2_to_f16x2(w[2 * h] >> 16),
+                                           e4m3x2_to_f16x2(w[2 * h + 1] & 0xFFFFu),
+                                           e4m3x2_to_f16x2(w[2 * h + 1] >> 16));
+                const int u = 2 * i + h;
+                sts128(rope_row + ((u ^ (k & 7)) << 4), o);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              sts128(rope_row + ((u ^ (k & 7)) << 4),
+                     make_uint4(bf16x2_to_f16x2(r[u].x), bf16x2_to_f16x2(r[u].y), bf16x2_to_f16x2(r[u].z),
+                                bf16x2_to_f16x2(r[u].w)));
+          }
+        } else {
+          zero_units(tT, 16, 16, k);
+          zero_units(tT, 32, 8, k);
+        }
+        fence_async_smem();
+        mbar_arrive(&bars.t_full[j & 1]);
+      }
+    }
+    if (bad && rank == 0 && q == 0) flag_error(err, MLA_DEVERR_BOUNDS);
   } else {
     // ------------------------------------------- softmax and epilogue
-    const int quad = warp & 3;
-    const int hr = quad * 32 + lane;  // head row within the group
+    const int hr = warp * 32 + lane;  // head row within the group
     const int head = hg * kHeads + hr;
     const bool head_ok = head < p.num_heads;
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float gs = *p.gs;
     const bool gs_ok = scale_ok(gs);
     float score_scale = p.softmax_scale * gs * kLog2e;
     bool ok = true;
     float m_run = -INFINITY, l_run = 0.f;
     if (nt > 0) {
-      // Q half -> TMEM: [sigma*q_lat[256r : 256r+256] as f16 pairs,
-      //                  sigma*q_pe[32r : 32r+32]/gs as bf16 pairs]
+      // Q -> f16 operands: TMEM [sigma*q_pe/gs, sigma*q_lat[0:192]], shared
+      // memory sigma*q_lat[192:512] (swizzled rows).
       const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(b) * p.num_heads + head) * 576;
       const float inv_gs = gs_ok ? 1.f / gs : 0.f;
-      float qmax = 0.f;  // over the whole latent row, so both CTAs pick the same sigma
+      float qmax = 0.f;  // max over q_lat and q_pe/gs
       if (head_ok) {
 #pragma unroll 4
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < 72; ++i) {
           const uint4 w = reinterpret_cast<const uint4*>(qrow)[i];
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          const float f = (i < 64) ? 1.f : inv_gs;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int kx = 0; kx < 4; ++kx) {
             float lo, hi;
-            bf16x2_to_f32(ws[k], lo, hi);
-            qmax = fmaxf(qmax, fmaxf(fabsf(lo), fabsf(hi)));
+            bf16x2_to_f32(ws[kx], lo, hi);
+            qmax = fmaxf(qmax, fmaxf(fabsf(lo * f), fabsf(hi * f)));
           }
         }
       }
@@ -424,105 +498,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       const int a_sh = max(0, min(qexp - 14, 100));
       const float sigma = __uint_as_float(static_cast<uint32_t>(127 - a_sh) << 23);
       score_scale *= __uint_as_float(static_cast<uint32_t>(127 + a_sh) << 23);
+      // 16-byte source unit u of the row (8 bf16) -> 8 operand values
+      auto q_unit = [&](int u) -> uint4 {
+        if (!head_ok) return make_uint4(0, 0, 0, 0);
+        const uint4 w = reinterpret_cast<const uint4*>(qrow)[u];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
 #pragma unroll
-      for (int c = 0; c < 144; c += 16) {
-        uint32_t v[16];
-        if (head_ok) {
-          if (c < 128) {
-            const uint4* src = reinterpret_cast<const uint4*>(qrow + 256 * rank + 2 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 w = src[i];
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                float lo, hi;
-                bf16x2_to_f32(ws[k], lo, hi);
-                __half2 h2 = __floats2half2_rn(lo * sigma, hi * sigma);
-                v[4 * i + k] = *reinterpret_cast<uint32_t*>(&h2);
-              }
-            }
-          } else {
-            const uint4* src = reinterpret_cast<const uint4*>(qrow + 512 + 32 * rank);
-            const float f = inv_gs * sigma;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 w = src[i];
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                float lo, hi;
-                bf16x2_to_f32(ws[k], lo, hi);
-                v[4 * i + k] = pack_bf16(lo * f, hi * f);
-              }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0u;
+        for (int kx = 0; kx < 4; ++kx) {
+          float lo, hi;
+          bf16x2_to_f32(ws[kx], lo, hi);
+          const float f = (u < 64) ? sigma : inv_gs * sigma;
+          o[kx] = pack_f16(lo * f, hi * f);
         }
-        tmem_st16(tmem + lane_off + kTQ + c, v);
+        return make_uint4(o[0], o[1], o[2], o[3]);
+      };
+      // TMEM part: RoPE (units 64..71) then latent units 0..23
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int col = c + 4 * i;  // 4 columns = one unit of 8 values
+          const int u = (col < 32) ? 64 + col / 4 : (col - 32) / 4;
+          const uint4 x = q_unit(u);
+          v[4 * i] = x.x;
+          v[4 * i + 1] = x.y;
+          v[4 * i + 2] = x.z;
+          v[4 * i + 3] = x.w;
+        }
+        tmem_st16(tmem + lane_off + kTQRope + c, v);
       }
+      // shared-memory part: latent units 24..63 -> chunks 0..4 of sQ
+#pragma unroll 4
+      for (int u = 24; u < 64; ++u) {
+        const int cu = u - 24;
+        sts128(sQ + (cu >> 3) * kQChunk + hr * 128 + (((cu & 7) ^ (hr & 7)) << 4), q_unit(u));
+      }
+      fence_async_smem();
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.q_ready);
 
-      const uint32_t xch_local = smem_u32(sXch);
-      const uint32_t xch_peer = map_peer(xch_local, peer);
-      const uint32_t swz = hr & 7;
-      // fetch(j): read this CTA's partial scores of tile j from TMEM, free
-      // the S buffer, send them to the peer and note which keys are valid.
-      auto fetch = [&](int j, float (&s)[kTok], int32_t& idx) -> bool {
-        const int sb = j & 1;
-        const int xb = j % kXchBufs;
-        if (hr == 0) mbar_expect_tx(&bars.xch_full[xb], kXchBytes);
-        idx = load_index(p, b, (tile0 + j) * kTok + lane);  // consumed two steps later
-        if (!mbar_wait(&bars.s_full[sb], (j >> 1) & 1, err, &abort_s)) return false;
-        tc_fence_after();
-        uint32_t v0[16], v1[16];
-        tmem_ld16(tmem + lane_off + col_s(sb), v0);
-        tmem_ld16(tmem + lane_off + col_s(sb) + 16, v1);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&bars.s_free[sb]);
-        const uint32_t dst = xch_peer + xb * kXchBytes + hr * 128;
-        const uint32_t rbar = map_peer(smem_u32(&bars.xch_full[xb]), peer);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          st_async_v4(dst + ((static_cast<uint32_t>(i) ^ swz) << 4),
-                      make_uint4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]), rbar);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          st_async_v4(dst + ((static_cast<uint32_t>(i + 4) ^ swz) << 4),
-                      make_uint4(v1[4 * i], v1[4 * i + 1], v1[4 * i + 2], v1[4 * i + 3]), rbar);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          s[i] = __uint_as_float(v0[i]);
-          s[16 + i] = __uint_as_float(v1[i]);
-        }
-        return true;
-      };
-
-      // step(j): combine tile j with the peer's partial, online softmax, P(j)
-      // into TMEM; then fetch tile j+2 into the same registers.
-      auto step = [&](int j, float (&s)[kTok], int32_t& idx) -> bool {
+      // per-tile validity: lane checks keys `lane` and `lane + 32`
+      int32_t ia = load_index(p, b, tile0 * kTok + lane), ib = load_index(p, b, tile0 * kTok + 32 + lane);
+      for (int j = 0; j < nt; ++j) {
         const int pb = j & 1;
-        const int xb = j % kXchBufs;
-        bool bad = false;
-        const unsigned valid = __ballot_sync(0xffffffffu, key_slot(p, idx, (tile0 + j) * kTok + lane, n_keys, bad) >= 0);
-        if (!mbar_wait(&bars.xch_full[xb], (j / kXchBufs) & 1, err, &abort_s)) return false;
-        const uint8_t* src = sXch + xb * kXchBytes + hr * 128;
+        const int key = (tile0 + j) * kTok + lane;
+        bool badv = false;
+        const unsigned va = __ballot_sync(0xffffffffu, key_slot(p, ia, key, n_keys, badv) >= 0);
+        const unsigned vb = __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0);
+        if (j + 1 < nt) {
+          ia = load_index(p, b, key + kTok);
+          ib = load_index(p, b, key + kTok + 32);
+        }
+        if (!mbar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         float x[kTok];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 f = *reinterpret_cast<const float4*>(src + ((static_cast<uint32_t>(i) ^ swz) << 4));
-          x[4 * i] = s[4 * i] + f.x;
-          x[4 * i + 1] = s[4 * i + 1] + f.y;
-          x[4 * i + 2] = s[4 * i + 2] + f.z;
-          x[4 * i + 3] = s[4 * i + 3] + f.w;
+        for (int c = 0; c < kTok; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_off + col_s(pb) + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
         }
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (valid == 0xffffffffu) {
+        if ((va & vb) == 0xffffffffu) {
 #pragma unroll
           for (int c = 0; c < kTok; ++c) {
             x[c] *= score_scale;
@@ -531,7 +576,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         } else {
 #pragma unroll
           for (int c = 0; c < kTok; ++c) {
-            x[c] = ((valid >> c) & 1u) ? x[c] * score_scale : -INFINITY;
+            const unsigned m = c < 32 ? va : vb;
+            x[c] = ((m >> (c & 31)) & 1u) ? x[c] * score_scale : -INFINITY;
             mq[c & 3] = fmaxf(mq[c & 3], x[c]);
           }
         }
@@ -542,10 +588,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
           m_use = mx;
           alpha = ex2_approx(m_run - mx);
         }
-        // P(j) reuses the buffer PV(j-2) read; an O rescale needs PV(j-1) retired
-        if (j >= 2 && !mbar_wait(&bars.pv_done[pb], ((j - 2) >> 1) & 1, err, &abort_s)) return false;
+        // an O rescale needs PV(j-1) retired and must precede PV(j)
         if (__any_sync(0xffffffffu, raise && j > 0)) {
-          if (!mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s)) return false;
+          if (!mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll 4
           for (int c = 0; c < 256; c += 16) {
@@ -561,31 +609,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         m_run = m_use;
         const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;  // no valid key so far
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pv[16];
+        uint32_t pv[kTok / 2];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kTok / 2; ++i) {
           const float p0 = ex2_approx(x[2 * i] - m_ref), p1 = ex2_approx(x[2 * i + 1] - m_ref);
           ls[i & 3] += p0 + p1;
-          __half2 h2 = __floats2half2_rn(p0, p1);  // P <= 2^8 (lazy reference), f16 operand
-          pv[i] = *reinterpret_cast<uint32_t*>(&h2);
+          pv[i] = pack_f16(p0, p1);  // P <= 2^8 (lazy reference), f16 operand
         }
         l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-        tc_fence_after();
-        tmem_st16(tmem + lane_off + col_p(pb), pv);
+        // P(j) over S(j): the buffer's previous P was read by PV(j-2), which
+        // ran before QK(j) wrote S(j)
+        uint32_t v0[16], v1[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          v0[i] = pv[i];
+          v1[i] = pv[16 + i];
+        }
+        tmem_st16(tmem + lane_off + col_s(pb), v0);
+        tmem_st16(tmem + lane_off + col_s(pb) + 16, v1);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars.p_full[pb]);
-        if (j + 2 < nt) return fetch(j + 2, s, idx);
-        return true;
-      };
-
-      float s_a[kTok], s_b[kTok];
-      int32_t idx_a = -1, idx_b = -1;
-      ok = fetch(0, s_a, idx_a);
-      if (ok && nt > 1) ok = fetch(1, s_b, idx_b);
-      for (int j = 0; ok && j < nt; j += 2) {
-        ok = step(j, s_a, idx_a);
-        if (ok && j + 1 < nt) ok = step(j + 1, s_b, idx_b);
       }
       if (ok) ok = mbar_wait(&bars.o_full, 0, err, &abort_s);
     }
@@ -619,9 +663,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA leaves while its peer may still address it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 // Merge the per-split partials of one (batch, head): LSE = ln sum exp(lse_i),

@@ -35,15 +35,29 @@ def oracle_slots(w):
     return attention.decode_slots_topk(w.topk_indices.cpu().numpy())
 
 
+def bf16_half_ulp(x) -> np.ndarray:
+    """Half a bf16 unit in the last place at |x|: the largest change that
+    rounding x to bf16 (8 significant bits) can make."""
+    a = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 8)
+
+
 def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str):
+    """Decode outputs (bf16) against the float64 oracle.  The max-abs bar
+    applies to the value before its final rounding to the bf16 output: an
+    element may differ by MAX_ABS plus half a bf16 ulp at its magnitude (at
+    |o| ~ 80, reached with x20 latent outliers, that rounding alone is 0.25).
+    The mean relative L1 error is taken as is."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref)
-    max_abs = float(err.max()) if err.size else 0.0
+    excess = err - np.maximum(bf16_half_ulp(ref), bf16_half_ulp(got))
+    max_abs = float(excess.max()) if err.size else 0.0
     denom = float(np.abs(ref).sum())
     mean_rel = float(err.sum() / denom) if denom > 0 else float(err.sum())
     assert max_abs <= MAX_ABS and mean_rel <= MEAN_REL, \
-        f"{what}: max_abs={max_abs:.3e} (<= {MAX_ABS}), mean_rel={mean_rel:.3e} (<= {MEAN_REL})"
+        f"{what}: max_abs beyond output rounding={max_abs:.3e} (<= {MAX_ABS}), " \
+        f"mean_rel={mean_rel:.3e} (<= {MEAN_REL})"
     return max_abs, mean_rel
 
 

@@ -65,3 +65,18 @@ def test_decode_topk_small():
     assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
     assert_attention_close(out, o_ref, "decode top-k small")
     assert_lse_close(lse, l_ref, "decode top-k lse")
+
+
+@pytest.mark.parametrize("rb", [432, 368])
+@pytest.mark.parametrize("splits", [1, 2, 7])
+def test_decode_many_tiles_per_split(rb, splits):
+    # several 64-key tiles per CTA: exercises both operand buffers, the score
+    # product split around P.V, and the lazy rescale across tiles (outliers)
+    lens = (1000, 129, 2049, 64)
+    w = workloads.decode_paged("tiles", len(lens), 128, lens, rb, perm_pages=True, outlier_frac=0.01,
+                               outlier_mult=20.0, seed=7)
+    gs = oracle_gs(w.kv_c)
+    out, lse = run_gpu(w, gs, splits)
+    o_ref, l_ref = run_oracle(w, gs)
+    assert_attention_close(out, o_ref, f"decode many tiles rb={rb} splits={splits}")
+    assert_lse_close(lse, l_ref, "decode many tiles lse")

@@ -202,3 +202,17 @@ def test_absorption_identity():
     qn = rng.standard_normal(128)
     c = rng.standard_normal(512)
     assert np.isclose(qn @ (W @ c), (qn @ W) @ c, rtol=1e-12)
+
+
+def test_bf16_rounding_allowance_matches_bf16():
+    # the decode tolerance allows half a bf16 ulp for the output rounding:
+    # rounding to bf16 must never exceed it, and must reach it at ties
+    import torch
+    from tests.helpers import bf16_half_ulp
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000),
+                        [1.0 + 2.0 ** -8, 77.25, -300.5]])
+    r = torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).to(torch.float64).numpy()
+    d = np.abs(r - x)
+    assert np.all(d <= bf16_half_ulp(x) * (1 + 1e-12))
+    assert np.isclose(d[-3], bf16_half_ulp(x[-3]))  # exact tie at 1 + 2^-8
