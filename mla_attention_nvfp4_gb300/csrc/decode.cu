@@ -35,14 +35,16 @@
 //          for two tiles: the "V part" (this CTA's 256 latent features, read
 //          by both products) and the "T part" (the other 256 latent features
 //          and the RoPE features, read by the score product only).
-//   The MMA order per tile is  QK_T(t+1), PV(t), QK_V(t+1): the softmax of
-//   tile t overlaps QK_T(t+1), and the V part of tile t+1 may be written
-//   while PV(t-1)..QK_T(t+1) run, so two buffers of each part suffice.
+//   Each issuer runs  QK_T(j), QK_V(j), PV(j)  for its tiles; the softmax
+//   of tile j overlaps the other issuer's tile j+1, and the V part of tile
+//   j+2 may be written while QK_T(j+2) runs, so two buffers of each part
+//   (one per tile parity) suffice.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0..3   Q staging, online softmax (thread = head), lazy O rescale,
 //                partial-output epilogue.
-//   warp 4       TMEM owner and MMA issuer (one thread).
+//   warps 4, 11  MMA issuers (one thread each) for even and odd tiles;
+//                warp 4 owns the TMEM allocation.
 //   warps 5..10  dequantisation: thread = (key, third of the record), 16-byte
 //                loads straight from global memory (L2-prefetched a tile
 //                ahead), e2m1 -> f16 conversion times the block scale, stores
@@ -62,9 +64,11 @@ using namespace sm100;
 
 constexpr int kTok = 64;           // keys per tile (MMA N of the score product)
 constexpr int kHeads = 128;        // heads per work unit (MMA M)
-constexpr int kThreads = 352;
-constexpr int kMmaWarp = 4;
+constexpr int kThreads = 384;
+constexpr int kMmaWarp = 4;    // MMA issuer for even tiles, TMEM owner
+constexpr int kMmaWarp2 = 11;  // MMA issuer for odd tiles
 constexpr int kDeqWarp0 = 5;
+constexpr int kDeqWarps = 6;
 constexpr uint32_t kChunk = kTok * 128;      // 64 keys x 64 features, f16
 constexpr uint32_t kQChunk = kHeads * 128;   // 128 heads x 64 features, f16
 constexpr uint32_t kVBytes = 4 * kChunk;     // V part: 4 latent chunks
@@ -86,7 +90,10 @@ constexpr uint32_t kIdescQK = idesc_f16_f32(128, kTok, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 256, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;
+// The running max is raised (and O rescaled) only when a tile's max exceeds
+// it by more than 2^14: P = 2^(s - m) then stays below 2^14, inside f16,
+// and sum P.V stays far inside fp32.
+constexpr float kRescaleThreshold = 14.0f;
 
 struct Params {
   const __nv_bfloat16* q;
@@ -150,7 +157,16 @@ __device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t,
   return slot;
 }
 
-__device__ __forceinline__ uint4 ldg16(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+// 16-byte read-only load issued where it is written (volatile): the raw
+// record bytes of the next tile must be in flight while this tile converts,
+// and an ordinary load may be scheduled next to its first use.
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -221,9 +237,169 @@ __device__ __forceinline__ void zero_units(uint32_t tile, int u0, int n, int row
     sts128(tile + (u >> 3) * kChunk + row * 128 + (((u & 7) ^ (row & 7)) << 4), make_uint4(0, 0, 0, 0));
 }
 
+// ------------------------------------------------------------ dequantisation
+// Thread = (key k of the tile, part Q): Q = 0 writes V units 0..23, Q = 1
+// T units 0..15 and V units 24..31, Q = 2 T units 16..31 and the RoPE chunk
+// (V = latent features [256 rank, +256), T = the other 256; a unit is 8
+// features).  Each thread loads the raw bytes of its part with 16-byte loads
+// straight from global memory, one tile ahead of their conversion; the
+// record itself is prefetched into L2 two tiles ahead.
+
+template <int Q, int kRecord>
+struct RawPart {
+  static constexpr int kRope = (kRecord == 368) ? 4 : 8;  // RoPE segments
+  static constexpr int kN = (Q == 0) ? 7 : (Q == 1) ? 8 : 5 + kRope;
+  uint4 v[kN];
+};
+
+template <int Q, int kRecord>
+__device__ __forceinline__ void load_part(RawPart<Q, kRecord>& r, const uint8_t* rec, int rank) {
+  const int other = 1 - rank;
+  if constexpr (Q == 0) {
+#pragma unroll
+    for (int i = 0; i < 6; ++i) r.v[i] = ldg16(rec + 128 * rank + 16 * i);
+    r.v[6] = ldg16(rec + 256 + 16 * rank);
+  } else if constexpr (Q == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.v[i] = ldg16(rec + 128 * other + 16 * i);
+    r.v[4] = ldg16(rec + 256 + 16 * other);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) r.v[5 + i] = ldg16(rec + 128 * rank + 96 + 16 * i);
+    r.v[7] = ldg16(rec + 256 + 16 * rank);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.v[i] = ldg16(rec + 128 * other + 64 + 16 * i);
+    r.v[4] = ldg16(rec + 256 + 16 * other);
+#pragma unroll
+    for (int i = 0; i < RawPart<Q, kRecord>::kRope; ++i) r.v[5 + i] = ldg16(rec + 288 + 16 * i);
+  }
+}
+
+struct DeqCtx {
+  const Params& p;
+  Barriers* bars;
+  volatile int* abort_s;
+  uint32_t sV, sT;
+  int rank, b, tile0, nt, n_keys, k;
+};
+
+// Convert part Q of key k of tile j (raw bytes in r, or zeros for a padding
+// key) into the tile's operand buffers.  False if a wait gave up.
+template <int Q, int kRecord>
+__device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPart<Q, kRecord>& r, bool valid) {
+  uint32_t* err = c.p.error_word;
+  Barriers& bars = *c.bars;
+  const int k = c.k;
+  const uint32_t tV = c.sV + (j & 1) * kVBytes, tT = c.sT + (j & 1) * kTBytes;
+  const uint32_t ph = ((j >> 1) & 1) ^ 1;  // phase in which the previous user released the buffer
+  if constexpr (Q == 0) {
+    if (!mbar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 6; ++i) dequant_segment(r.v[i], byte_of(r.v[6], 2 * i), byte_of(r.v[6], 2 * i + 1), tV, 4 * i, k);
+    } else {
+      zero_units(tV, 0, 24, k);
+    }
+    fence_async_smem();
+    mbar_arrive(&bars.v_full[j & 1]);
+  } else if constexpr (Q == 1) {
+    if (!mbar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dequant_segment(r.v[i], byte_of(r.v[4], 2 * i), byte_of(r.v[4], 2 * i + 1), tT, 4 * i, k);
+    } else {
+      zero_units(tT, 0, 16, k);
+    }
+    fence_async_smem();
+    mbar_arrive(&bars.t_full[j & 1]);
+    if (!mbar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        dequant_segment(r.v[5 + i], byte_of(r.v[7], 12 + 2 * i), byte_of(r.v[7], 13 + 2 * i), tV, 24 + 4 * i, k);
+    } else {
+      zero_units(tV, 24, 8, k);
+    }
+    fence_async_smem();
+    mbar_arrive(&bars.v_full[j & 1]);
+  } else {
+    if (!mbar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
+    const uint32_t rope_row = tT + 4 * kChunk + k * 128;
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dequant_segment(r.v[i], byte_of(r.v[4], 8 + 2 * i), byte_of(r.v[4], 9 + 2 * i), tT, 16 + 4 * i, k);
+      if constexpr (kRecord == 368) {  // e4m3 -> f16, exact
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 x = r.v[5 + i];
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 o = make_uint4(e4m3x2_to_f16x2(w[2 * h] & 0xFFFFu), e4m3x2_to_f16x2(w[2 * h] >> 16),
+                                       e4m3x2_to_f16x2(w[2 * h + 1] & 0xFFFFu), e4m3x2_to_f16x2(w[2 * h + 1] >> 16));
+            const int u = 2 * i + h;
+            sts128(rope_row + ((u ^ (k & 7)) << 4), o);
+          }
+        }
+      } else {  // bf16 -> f16
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = r.v[5 + u];
+          sts128(rope_row + ((u ^ (k & 7)) << 4),
+                 make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w)));
+        }
+      }
+    } else {
+      zero_units(tT, 16, 16, k);
+      zero_units(tT, 32, 8, k);
+    }
+    fence_async_smem();
+    mbar_arrive(&bars.t_full[j & 1]);
+  }
+  return true;
+}
+
+// The dequantisation loop of one thread.  Returns whether an out-of-range
+// page or slot id was met.
+template <int Q, int kRecord>
+__device__ bool dequant_role(const DeqCtx& c) {
+  const Params& p = c.p;
+  bool bad = false;
+  auto slot_of = [&](int j, int32_t idx) { return key_slot(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad); };
+  auto index_of = [&](int j) { return load_index(p, c.b, (c.tile0 + j) * kTok + c.k); };
+  auto prefetch = [&](int64_t slot) {
+    if (Q == 0 && slot >= 0) prefetch_l2(p.cache + slot * kRecord, kRecord);
+  };
+  const int nt = c.nt;
+  int64_t s_cur = nt > 0 ? slot_of(0, index_of(0)) : -1;  // tile j
+  int64_t s_nxt = nt > 1 ? slot_of(1, index_of(1)) : -1;  // tile j + 1
+  int32_t i_2 = nt > 2 ? index_of(2) : -1;                // index of tile j + 2
+  prefetch(s_cur);
+  prefetch(s_nxt);
+  RawPart<Q, kRecord> ra, rb;
+  if (s_cur >= 0) load_part(ra, p.cache + s_cur * kRecord, c.rank);
+  // convert tile j from `cur` while tile j+1's bytes load into `nxt`
+  auto step = [&](int j, RawPart<Q, kRecord>& cur, RawPart<Q, kRecord>& nxt) -> bool {
+    const bool valid = s_cur >= 0;
+    if (j + 1 < nt && s_nxt >= 0) load_part(nxt, p.cache + s_nxt * kRecord, c.rank);
+    const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
+    prefetch(s_2);
+    i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
+    const bool ok = convert_part<Q, kRecord>(c, j, cur, valid);
+    s_cur = s_nxt;
+    s_nxt = s_2;
+    return ok;
+  };
+  for (int j = 0; j < nt; j += 2) {
+    if (!step(j, ra, rb) || j + 1 >= nt) break;
+    if (!step(j + 1, rb, ra)) break;
+  }
+  return bad;
+}
+
 template <int kRecord>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
-  constexpr bool kFp8Rope = (kRecord == 368);
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_s;
@@ -254,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       mbar_init(&bars.p_full[i], 128);
       mbar_init(&bars.pv_done[i], 1);
     }
-    mbar_init(&bars.o_full, 1);
+    mbar_init(&bars.o_full, 2);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -266,8 +442,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp || warp == kMmaWarp2) {
     // ----------------------------------------------------------------- MMA
+    // Two issuing threads: one thread issues tcgen05.mma at roughly one
+    // instruction per 50 cycles, well below the tensor pipe's rate at N = 64,
+    // so tiles alternate between two issuers.  Every buffer (scores, T, V)
+    // is indexed by tile parity, so the issuer of parity p owns buffer p.
+    const int par = (warp == kMmaWarp) ? 0 : 1;
     if (lane == 0 && nt > 0) {
       // Descriptors are formed once; a tile, chunk or K-step offset is added
       // to the start-address field (16-byte units, no carry: shared
@@ -327,140 +508,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         const uint64_t vd = dpv + pb * (kVBytes / 16);
 #pragma unroll
         for (int kk = 0; kk < kTok / 16; ++kk)
-          mma_ts(tmem + kTO, tmem + col_s(pb) + 8 * kk, vd + (2048 * kk) / 16, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kTO, tmem + col_s(pb) + 8 * kk, vd + (2048 * kk) / 16, kIdescPV, 1u);  // O starts at 0
         mma_commit(&bars.v_empty[pb]);
         mma_commit(&bars.pv_done[pb]);
         return true;
       };
-      if (ok) ok = issue_qk_t(0);
-      if (ok) ok = issue_qk_v(0);
-      for (int t = 0; ok && t < nt; ++t) {
-        if (t + 1 < nt && !issue_qk_t(t + 1)) break;
-        if (!issue_pv(t)) break;
-        if (t + 1 < nt && !issue_qk_v(t + 1)) break;
-      }
+      // per tile: the T part of the scores, the V part, then P.V once the
+      // softmax has written P; the other issuer's tile fills the wait
+      for (int j = par; ok && j < nt; j += 2) ok = issue_qk_t(j) && issue_qk_v(j) && issue_pv(j);
       mma_commit(&bars.o_full);
-      mbar_wait(&bars.o_full, 0, err, nullptr);  // every MMA retired
+      mbar_wait(&bars.o_full, 0, err, nullptr);  // both issuers' MMAs retired
     }
-  } else if (warp >= kDeqWarp0) {
+  } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
     // ---------------------------------------------------------- dequantise
-    // thread = (key k of the tile, part q): q = 0 writes V units 0..23, q = 1
-    // V units 24..31 and T units 0..15, q = 2 T units 16..31 and the RoPE
-    // chunk.  V = latent features [256 rank, +256), T = the other 256.
     const int di = threadIdx.x - 32 * kDeqWarp0;
     const int k = di & 63, q = di >> 6;
-    const int other = 1 - rank;
-    bool bad = false;
-    int32_t idx0 = nt > 0 ? load_index(p, b, tile0 * kTok + k) : -1;
-    int32_t idx1 = nt > 1 ? load_index(p, b, (tile0 + 1) * kTok + k) : -1;
-    if (q == 0 && nt > 0) {
-      bool dummy = false;
-      const int64_t s0 = key_slot(p, idx0, tile0 * kTok + k, n_keys, dummy);
-      if (s0 >= 0) prefetch_l2(p.cache + s0 * kRecord, kRecord);
-    }
-    for (int j = 0; j < nt; ++j) {
-      const int key = (tile0 + j) * kTok + k;
-      const int64_t slot = key_slot(p, idx0, key, n_keys, bad);
-      idx0 = idx1;
-      if (j + 2 < nt) idx1 = load_index(p, b, key + 2 * kTok);
-      if (q == 0 && j + 1 < nt) {
-        bool dummy = false;
-        const int64_t sn = key_slot(p, idx0, key + kTok, n_keys, dummy);
-        if (sn >= 0) prefetch_l2(p.cache + sn * kRecord, kRecord);
-      }
-      const bool valid = slot >= 0;
-      const uint8_t* rec = p.cache + (valid ? slot : 0) * kRecord;
-      const uint32_t tV = sV + (j & 1) * kVBytes, tT = sT + (j & 1) * kTBytes;
-      const uint32_t ph_empty = ((j >> 1) & 1) ^ 1;
-      if (q == 0) {
-        uint4 c[6], sc = make_uint4(0, 0, 0, 0);
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 6; ++i) c[i] = ldg16(rec + 128 * rank + 16 * i);
-          sc = ldg16(rec + 256 + 16 * rank);
-        }
-        if (!mbar_wait(&bars.v_empty[j & 1], ph_empty, err, &abort_s)) break;
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 6; ++i) dequant_segment(c[i], byte_of(sc, 2 * i), byte_of(sc, 2 * i + 1), tV, 4 * i, k);
-        } else {
-          zero_units(tV, 0, 24, k);
-        }
-        fence_async_smem();
-        mbar_arrive(&bars.v_full[j & 1]);
-      } else if (q == 1) {
-        uint4 cv[2], ct[4], scv = make_uint4(0, 0, 0, 0), sct = make_uint4(0, 0, 0, 0);
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) ct[i] = ldg16(rec + 128 * other + 16 * i);
-          sct = ldg16(rec + 256 + 16 * other);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) cv[i] = ldg16(rec + 128 * rank + 96 + 16 * i);
-          scv = ldg16(rec + 256 + 16 * rank);
-        }
-        if (!mbar_wait(&bars.t_empty[j & 1], ph_empty, err, &abort_s)) break;
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dequant_segment(ct[i], byte_of(sct, 2 * i), byte_of(sct, 2 * i + 1), tT, 4 * i, k);
-        } else {
-          zero_units(tT, 0, 16, k);
-        }
-        fence_async_smem();
-        mbar_arrive(&bars.t_full[j & 1]);
-        if (!mbar_wait(&bars.v_empty[j & 1], ph_empty, err, &abort_s)) break;
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            dequant_segment(cv[i], byte_of(scv, 12 + 2 * i), byte_of(scv, 13 + 2 * i), tV, 24 + 4 * i, k);
-        } else {
-          zero_units(tV, 24, 8, k);
-        }
-        fence_async_smem();
-        mbar_arrive(&bars.v_full[j & 1]);
-      } else {
-        constexpr int kRopeSegs = kFp8Rope ? 4 : 8;
-        uint4 ct[4], r[kRopeSegs], sct = make_uint4(0, 0, 0, 0);
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) ct[i] = ldg16(rec + 128 * other + 64 + 16 * i);
-          sct = ldg16(rec + 256 + 16 * other);
-#pragma unroll
-          for (int i = 0; i < kRopeSegs; ++i) r[i] = ldg16(rec + 288 + 16 * i);
-        }
-        if (!mbar_wait(&bars.t_empty[j & 1], ph_empty, err, &abort_s)) break;
-        const uint32_t rope_row = tT + 4 * kChunk + k * 128;
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dequant_segment(ct[i], byte_of(sct, 8 + 2 * i), byte_of(sct, 9 + 2 * i), tT, 16 + 4 * i, k);
-          if constexpr (kFp8Rope) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint4 o = make_uint4(e4m3x2_to_f16x2(w[2 * h] & 0xFFFFu), e4m3x2_to_f16x2(w[2 * h] >> 16),
-                                           e4m3x2_to_f16x2(w[2 * h + 1] & 0xFFFFu),
-                                           e4m3x2_to_f16x2(w[2 * h + 1] >> 16));
-                const int u = 2 * i + h;
-                sts128(rope_row + ((u ^ (k & 7)) << 4), o);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              sts128(rope_row + ((u ^ (k & 7)) << 4),
-                     make_uint4(bf16x2_to_f16x2(r[u].x), bf16x2_to_f16x2(r[u].y), bf16x2_to_f16x2(r[u].z),
-                                bf16x2_to_f16x2(r[u].w)));
-          }
-        } else {
-          zero_units(tT, 16, 16, k);
-          zero_units(tT, 32, 8, k);
-        }
-        fence_async_smem();
-        mbar_arrive(&bars.t_full[j & 1]);
-      }
-    }
+    DeqCtx c{p, &bars, &abort_s, sV, sT, rank, b, tile0, nt, n_keys, k};
+    bool bad;
+    if (q == 0)
+      bad = dequant_role<0, kRecord>(c);
+    else if (q == 1)
+      bad = dequant_role<1, kRecord>(c);
+    else
+      bad = dequant_role<2, kRecord>(c);
     if (bad && rank == 0 && q == 0) flag_error(err, MLA_DEVERR_BOUNDS);
   } else {
     // ------------------------------------------- softmax and epilogue
@@ -476,64 +546,72 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
     if (nt > 0) {
       // Q -> f16 operands: TMEM [sigma*q_pe/gs, sigma*q_lat[0:192]], shared
       // memory sigma*q_lat[192:512] (swizzled rows).
-      const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(b) * p.num_heads + head) * 576;
+      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q + (static_cast<int64_t>(b) * p.num_heads + head) * 576);
       const float inv_gs = gs_ok ? 1.f / gs : 0.f;
-      float qmax = 0.f;  // max over q_lat and q_pe/gs
-      if (head_ok) {
-#pragma unroll 4
-        for (int i = 0; i < 72; ++i) {
-          const uint4 w = reinterpret_cast<const uint4*>(qrow)[i];
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-          const float f = (i < 64) ? 1.f : inv_gs;
+      // Operand order of the 72 source units (8 bf16 each): positions 0..7
+      // = q_pe (units 64..71), 8..31 = q_lat units 0..23 (TMEM, 4 columns a
+      // unit), 32..71 = q_lat units 24..63 (shared memory chunks 0..4).
+      // One pass in three batches of 24 loads converts with the given sigma
+      // and returns max(|q_lat|, |q_pe/gs|).
+      auto stage = [&](float sigma) -> float {
+        float qmax = 0.f;
+#pragma unroll 1
+        for (int g = 0; g < 3; ++g) {
+          uint4 w[24];
 #pragma unroll
-          for (int kx = 0; kx < 4; ++kx) {
-            float lo, hi;
-            bf16x2_to_f32(ws[kx], lo, hi);
-            qmax = fmaxf(qmax, fmaxf(fabsf(lo * f), fabsf(hi * f)));
+          for (int i = 0; i < 24; ++i) {
+            const int up = 24 * g + i, u = up < 8 ? 64 + up : up - 8;
+            w[i] = head_ok ? ldg16(qrow + 16 * u) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int i4 = 0; i4 < 24; i4 += 4) {
+            uint32_t v[16];
+#pragma unroll
+            for (int i = i4; i < i4 + 4; ++i) {
+              const int up = 24 * g + i;
+              const float f = up < 8 ? inv_gs : 1.f;
+              const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+              for (int kx = 0; kx < 4; ++kx) {
+                float lo, hi;
+                bf16x2_to_f32(ws[kx], lo, hi);
+                lo *= f;
+                hi *= f;
+                qmax = fmaxf(qmax, fmaxf(fabsf(lo), fabsf(hi)));
+                v[4 * (i - i4) + kx] = pack_f16(lo * sigma, hi * sigma);
+              }
+            }
+            const int up0 = 24 * g + i4;
+            if (up0 < 32) {
+              tmem_st16(tmem + lane_off + kTQRope + 4 * up0, v);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int cu = up0 - 32 + i;
+                sts128(sQ + (cu >> 3) * kQChunk + hr * 128 + (((cu & 7) ^ (hr & 7)) << 4),
+                       make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+              }
+            }
           }
         }
-      }
-      // sigma = 2^-a with sigma*qmax < 2^16 (f16 max 65504)
+        return qmax;
+      };
+      // sigma = 2^-a with sigma*qmax < 2^16 (f16 max 65504); a = 0 unless a
+      // query value reaches 2^15, in which case the row is staged again
+      const float qmax = stage(1.f);
       const int qexp = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFFu) - 127;
       const int a_sh = max(0, min(qexp - 14, 100));
-      const float sigma = __uint_as_float(static_cast<uint32_t>(127 - a_sh) << 23);
-      score_scale *= __uint_as_float(static_cast<uint32_t>(127 + a_sh) << 23);
-      // 16-byte source unit u of the row (8 bf16) -> 8 operand values
-      auto q_unit = [&](int u) -> uint4 {
-        if (!head_ok) return make_uint4(0, 0, 0, 0);
-        const uint4 w = reinterpret_cast<const uint4*>(qrow)[u];
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int kx = 0; kx < 4; ++kx) {
-          float lo, hi;
-          bf16x2_to_f32(ws[kx], lo, hi);
-          const float f = (u < 64) ? sigma : inv_gs * sigma;
-          o[kx] = pack_f16(lo * f, hi * f);
-        }
-        return make_uint4(o[0], o[1], o[2], o[3]);
-      };
-      // TMEM part: RoPE (units 64..71) then latent units 0..23
-#pragma unroll 1
-      for (int c = 0; c < 128; c += 16) {
-        uint32_t v[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int col = c + 4 * i;  // 4 columns = one unit of 8 values
-          const int u = (col < 32) ? 64 + col / 4 : (col - 32) / 4;
-          const uint4 x = q_unit(u);
-          v[4 * i] = x.x;
-          v[4 * i + 1] = x.y;
-          v[4 * i + 2] = x.z;
-          v[4 * i + 3] = x.w;
-        }
-        tmem_st16(tmem + lane_off + kTQRope + c, v);
+      if (__any_sync(0xffffffffu, a_sh > 0)) {
+        tmem_st_wait();  // the first pass's TMEM stores land before the second's
+        stage(__uint_as_float(static_cast<uint32_t>(127 - a_sh) << 23));
       }
-      // shared-memory part: latent units 24..63 -> chunks 0..4 of sQ
-#pragma unroll 4
-      for (int u = 24; u < 64; ++u) {
-        const int cu = u - 24;
-        sts128(sQ + (cu >> 3) * kQChunk + hr * 128 + (((cu & 7) ^ (hr & 7)) << 4), q_unit(u));
+      score_scale *= __uint_as_float(static_cast<uint32_t>(127 + a_sh) << 23);
+      {  // O starts at zero: every P.V accumulates, whichever issuer runs first
+        uint32_t z[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 16) tmem_st16(tmem + lane_off + kTO + c, z);
       }
       fence_async_smem();
       tmem_st_wait();
@@ -557,40 +635,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
           break;
         }
         tc_fence_after();
+        // raw scores: four loads in flight, one wait
         float x[kTok];
+        {
+          uint32_t v[4][16];
 #pragma unroll
-        for (int c = 0; c < kTok; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_off + col_s(pb) + c, v);
+          for (int c = 0; c < 4; ++c) tmem_ld16(tmem + lane_off + col_s(pb) + 16 * c, v[c]);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
+          for (int c = 0; c < kTok; ++c) x[c] = __uint_as_float(v[c >> 4][c & 15]);
         }
+        // max of the raw scores (score_scale > 0), padding keys at -inf; the
+        // scale is applied inside the exponent below
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if ((va & vb) == 0xffffffffu) {
 #pragma unroll
-          for (int c = 0; c < kTok; ++c) {
-            x[c] *= score_scale;
-            mq[c & 3] = fmaxf(mq[c & 3], x[c]);
-          }
+          for (int c = 0; c < kTok; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
         } else {
 #pragma unroll
           for (int c = 0; c < kTok; ++c) {
             const unsigned m = c < 32 ? va : vb;
-            x[c] = ((m >> (c & 31)) & 1u) ? x[c] * score_scale : -INFINITY;
+            x[c] = ((m >> (c & 31)) & 1u) ? x[c] : -INFINITY;
             mq[c & 3] = fmaxf(mq[c & 3], x[c]);
           }
         }
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * score_scale;  // log2 units
         float m_use = m_run, alpha = 1.f;
         const bool raise = mx > m_run + kRescaleThreshold;
         if (raise) {
           m_use = mx;
           alpha = ex2_approx(m_run - mx);
         }
-        // an O rescale needs PV(j-1) retired and must precede PV(j)
+        // an O rescale must follow every earlier P.V and precede PV(j).
+        // PV(j-1) and PV(j-2) come from different issuers; each issuer's
+        // earlier P.V products retire before its later ones.
         if (__any_sync(0xffffffffu, raise && j > 0)) {
-          if (!mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s)) {
+          if (!mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s) ||
+              (j >= 2 && !mbar_wait(&bars.pv_done[j & 1], ((j - 2) >> 1) & 1, err, &abort_s))) {
             ok = false;
             break;
           }
@@ -612,9 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         uint32_t pv[kTok / 2];
 #pragma unroll
         for (int i = 0; i < kTok / 2; ++i) {
-          const float p0 = ex2_approx(x[2 * i] - m_ref), p1 = ex2_approx(x[2 * i + 1] - m_ref);
+          const float p0 = ex2_approx(fmaf(x[2 * i], score_scale, -m_ref));
+          const float p1 = ex2_approx(fmaf(x[2 * i + 1], score_scale, -m_ref));
           ls[i & 3] += p0 + p1;
-          pv[i] = pack_f16(p0, p1);  // P <= 2^8 (lazy reference), f16 operand
+          pv[i] = pack_f16(p0, p1);  // P <= 2^14 (lazy reference), f16 operand
         }
         l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         // P(j) over S(j): the buffer's previous P was read by PV(j-2), which

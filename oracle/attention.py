@@ -80,22 +80,26 @@ def decode_slots_topk(topk_indices):
     return out
 
 
-def decode(q, cache, record_bytes, gs, softmax_scale, slots_per_seq):
+def decode(q, cache, record_bytes, gs, softmax_scale, slots_per_seq, with_abs=False):
     """q [B,H,576] (bf16 values), cache [num_slots, record_bytes] u8.
 
-    Returns (out [B,H,512], lse [B,H]) in float64.
+    Returns (out [B,H,512], lse [B,H]) in float64; with ``with_abs`` also
+    softmax(s) @ |x_hat|, the scale of any rounding of the probabilities.
     """
     q = np.asarray(q, dtype=np.float64)
     B, H, D = q.shape
     assert D == D_QK_DECODE
     out = np.zeros((B, H, D_V_DECODE))
+    out_abs = np.zeros((B, H, D_V_DECODE)) if with_abs else None
     lse = np.zeros((B, H))
     for b in range(B):
         slots = slots_per_seq[b]
         lat, rope = cache_mod.decode_records(cache[slots], gs, record_bytes)
         k = np.concatenate([lat, rope], axis=1)
         out[b], lse[b] = attend(q[b], k, lat, softmax_scale)
-    return out, lse
+        if with_abs:
+            out_abs[b], _ = attend(q[b], k, np.abs(lat), softmax_scale)
+    return (out, lse, out_abs) if with_abs else (out, lse)
 
 
 def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None, with_abs=False):

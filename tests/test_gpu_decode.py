@@ -31,8 +31,9 @@ def run_gpu(w, gs, num_splits=0):
 
 
 def run_oracle(w, gs):
+    """(out, lse, softmax @ |v|) of the float64 oracle."""
     c = oracle_cache(w, gs)
-    return attention.decode(f32(w.q), c, w.record_bytes, gs, w.softmax_scale, oracle_slots(w))
+    return attention.decode(f32(w.q), c, w.record_bytes, gs, w.softmax_scale, oracle_slots(w), with_abs=True)
 
 
 @pytest.mark.parametrize("rb", [432, 368])
@@ -41,8 +42,8 @@ def test_decode_tiny(rb, splits):
     w = workloads.decode_tiny(record_bytes=rb)
     gs = oracle_gs(w.kv_c)
     out, lse = run_gpu(w, gs, splits)
-    o_ref, l_ref = run_oracle(w, gs)
-    assert_attention_close(out, o_ref, f"decode tiny rb={rb} splits={splits}")
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(out, o_ref, f"decode tiny rb={rb} splits={splits}", o_abs)
     assert_lse_close(lse, l_ref, "decode tiny lse")
 
 
@@ -51,8 +52,8 @@ def test_decode_shapes(heads, lens):
     w = workloads.decode_paged("sweep", len(lens), heads, lens, 432, perm_pages=True, seed=3)
     gs = oracle_gs(w.kv_c)
     out, lse = run_gpu(w, gs)
-    o_ref, l_ref = run_oracle(w, gs)
-    assert_attention_close(out, o_ref, f"decode heads={heads} lens={lens}")
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(out, o_ref, f"decode heads={heads} lens={lens}", o_abs)
     assert_lse_close(lse, l_ref, "decode lse")
 
 
@@ -61,9 +62,9 @@ def test_decode_topk_small():
     w.topk_indices[2, :] = -1  # a row with nothing to attend to
     gs = oracle_gs(w.kv_c)
     out, lse = run_gpu(w, gs)
-    o_ref, l_ref = run_oracle(w, gs)
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
     assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
-    assert_attention_close(out, o_ref, "decode top-k small")
+    assert_attention_close(out, o_ref, "decode top-k small", o_abs)
     assert_lse_close(lse, l_ref, "decode top-k lse")
 
 
@@ -77,6 +78,23 @@ def test_decode_many_tiles_per_split(rb, splits):
                                outlier_mult=20.0, seed=7)
     gs = oracle_gs(w.kv_c)
     out, lse = run_gpu(w, gs, splits)
-    o_ref, l_ref = run_oracle(w, gs)
-    assert_attention_close(out, o_ref, f"decode many tiles rb={rb} splits={splits}")
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(out, o_ref, f"decode many tiles rb={rb} splits={splits}", o_abs)
     assert_lse_close(lse, l_ref, "decode many tiles lse")
+
+
+@pytest.mark.parametrize("case", ["small_latent", "large_query"])
+def test_decode_query_range_scaling(case):
+    # q_pe/gs or q itself beyond the f16 range: the query is staged with a
+    # per-head power-of-two scale, undone in the score scale
+    w = workloads.decode_paged("range", 2, 64, (300, 77), 432, perm_pages=True, seed=9)
+    if case == "small_latent":
+        w.kv_c = (w.kv_c.float() * 1e-3).to(torch.bfloat16)  # gs ~ 2e-6: q_pe/gs ~ 1e6
+    else:
+        w.q = (w.q.float() * 3e4).to(torch.bfloat16)
+        w.softmax_scale = w.softmax_scale / 3e4
+    gs = oracle_gs(w.kv_c)
+    out, lse = run_gpu(w, gs, 1)
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(out, o_ref, f"decode query range {case}", o_abs)
+    assert_lse_close(lse, l_ref, f"decode query range {case} lse")

@@ -49,8 +49,10 @@ def _check(w, samples):
         got = cache[w.slot_mapping[tok]].cpu().numpy()
         assert np.array_equal(got, rec), f"{w.name} seq {b}: cache records differ"
         lat, rope = ocache.decode_records(rec, gs, w.record_bytes)
-        o_ref, l_ref = attention.attend(f32(w.q[b]), np.concatenate([lat, rope], 1), lat, w.softmax_scale)
-        assert_attention_close(f32(out[b]), o_ref, f"{w.name} seq {b}")
+        k = np.concatenate([lat, rope], 1)
+        o_ref, l_ref = attention.attend(f32(w.q[b]), k, lat, w.softmax_scale)
+        o_abs, _ = attention.attend(f32(w.q[b]), k, np.abs(lat), w.softmax_scale)
+        assert_attention_close(f32(out[b]), o_ref, f"{w.name} seq {b}", o_abs)
         assert_lse_close(f32(lse[b]), l_ref, f"{w.name} seq {b} lse")
 
 

@@ -216,3 +216,15 @@ def test_bf16_rounding_allowance_matches_bf16():
     d = np.abs(r - x)
     assert np.all(d <= bf16_half_ulp(x) * (1 + 1e-12))
     assert np.isclose(d[-3], bf16_half_ulp(x[-3]))  # exact tie at 1 + 2^-8
+
+
+def test_decode_with_abs_bounds_output():
+    # softmax @ |v| bounds |softmax @ v| elementwise
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((4, 6))
+    k = rng.standard_normal((9, 6))
+    v = rng.standard_normal((9, 3))
+    o, _ = attention.attend(q, k, v, 0.5)
+    oa, _ = attention.attend(q, k, np.abs(v), 0.5)
+    assert np.all(oa >= np.abs(o) - 1e-15)
+    assert np.any(oa > np.abs(o) + 1e-3)  # mixed signs: strictly larger somewhere
