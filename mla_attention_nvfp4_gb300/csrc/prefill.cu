@@ -253,23 +253,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
       }
       tmem_ld_wait();
+      // max of the raw scores (scale_log2 > 0); the scale is applied inside
+      // the exponent below
       const int key0 = j * kBN + c0;
       float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (key0 + 63 > qi) {  // diagonal tile: mask keys after the query
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          x[c] = (key0 + c <= qi) ? x[c] * p.scale_log2 : -INFINITY;
+          x[c] = (key0 + c <= qi) ? x[c] : -INFINITY;
           mq[c & 3] = fmaxf(mq[c & 3], x[c]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] *= p.scale_log2;
-          mq[c & 3] = fmaxf(mq[c & 3], x[c]);
-        }
+        for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
       }
       // row max over both halves (also orders every S read before any P write)
-      red_s[b][g][r] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      red_s[b][g][r] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
       mbar_arrive(&bars.red[b]);
       if (!mbar_wait(&bars.red[b], ph, err, &abort_s)) {
         ok = false;
@@ -281,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool raise = mx > m_run + kRescaleThreshold;
       if (raise) {
         m_use = mx;
-        alpha = exp2f(m_run - mx);  // 0 on the first tile
+        alpha = ex2_approx(m_run - mx);  // 0 on the first tile
       }
       const bool warp_rescale = __any_sync(0xffffffffu, raise && j > 0);
       if (warp_rescale) {
@@ -309,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = exp2f(x[c + 2 * i] - m_use), p1 = exp2f(x[c + 2 * i + 1] - m_use);
+          const float p0 = ex2_approx(fmaf(x[c + 2 * i], p.scale_log2, -m_use));
+          const float p1 = ex2_approx(fmaf(x[c + 2 * i + 1], p.scale_log2, -m_use));
           ls[i & 3] += p0 + p1;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           v[i] = *reinterpret_cast<uint32_t*>(&h2);
