@@ -161,7 +161,8 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
 
     # --- workload (device-resident), seed 0 -----------------------------
-    w = workloads.decode_dsv3(device=dev)
+    w = workloads.decode_dsv3(device=dev, batch=16 if args.case == "decode-steady" else 64)
+    decode_splits = 1 if args.case == "decode-steady" else 0
     if args.case == "profile":
         # the same legs on a prefill of 2 x 4096 tokens (about 1.8 GB on the
         # device in all), for ncu captures; never a bench value
@@ -173,7 +174,7 @@ def run_ours(args, rank, world):
     cache = torch.zeros((w.num_slots, w.record_bytes), dtype=torch.uint8, device=dev)
     out = torch.empty((w.batch, w.heads, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.batch, w.heads), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(256, mla.mla_nvfp4_decode_workspace_size(w.batch, w.heads)), dtype=torch.uint8,
+    ws = torch.empty(max(256, mla.mla_nvfp4_decode_workspace_size(w.batch, w.heads, decode_splits)), dtype=torch.uint8,
                      device=dev)
     codes = torch.empty((p.total_tokens, p.heads * 64), dtype=torch.uint8, device=dev)
     scales = torch.empty(mla.prefill_scale_bytes(p.total_tokens, p.heads), dtype=torch.uint8, device=dev)
@@ -185,7 +186,7 @@ def run_ours(args, rank, world):
 
     def leg_decode():
         mla.mla_nvfp4_decode(w.q, cache, gs, w.softmax_scale, page_table=w.page_table, seq_lens=w.seq_lens,
-                             out=out, lse=lse, workspace=ws, error_word=err)
+                             out=out, lse=lse, workspace=ws, error_word=err, num_splits=decode_splits)
 
     def leg_prefill():
         mla.mla_nvfp4_prefill_fused_out(p.q, p.k, p.v, p.cu_seqlens, p.max_seqlen, p.softmax_scale, gsp,
@@ -277,7 +278,7 @@ def run_ours(args, rank, world):
             d_pt.copy_(h_pt, non_blocking=True)
             d_sl.copy_(h_sl, non_blocking=True)
             mla.mla_nvfp4_decode(d_q, cache, gs, w.softmax_scale, page_table=d_pt, seq_lens=d_sl, out=out,
-                                 workspace=ws, error_word=err)
+                                 workspace=ws, error_word=err, num_splits=decode_splits)
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -392,8 +393,9 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--case", default="full", choices=["full", "profile"],
-                    help="profile: smaller prefill input for ncu captures (not a bench value)")
+    ap.add_argument("--case", default="full", choices=["full", "profile", "decode-steady"],
+                    help="profile: smaller prefill input; decode-steady: decode of 16 x 4096 keys in one "
+                         "split (64 tiles per CTA); both for ncu captures, not bench values")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -417,7 +419,8 @@ def main():
                     "sample": sample}
     line = run_ours(args, rank, world)
     if args.case != "full":
-        line["config"]["workload"] = "PROFILE CASE (prefill 2x4096), not a bench value: " + WORKLOAD
+        what = "prefill 2x4096" if args.case == "profile" else "decode 16x4096, one split"
+        line["config"]["workload"] = f"PROFILE CASE ({what}), not a bench value: " + WORKLOAD
     if rank == 0:
         line["cpu_baseline"] = cpu_line
         print(json.dumps(line))
