@@ -46,9 +46,9 @@
 //   warps 4, 11  MMA issuers (one thread each) for even and odd tiles;
 //                warp 4 owns the TMEM allocation.
 //   warps 5..10  dequantisation: thread = (key, third of the record), 16-byte
-//                loads straight from global memory (L2-prefetched a tile
-//                ahead), e2m1 -> f16 conversion times the block scale, stores
-//                into the swizzled operand tiles.
+//                loads straight from global memory a tile ahead, e2m1 -> f16
+//                conversion times the block scale, stores into the swizzled
+//                operand tiles.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -128,13 +128,19 @@ struct alignas(8) Barriers {
 // (the page-table entry or the top-k index of key position t, clamped into
 // its row); key_slot() then turns that value into a slot id, or -1 for
 // padding / positions past the sequence, and notes out-of-range ids.
+__device__ __forceinline__ int32_t ldg_i32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ int32_t load_index(const Params& p, int b, int t) {
   if (p.topk != nullptr) {
     const int tc = min(max(t, 0), max(p.topk_n - 1, 0));
-    return p.topk[static_cast<int64_t>(b) * p.topk_n + tc];
+    return ldg_i32(p.topk + static_cast<int64_t>(b) * p.topk_n + tc);
   }
   const int pi = min(max(t, 0) / p.page_size, static_cast<int>(p.pt_stride) - 1);
-  return p.page_table[static_cast<int64_t>(b) * p.pt_stride + pi];
+  return ldg_i32(p.page_table + static_cast<int64_t>(b) * p.pt_stride + pi);
 }
 
 __device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t, int n_keys, bool& bad) {
@@ -166,10 +172,6 @@ __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
@@ -242,8 +244,9 @@ __device__ __forceinline__ void zero_units(uint32_t tile, int u0, int n, int row
 // T units 0..15 and V units 24..31, Q = 2 T units 16..31 and the RoPE chunk
 // (V = latent features [256 rank, +256), T = the other 256; a unit is 8
 // features).  Each thread loads the raw bytes of its part with 16-byte loads
-// straight from global memory, one tile ahead of their conversion; the
-// record itself is prefetched into L2 two tiles ahead.
+// straight from global memory, one tile (about 3 us) ahead of their
+// conversion.  (A bulk L2 prefetch of each record, issued per key, held the
+// issuing thread for thousands of cycles per tile and was dropped.)
 
 template <int Q, int kRecord>
 struct RawPart {
@@ -368,15 +371,11 @@ __device__ bool dequant_role(const DeqCtx& c) {
   bool bad = false;
   auto slot_of = [&](int j, int32_t idx) { return key_slot(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad); };
   auto index_of = [&](int j) { return load_index(p, c.b, (c.tile0 + j) * kTok + c.k); };
-  auto prefetch = [&](int64_t slot) {
-    if (Q == 0 && slot >= 0) prefetch_l2(p.cache + slot * kRecord, kRecord);
-  };
+
   const int nt = c.nt;
   int64_t s_cur = nt > 0 ? slot_of(0, index_of(0)) : -1;  // tile j
   int64_t s_nxt = nt > 1 ? slot_of(1, index_of(1)) : -1;  // tile j + 1
   int32_t i_2 = nt > 2 ? index_of(2) : -1;                // index of tile j + 2
-  prefetch(s_cur);
-  prefetch(s_nxt);
   RawPart<Q, kRecord> ra, rb;
   if (s_cur >= 0) load_part(ra, p.cache + s_cur * kRecord, c.rank);
   // convert tile j from `cur` while tile j+1's bytes load into `nxt`
@@ -384,7 +383,6 @@ __device__ bool dequant_role(const DeqCtx& c) {
     const bool valid = s_cur >= 0;
     if (j + 1 < nt && s_nxt >= 0) load_part(nxt, p.cache + s_nxt * kRecord, c.rank);
     const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
-    prefetch(s_2);
     i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
     const bool ok = convert_part<Q, kRecord>(c, j, cur, valid);
     s_cur = s_nxt;
