@@ -149,6 +149,27 @@ def _traffic(kernel: str):
     return d["bytes_per_launch"]
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank timings over the process group: the
+    slowest rank sets the whole job's time.  NCCL reduces on the GPU, gloo
+    (CPU tests) on the host."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Weak scaling: every rank processes the same units (independent
+    batches), so the job's rate is all ranks' units over the slowest rank's
+    time in milliseconds."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_ours(args, rank, world):
     import torch
     import mla_attention_nvfp4_gb300 as mla
@@ -227,17 +248,14 @@ def run_ours(args, rank, world):
         wall = time.perf_counter() - t0
     leg_ms = {n: sum(a.elapsed_time(b) for a, b in rec[n]) / args.steps for n in rec}
     step_ms = sum(leg_ms.values())
-    if world > 1:
-        t = torch.tensor([step_ms, leg_ms["decode"], leg_ms["prefill"], leg_ms["cache_write"]],
-                         dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, leg_ms["decode"], leg_ms["prefill"], leg_ms["cache_write"] = t.tolist()
+    step_ms, leg_ms["decode"], leg_ms["prefill"], leg_ms["cache_write"] = max_over_ranks(
+        [step_ms, leg_ms["decode"], leg_ms["prefill"], leg_ms["cache_write"]], world, dev)
 
     dec_b, cw_b = decode_bytes(w), cache_write_bytes(w)
     pf_flops, dec_flops = prefill_flops(p), decode_flops(w)
-    decode_gbs = world * dec_b / (leg_ms["decode"] * 1e-3) / 1e9
-    prefill_tflops = world * pf_flops / (leg_ms["prefill"] * 1e-3) / 1e12
-    cw_gbs = world * cw_b / (leg_ms["cache_write"] * 1e-3) / 1e9
+    decode_gbs = whole_job_rate(dec_b, world, leg_ms["decode"]) / 1e9
+    prefill_tflops = whole_job_rate(pf_flops, world, leg_ms["prefill"]) / 1e12
+    cw_gbs = whole_job_rate(cw_b, world, leg_ms["cache_write"]) / 1e9
     hbm = float(peaks["hbm_gbs"])
     bf16_burst = float(peaks["bf16_tflops"])
     fp32_alu = SM_COUNT * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12  # CUDA-core fp32 FMA peak
