@@ -215,6 +215,17 @@ int mla_nvfp4_decode_noalloc(const void* q, int batch, int num_heads, const uint
  *   lse          : fp32 [num_heads, total_tokens] or NULL.
  * Query i of a sequence attends to keys 0..i of the same sequence; the
  * normalised fp32 output rows are quantised with blocks of 16 along d.
+ *   Scheduling   : one CTA per SM takes work items from a device counter in
+ *                  the library (64 counters, used in turn, each back at zero
+ *                  when its launch ends).  Up to 64 calls may run at once on
+ *                  one device (different streams); the first call on a
+ *                  device looks the counters up (cudaGetSymbolAddress) and
+ *                  should come before any stream capture begins.
+ *   Errors       : MLA_ERR_INVALID_ARG for bad sizes, strides or alignment
+ *                  (nothing launched); device-side, MLA_DEVERR_BOUNDS in
+ *                  *error_word when cu_seqlens is out of range or a sequence
+ *                  is longer than max_seqlen, MLA_DEVERR_SCALE for a global
+ *                  scale outside [2^-100, 2^100].
  */
 int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
                                 int64_t q_stride_t, int64_t q_stride_h, int64_t k_stride_t,

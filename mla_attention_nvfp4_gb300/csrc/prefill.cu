@@ -11,24 +11,43 @@
 // first commit message (varlen prefill with asymmetric 192/128 head dims,
 // natural-log LSE).
 //
-// One CTA = one 128-row query tile of one (sequence, head).  Warp roles:
-//   warp 0      TMA producer: Q once, then K/V tiles of 128 keys into a
-//               two-stage ring (128-byte swizzled, K-major rows).
-//   warp 1      TMEM owner and MMA issuer (one thread):
-//                 S_j = Q K_j^T       M=128 N=128 K=192, A and B from smem
-//                 O  += P_j V_j       M=128 N=128 K=128, A (P) from TMEM,
-//                                     B = V tile read MN-major
-//   warps 2..9  softmax, O correction and epilogue: two warpgroups, each
-//               thread one query row and one half (64 columns) of S and O.
-// TMEM columns: S double buffer [0,128) [128,256); O [256,384).  P_j (bf16)
-// overwrites the first 64 columns of its S buffer after the row is read.
-// The running max is only raised when a row's max grows by more than 8
-// (log2 units), so O is rarely rescaled; P stays <= 2^8, exact enough in
-// bf16, and numerator and denominator share the same reference.
+// Persistent: one CTA per SM takes work items (query tile of 128 rows of
+// one sequence and head) from a launch-wide counter.  Items are numbered
+// (sequence, head) major with the last query tile first, so the CTAs working
+// at the same moment share the keys they read (L2 reuse) and each group's
+// heaviest tile starts first.  The key blocks of one CTA's items form one
+// stream, so the next item's first score product is issued before the
+// current item's last P.V and the tensor pipe does not drain between items;
+// a separate epilogue warpgroup quantises an item's output while the next
+// item runs.
+// Warp roles (448 threads):
+//   warp 0       scheduler and TMA producer: takes items, hands their
+//                indices to the other roles through a shared-memory ring,
+//                loads K/V blocks of 128 keys into a two-stage ring
+//                (128-byte swizzled, K-major rows) and, per item, Q once the
+//                previous item's last score product has read it; the next
+//                item is taken one item ahead and its Q tile prefetched into
+//                L2.
+//   warp 1       TMEM owner and MMA issuer (one thread):
+//                  S_g = Q K_g^T   M=128 N=128 K=192, A and B from smem
+//                  O  += P_g V_g   M=128 N=128 K=128, A (P) from TMEM,
+//                                  B = V tile read MN-major
+//                in the order S_g, P.V of block g-1 (of any item).
+//   warps 2..9   softmax and O correction: two warpgroups, each thread one
+//                query row and one half (64 columns) of S.
+//   warps 10..13 epilogue: thread = query row of the finished item.
+// TMEM columns: S [0,128) [128,256) by block parity, O [256,384)
+// [384,512) by item parity.  P_g (bf16) overwrites the first 64 columns of
+// its S buffer after the row is read.  The running max is only raised when a
+// row's max grows by more than 8 (log2 units), so O is rarely rescaled; P
+// stays <= 2^8, exact enough in bf16, and numerator and denominator share the
+// same reference.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "launch.h"
 #include "nvfp4.cuh"
@@ -40,7 +59,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128, kBN = 128, kDqk = 192, kDv = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr uint32_t kQBytes = kBM * kDqk * 2;  // 49152
 constexpr uint32_t kKBytes = kBN * kDqk * 2;  // 49152
 constexpr uint32_t kVBytes = kBN * kDv * 2;   // 32768
@@ -62,7 +81,9 @@ struct Params {
   int num_seqs;
   int64_t total;
   int num_heads;
-  int q_tiles;  // grid.x
+  int q_tiles;          // query tiles of the longest sequence
+  uint32_t num_items;   // q_tiles * num_seqs * num_heads
+  uint32_t* sched;      // [0] next item, [1] CTAs finished; zero between launches
   float scale_log2;
   const float* gs;
   uint8_t* codes;
@@ -71,14 +92,73 @@ struct Params {
   uint32_t* error_word;
 };
 
+constexpr int kRing = 4;  // item indices in flight from the producer to the other roles
+
 struct alignas(8) Barriers {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, o_full;
-  uint64_t red[2], red_l;  // the two softmax groups exchanging row maxima / sums
+  uint64_t pv_done, mma_done;
+  uint64_t red[2];                            // the two softmax groups exchanging row maxima
+  uint64_t o_full[2], o_empty[2], l_full[2];  // by item parity: MMA/softmax -> epilogue -> MMA
+  uint64_t item_full[kRing], item_empty[kRing];
 };
+
+// Work item idx: (sequence, head) major, then query tiles from the last one
+// down, so the items that read the same keys run at about the same time and
+// the heaviest tile of each (sequence, head) starts first.
+struct Item {
+  int h, seq_begin, n, row0, n_kv;
+  bool valid;
+};
+
+__device__ __forceinline__ Item item_at(const Params& p, uint32_t idx, bool& bad) {
+  const uint32_t group = idx / static_cast<uint32_t>(p.q_tiles);
+  const int qt = p.q_tiles - 1 - static_cast<int>(idx % static_cast<uint32_t>(p.q_tiles));
+  const int seq = static_cast<int>(group / static_cast<uint32_t>(p.num_heads));
+  Item it;
+  it.h = static_cast<int>(group % static_cast<uint32_t>(p.num_heads));
+  it.seq_begin = p.cu[seq];
+  const int seq_end = p.cu[seq + 1];
+  it.n = seq_end - it.seq_begin;
+  it.row0 = qt * kBM;
+  if (it.seq_begin < 0 || seq_end > p.total || it.n < 0 || it.n > p.q_tiles * kBM) {
+    bad = true;
+    it.n = 0;
+  }
+  it.valid = it.row0 < it.n;
+  it.n_kv = it.valid ? (min(it.n, it.row0 + kBM) - 1) / kBN + 1 : 0;  // causal: keys < row0 + 128
+  return it;
+}
+
+// Next valid item from the launch-wide counter, or -1 when none is left.
+// The tiles of a group past its sequence's end come first in the group, so
+// one invalid index moves the counter to the group's first valid tile.
+__device__ int grab_item(const Params& p, bool& bad) {
+  for (;;) {
+    const uint32_t idx = atomicAdd(p.sched, 1u);
+    if (idx >= p.num_items) return -1;
+    const Item w = item_at(p, idx, bad);
+    if (w.valid) return static_cast<int>(idx);
+    const uint32_t group = idx / static_cast<uint32_t>(p.q_tiles);
+    const uint32_t tiles = static_cast<uint32_t>((w.n + kBM - 1) / kBM);
+    atomicMax(p.sched, group * static_cast<uint32_t>(p.q_tiles) + static_cast<uint32_t>(p.q_tiles) - tiles);
+  }
+}
+
+// L2 prefetch of one box of a tensor map (no shared memory written).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0), "r"(c1),
+               "r"(c2)
+               : "memory");
+}
+
+// A wait whose outcome is the same in every lane, so that the warp-wide
+// tcgen05 loads and stores after it are reached by all lanes or by none.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* err, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, abort));
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -87,29 +167,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
-  __shared__ float red_s[2][2][kBM];  // per-group row maxima, double-buffered by tile parity
-  __shared__ float red_l[2][kBM];     // per-group row sums
+  __shared__ int ring_s[kRing];       // item index, -1 = no more items
+  __shared__ float red_s[2][2][kBM];  // per-group row maxima, by block parity
+  __shared__ float l_s[2][2][kBM];    // per-group row sums, by item parity
+  __shared__ float m_s[2][kBM];       // row reference maxima, by item parity
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y, seq = blockIdx.z;
-  const int tile = p.q_tiles - 1 - static_cast<int>(blockIdx.x);  // heavy (late) tiles first
   const int64_t k_tiles_sf = (static_cast<int64_t>(p.num_heads) * 8 + 3) / 4;
 
-  // rows [total, roundup(total,128)) of this head's scale columns are zero
-  if (blockIdx.x == 0 && seq == 0) {
+  // rows [total, roundup(total,128)) of the scale columns are zero
+  {
     const int64_t Mp = (p.total + 127) / 128 * 128;
-    for (int64_t i = threadIdx.x; i < (Mp - p.total) * 8; i += kThreads)
-      p.scales[sf_offset(p.total + i / 8, static_cast<int64_t>(h) * 8 + i % 8, k_tiles_sf)] = 0;
+    const int64_t pad = (Mp - p.total) * 8;
+    for (int h = blockIdx.x; h < p.num_heads; h += gridDim.x)
+      for (int64_t i = threadIdx.x; i < pad; i += kThreads)
+        p.scales[sf_offset(p.total + i / 8, static_cast<int64_t>(h) * 8 + i % 8, k_tiles_sf)] = 0;
   }
-  const int seq_begin = p.cu[seq], seq_end = p.cu[seq + 1];
-  const int n = seq_end - seq_begin;
-  if (seq_begin < 0 || seq_end > p.total || n < 0) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) flag_error(p.error_word, MLA_DEVERR_BOUNDS);
-    return;
-  }
-  const int row0 = tile * kBM;
-  if (row0 >= n) return;
-  const int n_kv = (min(n, row0 + kBM) - 1) / kBN + 1;  // causal: keys < row0 + 128
   const float gs = *p.gs;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -120,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_s = 0;
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -127,12 +201,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.v_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
       mbar_init(&bars.p_full[s], 256);
+      mbar_init(&bars.red[s], 256);
+      mbar_init(&bars.o_full[s], 1);
+      mbar_init(&bars.o_empty[s], 128);
+      mbar_init(&bars.l_full[s], 256);
+    }
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&bars.item_full[s], 1);
+      mbar_init(&bars.item_empty[s], 1 + 256 + 128);  // MMA thread, softmax, epilogue
     }
     mbar_init(&bars.pv_done, 1);
-    mbar_init(&bars.o_full, 1);
-    mbar_init(&bars.red[0], 256);
-    mbar_init(&bars.red[1], 256);
-    mbar_init(&bars.red_l, 256);
+    mbar_init(&bars.mma_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -144,8 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const uint32_t tS0 = tmem, tS1 = tmem + 128;
-  const uint32_t tO = tmem + 256;
+  const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
   uint32_t* err = p.error_word;
+  bool bad = false;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -153,29 +233,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      const int tok0 = seq_begin + row0;
-      mbar_expect_tx(&bars.q_full, kQBytes);
-      for (int cb = 0; cb < 3; ++cb) tma_load_3d(sQ + cb * 16384, &tm_q, cb * 64, h, tok0, &bars.q_full);
-      int j = 0;
-      for (; j < n_kv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        const int key0 = seq_begin + j * kBN;
-        if (!mbar_wait(&bars.k_empty[s], ph ^ 1, err, &abort_s)) break;
-        mbar_expect_tx(&bars.k_full[s], kKBytes);
-        for (int cb = 0; cb < 3; ++cb)
-          tma_load_3d(sK + s * kKBytes + cb * 16384, &tm_k, cb * 64, h, key0, &bars.k_full[s]);
-        if (!mbar_wait(&bars.v_empty[s], ph ^ 1, err, &abort_s)) break;
-        mbar_expect_tx(&bars.v_full[s], kVBytes);
-        for (int cb = 0; cb < 2; ++cb)
-          tma_load_3d(sV + s * kVBytes + cb * 16384, &tm_v, cb * 64, h, key0, &bars.v_full[s]);
+      int nq = 0, nk = 0, nv = 0;  // Q tiles, K blocks and V blocks whose copies were issued
+      int cur = grab_item(p, bad);
+      for (int it = 0;; ++it) {
+        // publish the item (or the end) to the other roles
+        if (!mbar_wait(&bars.item_empty[it % kRing], ((it / kRing) & 1) ^ 1, err, &abort_s)) break;
+        ring_s[it % kRing] = cur;
+        mbar_arrive(&bars.item_full[it % kRing]);
+        if (cur < 0) break;
+        const Item w = item_at(p, static_cast<uint32_t>(cur), bad);
+        // the next item is taken now so that its Q tile can be brought into L2
+        const int nxt = grab_item(p, bad);
+        if (nxt >= 0) {
+          bool dummy = false;
+          const Item w2 = item_at(p, static_cast<uint32_t>(nxt), dummy);
+          for (int cb = 0; cb < 3; ++cb) tma_prefetch_3d(&tm_q, cb * 64, w2.h, w2.seq_begin + w2.row0);
+        }
+        bool ok = true;
+        for (int j = 0; j < w.n_kv; ++j) {
+          const int s = nk & 1;  // nk == nv here: global block index
+          const uint32_t ph = (nk >> 1) & 1;
+          const int key0 = w.seq_begin + j * kBN;
+          if (!(ok = mbar_wait(&bars.k_empty[s], ph ^ 1, err, &abort_s))) break;
+          mbar_expect_tx(&bars.k_full[s], kKBytes);
+          for (int cb = 0; cb < 3; ++cb)
+            tma_load_3d(sK + s * kKBytes + cb * 16384, &tm_k, cb * 64, w.h, key0, &bars.k_full[s]);
+          ++nk;
+          if (j == 0) {  // Q of this item, once the previous item's last score product has read it
+            if (!(ok = mbar_wait(&bars.q_empty, (nq & 1) ^ 1, err, &abort_s))) break;
+            mbar_expect_tx(&bars.q_full, kQBytes);
+            for (int cb = 0; cb < 3; ++cb)
+              tma_load_3d(sQ + cb * 16384, &tm_q, cb * 64, w.h, w.seq_begin + w.row0, &bars.q_full);
+            ++nq;
+          }
+          if (!(ok = mbar_wait(&bars.v_empty[s], ph ^ 1, err, &abort_s))) break;
+          mbar_expect_tx(&bars.v_full[s], kVBytes);
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_3d(sV + s * kVBytes + cb * 16384, &tm_v, cb * 64, w.h, key0, &bars.v_full[s]);
+          ++nv;
+        }
+        if (!ok) break;
+        cur = nxt;
       }
       // every copy issued has landed before the CTA can exit
-      mbar_wait(&bars.q_full, 0, err, nullptr);
-      for (int jj = max(0, j - 2); jj < j; ++jj) {
-        mbar_wait(&bars.k_full[jj & 1], (jj >> 1) & 1, err, nullptr);
-        mbar_wait(&bars.v_full[jj & 1], (jj >> 1) & 1, err, nullptr);
-      }
+      if (nq > 0) mbar_wait(&bars.q_full, (nq - 1) & 1, err, nullptr);
+      for (int g = max(0, nk - 2); g < nk; ++g) mbar_wait(&bars.k_full[g & 1], (g >> 1) & 1, err, nullptr);
+      for (int g = max(0, nv - 2); g < nv; ++g) mbar_wait(&bars.v_full[g & 1], (g >> 1) & 1, err, nullptr);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -186,189 +289,279 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq = smem_desc_sw128(q_addr, 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(k_addr, 0, 1024), dk1 = smem_desc_sw128(k_addr + kKBytes, 0, 1024);
       const uint64_t dv0 = smem_desc_sw128(v_addr, 16384, 1024), dv1 = smem_desc_sw128(v_addr + kVBytes, 16384, 1024);
-      bool ok = mbar_wait(&bars.q_full, 0, err, &abort_s);
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(&bars.p_full[b], ph, err, &abort_s)) return false;
-        if (!mbar_wait(&bars.v_full[b], ph, err, &abort_s)) return false;
+      // the P.V product of block g, its item's parity, first / last block of the item
+      struct PV {
+        int g, it;
+        bool first, last;
+      };
+      auto issue_pv = [&](const PV& b) -> bool {
+        const int s = b.g & 1;
+        const uint32_t ph = (b.g >> 1) & 1;
+        const int o = b.it & 1;
+        // the first P.V of an item overwrites O[o]: the epilogue of the item
+        // two before must have read it
+        if (b.first && !mbar_wait(&bars.o_empty[o], ((b.it >> 1) & 1) ^ 1, err, &abort_s)) return false;
+        if (!mbar_wait(&bars.p_full[s], ph, err, &abort_s)) return false;
+        if (!mbar_wait(&bars.v_full[s], ph, err, &abort_s)) return false;
         tc_fence_after();
-        const uint64_t vd = b ? dv1 : dv0;
+        const uint64_t vd = s ? dv1 : dv0;
+        const uint32_t tO = o ? tO1 : tO0;
+        const uint32_t tP = s ? tS1 : tS0;
+        if (b.first) {
+          mma_ts(tO, tP, vd, kIdescPV, 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tO, (b ? tS1 : tS0) + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.v_empty[b]);
+          for (int kk = 1; kk < kBN / 16; ++kk) mma_ts(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, 1u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) mma_ts(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, 1u);
+        }
+        mma_commit(&bars.v_empty[s]);
         mma_commit(&bars.pv_done);
+        if (b.last) mma_commit(&bars.o_full[o]);
         return true;
       };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&bars.k_full[s], ph, err, &abort_s)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t kd = s ? dk1 : dk0;
+      int gb = 0, nq = 0;
+      bool ok = true, pending = false;
+      PV pv{0, 0, false, false};
+      for (int it = 0; ok; ++it) {
+        if (!mbar_wait(&bars.item_full[it % kRing], (it / kRing) & 1, err, &abort_s)) break;
+        const int idx = ring_s[it % kRing];
+        mbar_arrive(&bars.item_empty[it % kRing]);
+        if (idx < 0) break;
+        bool dummy = false;
+        const Item w = item_at(p, static_cast<uint32_t>(idx), dummy);
+        for (int j = 0; j < w.n_kv; ++j, ++gb) {
+          const int s = gb & 1;
+          const uint32_t ph = (gb >> 1) & 1;
+          if (j == 0 && !mbar_wait(&bars.q_full, nq & 1, err, &abort_s)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&bars.k_full[s], ph, err, &abort_s)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd = s ? dk1 : dk0;
+          const uint32_t tS = s ? tS1 : tS0;
+          mma_ss(tS, dq, kd, kIdescS, 0u);
 #pragma unroll
-        for (int kk = 0; kk < kDqk / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_ss(s ? tS1 : tS0, dq + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
+          for (int kk = 1; kk < kDqk / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(tS, dq + off, kd + off, kIdescS, 1u);
+          }
+          mma_commit(&bars.s_full[s]);
+          mma_commit(&bars.k_empty[s]);
+          if (j == w.n_kv - 1) {
+            mma_commit(&bars.q_empty);
+            ++nq;
+          }
+          if (pending && !issue_pv(pv)) {
+            ok = false;
+            break;
+          }
+          pv = PV{gb, it, j == 0, j == w.n_kv - 1};
+          pending = true;
         }
-        mma_commit(&bars.s_full[s]);
-        mma_commit(&bars.k_empty[s]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
       }
-      if (ok) issue_pv(n_kv - 1);
-      mma_commit(&bars.o_full);
-      mbar_wait(&bars.o_full, 0, err, nullptr);  // all MMAs retired
+      if (ok && pending) issue_pv(pv);
+      if (gb > 0) {
+        mma_commit(&bars.mma_done);
+        mbar_wait(&bars.mma_done, 0, err, nullptr);  // every MMA retired
+      }
     }
-  } else {
-    // ------------------------------------------------- softmax + epilogue
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ softmax
     // Two warpgroups share each row: group g handles score columns
-    // [64g, 64g+64) and output columns [64g, 64g+64).  Row maxima and sums
-    // are combined through shared memory.
+    // [64g, 64g+64).  Row maxima are combined through shared memory.
     const int g = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int qi = row0 + r;         // query index within the sequence
-    const int c0 = 64 * g;           // first score / output column of this group
-    float m_run = -INFINITY, l_run = 0.f;
+    const int c0 = 64 * g;           // first score column of this group
+    int gb = 0;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait(&bars.s_full[b], ph, err, &abort_s)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float x[64];
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t v[16];
-        tmem_ld16((b ? tS1 : tS0) + lane_off + c0 + c, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
-      }
-      tmem_ld_wait();
-      // max of the raw scores (scale_log2 > 0); the scale is applied inside
-      // the exponent below
-      const int key0 = j * kBN + c0;
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (key0 + 63 > qi) {  // diagonal tile: mask keys after the query
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          x[c] = (key0 + c <= qi) ? x[c] : -INFINITY;
-          mq[c & 3] = fmaxf(mq[c & 3], x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
-      }
-      // row max over both halves (also orders every S read before any P write)
-      red_s[b][g][r] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
-      mbar_arrive(&bars.red[b]);
-      if (!mbar_wait(&bars.red[b], ph, err, &abort_s)) {
-        ok = false;
-        break;
-      }
-      const float mx = fmaxf(red_s[b][0][r], red_s[b][1][r]);
-      // lazy reference update (identical in both groups)
-      float m_use = m_run, alpha = 1.f;
-      const bool raise = mx > m_run + kRescaleThreshold;
-      if (raise) {
-        m_use = mx;
-        alpha = ex2_approx(m_run - mx);  // 0 on the first tile
-      }
-      const bool warp_rescale = __any_sync(0xffffffffu, raise && j > 0);
-      if (warp_rescale) {
-        // O must not be in flight: PV_{j-1} has to be complete
-        if (!mbar_wait(&bars.pv_done, (j - 1) & 1, err, &abort_s)) {
+    for (int it = 0; ok; ++it) {
+      if (!warp_wait(&bars.item_full[it % kRing], (it / kRing) & 1, err, &abort_s)) break;
+      const int idx = ring_s[it % kRing];
+      mbar_arrive(&bars.item_empty[it % kRing]);
+      if (idx < 0) break;
+      bool dummy = false;
+      const Item w = item_at(p, static_cast<uint32_t>(idx), dummy);
+      const int qi = w.row0 + r;  // query index within the sequence
+      const uint32_t tO = (it & 1) ? tO1 : tO0;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < w.n_kv; ++j, ++gb) {
+        const int b = gb & 1;
+        const uint32_t ph = (gb >> 1) & 1;
+        if (!warp_wait(&bars.s_full[b], ph, err, &abort_s)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        float x[64];
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
           uint32_t v[16];
-          tmem_ld16(tO + lane_off + c0 + c, v);
-          tmem_ld_wait();
+          tmem_ld16((b ? tS1 : tS0) + lane_off + c0 + c, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st16(tO + lane_off + c0 + c, v);
+          for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
         }
+        tmem_ld_wait();
+        // max of the raw scores (scale_log2 > 0); the scale is applied
+        // inside the exponent below
+        const int key0 = j * kBN + c0;
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (key0 + 63 > qi) {  // diagonal block: mask keys after the query
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            x[c] = (key0 + c <= qi) ? x[c] : -INFINITY;
+            mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+        }
+        // row max over both halves (also orders every S read before any P write)
+        red_s[b][g][r] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
+        mbar_arrive(&bars.red[b]);
+        if (!warp_wait(&bars.red[b], ph, err, &abort_s)) {
+          ok = false;
+          break;
+        }
+        const float mx = fmaxf(red_s[b][0][r], red_s[b][1][r]);
+        // lazy reference update (identical in both groups)
+        float m_use = m_run, alpha = 1.f;
+        const bool raise = mx > m_run + kRescaleThreshold;
+        if (raise) {
+          m_use = mx;
+          alpha = ex2_approx(m_run - mx);  // 0 on the first block
+        }
+        if (__any_sync(0xffffffffu, raise && j > 0)) {
+          // O must not be in flight: the previous P.V (block gb-1, this item)
+          if (!warp_wait(&bars.pv_done, (gb - 1) & 1, err, &abort_s)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(tO + lane_off + c0 + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st16(tO + lane_off + c0 + c, v);
+          }
+          tmem_st_wait();
+        }
+        m_run = m_use;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {  // P as bf16 pairs: columns [32g, 32g+32) of the S buffer
+          uint32_t v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2_approx(fmaf(x[c + 2 * i], p.scale_log2, -m_use));
+            const float p1 = ex2_approx(fmaf(x[c + 2 * i + 1], p.scale_log2, -m_use));
+            ls[i & 3] += p0 + p1;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            v[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          tmem_st16((b ? tS1 : tS0) + lane_off + 32 * g + c / 2, v);
+        }
+        l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.p_full[b]);
       }
-      m_run = m_use;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 64; c += 32) {  // P as bf16 pairs: columns [32g, 32g+32) of the S buffer
-        uint32_t v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(x[c + 2 * i], p.scale_log2, -m_use));
-          const float p1 = ex2_approx(fmaf(x[c + 2 * i + 1], p.scale_log2, -m_use));
-          ls[i & 3] += p0 + p1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          v[i] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-        tmem_st16((b ? tS1 : tS0) + lane_off + 32 * g + c / 2, v);
-      }
-      l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars.p_full[b]);
+      if (!ok) break;
+      // row statistics for the epilogue; the slot of this item parity is
+      // free once the epilogue of the item two before has read it
+      if (!warp_wait(&bars.o_empty[it & 1], ((it >> 1) & 1) ^ 1, err, &abort_s)) break;
+      l_s[it & 1][g][r] = l_run;
+      if (g == 0) m_s[it & 1][r] = m_run;
+      mbar_arrive(&bars.l_full[it & 1]);
     }
-    // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(&bars.o_full, 0, err, &abort_s)) {
-      red_l[g][r] = l_run;
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const bool gs_ok = scale_ok(gs);
+    const float kf = scale_factor(gs);
+    for (int it = 0;; ++it) {
+      if (!warp_wait(&bars.item_full[it % kRing], (it / kRing) & 1, err, &abort_s)) break;
+      const int idx = ring_s[it % kRing];
+      mbar_arrive(&bars.item_empty[it % kRing]);
+      if (idx < 0) break;
+      bool dummy = false;
+      const Item w = item_at(p, static_cast<uint32_t>(idx), dummy);
+      const int o = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!warp_wait(&bars.o_full[o], ph, err, &abort_s) || !warp_wait(&bars.l_full[o], ph, err, &abort_s)) break;
       tc_fence_after();
-      float o[64];
+      const float l_tot = l_s[o][0][r] + l_s[o][1][r];
+      const float m_row = m_s[o][r];
+      const int qi = w.row0 + r;
+      const uint32_t tO = o ? tO1 : tO0;
+      const int64_t m = w.seq_begin + qi;
+      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float ov[64];
 #pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(tO + lane_off + c0 + c, v);
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(tO + lane_off + 64 * half + c, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[c + i] = __uint_as_float(v[i]);
-      }
-      tmem_ld_wait();
-      mbar_arrive(&bars.red_l);
-      mbar_wait(&bars.red_l, 0, err, &abort_s);
-      const float l_tot = red_l[0][r] + red_l[1][r];
-      if (qi < n) {
-        const int64_t m = seq_begin + qi;
-        const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) o[c] *= inv_l;
-        const bool gs_ok = scale_ok(gs);
-        const float kf = scale_factor(gs);
-        uint32_t w[8];
-        uint32_t sb[4];
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          float R = 0.f;
-          sb[blk] = gs_ok ? block_scale(fmaxf(amax8(o + 16 * blk), amax8(o + 16 * blk + 8)), kf, gs, R) : 0u;
-          w[2 * blk] = gs_ok ? encode8(o + 16 * blk, R) : 0u;
-          w[2 * blk + 1] = gs_ok ? encode8(o + 16 * blk + 8, R) : 0u;
+          for (int i = 0; i < 16; ++i) ov[c + i] = __uint_as_float(v[i]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + h * 64 + 32 * g);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        const int64_t kc = static_cast<int64_t>(h) * 8 + 4 * g;
-        *reinterpret_cast<uint32_t*>(p.scales + sf_offset(m, kc, k_tiles_sf)) =
-            sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
-        if (g == 0 && p.lse != nullptr)
-          p.lse[static_cast<int64_t>(h) * p.total + m] = l_tot > 0.f ? (m_run + log2f(l_tot)) * kLn2 : -INFINITY;
-        if (!gs_ok && qi == 0 && g == 0) flag_error(err, MLA_DEVERR_SCALE);
+        tmem_ld_wait();
+        if (qi < w.n) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) ov[c] *= inv_l;
+          uint32_t wd[8];
+          uint32_t sb[4];
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            float R = 0.f;
+            sb[blk] = gs_ok ? block_scale(fmaxf(amax8(ov + 16 * blk), amax8(ov + 16 * blk + 8)), kf, gs, R) : 0u;
+            wd[2 * blk] = gs_ok ? encode8(ov + 16 * blk, R) : 0u;
+            wd[2 * blk + 1] = gs_ok ? encode8(ov + 16 * blk + 8, R) : 0u;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + w.h * 64 +
+                                                32 * half);
+          dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+          const int64_t kc = static_cast<int64_t>(w.h) * 8 + 4 * half;
+          *reinterpret_cast<uint32_t*>(p.scales + sf_offset(m, kc, k_tiles_sf)) =
+              sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+        }
       }
+      if (qi < w.n) {
+        if (p.lse != nullptr)
+          p.lse[static_cast<int64_t>(w.h) * p.total + m] = l_tot > 0.f ? (m_row + log2f(l_tot)) * kLn2 : -INFINITY;
+        if (!gs_ok && qi == 0) flag_error(err, MLA_DEVERR_SCALE);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars.o_empty[o]);
     }
   }
+  if (bad) flag_error(err, MLA_DEVERR_BOUNDS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // the last CTA to finish returns the counter to zero for the next launch
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      __threadfence();
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
+  }
 }
 
 // --------------------------------------------------------------- host side
@@ -405,9 +598,40 @@ bool make_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t T,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Work counters: kSchedSlots pairs (next item, CTAs finished), each zero
+// between launches.  Successive launches take successive slots, so launches
+// that overlap on the device (other streams) use different counters unless
+// kSchedSlots of them are in flight at once.
+constexpr int kSchedSlots = 64;
+__device__ uint32_t g_sched[kSchedSlots][2];
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint32_t*> g_sched_base[kMaxDevices];
+std::atomic<uint32_t> g_sched_next{0};
+std::mutex g_sched_setup;
+
+int sched_counter(uint32_t** out) {
+  int dev = 0;
+  if (const int st = cuda_status(cudaGetDevice(&dev))) return st;
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_LAUNCH;
+  uint32_t* base = g_sched_base[dev].load(std::memory_order_acquire);
+  if (base == nullptr) {
+    std::lock_guard<std::mutex> lock(g_sched_setup);
+    base = g_sched_base[dev].load(std::memory_order_relaxed);
+    if (base == nullptr) {
+      void* ptr = nullptr;
+      if (const int st = cuda_status(cudaGetSymbolAddress(&ptr, g_sched))) return st;
+      base = static_cast<uint32_t*>(ptr);
+      g_sched_base[dev].store(base, std::memory_order_release);
+    }
+  }
+  *out = base + 2 * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+  return MLA_OK;
+}
+
 }  // namespace
 
-int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int /*num_sms*/) {
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms) {
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, a.q, kDqk, a.num_heads, a.total_tokens, a.q_st, a.q_sh) ||
       !make_map(&tk, a.k, kDqk, a.num_heads, a.total_tokens, a.k_st, a.k_sh) ||
@@ -419,6 +643,10 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int /*num_sms*/) {
   p.total = a.total_tokens;
   p.num_heads = a.num_heads;
   p.q_tiles = (a.max_seqlen + kBM - 1) / kBM;
+  const int64_t items = static_cast<int64_t>(p.q_tiles) * a.num_seqs * a.num_heads;
+  if (items > (int64_t(1) << 31) - 1) return MLA_ERR_INVALID_ARG;
+  p.num_items = static_cast<uint32_t>(items);
+  if (const int st = sched_counter(&p.sched)) return st;
   p.scale_log2 = a.softmax_scale * kLog2e;
   p.gs = a.gs;
   p.codes = a.out_codes;
@@ -427,8 +655,9 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int /*num_sms*/) {
   p.error_word = a.error_word;
   if (const int st = cuda_status(cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemAlloc)))) return st;
-  dim3 grid(p.q_tiles, a.num_heads, a.num_seqs);
-  if (grid.y > 65535u || grid.z > 65535u) return MLA_ERR_INVALID_ARG;
+  if (p.num_items == 0) return MLA_OK;
+  // persistent: one CTA per SM
+  const int grid = p.num_items < static_cast<uint32_t>(num_sms) ? static_cast<int>(p.num_items) : num_sms;
   prefill_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
   return launch_status();
 }

@@ -140,13 +140,15 @@ def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None, with_abs=False):
     return (o, lse, o_abs) if with_abs else (o, lse)
 
 
-def prefill_rows(q, k, v, cu_seqlens, softmax_scale, rows, head):
-    """Causal prefill for selected global query rows of one head (sampling)."""
+def prefill_rows(q, k, v, cu_seqlens, softmax_scale, rows, head, with_abs=False):
+    """Causal prefill for selected global query rows of one head (sampling).
+    With ``with_abs`` also softmax(s) @ |v| for those rows."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     o = np.zeros((len(rows), v.shape[2]))
+    o_abs = np.zeros((len(rows), v.shape[2]))
     lse = np.zeros(len(rows))
     for i, r in enumerate(rows):
         s = int(np.searchsorted(cu, r, side="right") - 1)
@@ -154,4 +156,6 @@ def prefill_rows(q, k, v, cu_seqlens, softmax_scale, rows, head):
         kk = k[a:r + 1, head]
         o_i, l_i = attend(q[r:r + 1, head], kk, v[a:r + 1, head], softmax_scale)
         o[i], lse[i] = o_i[0], l_i[0]
-    return o, lse
+        if with_abs:
+            o_abs[i] = attend(q[r:r + 1, head], kk, np.abs(v[a:r + 1, head]), softmax_scale)[0][0]
+    return (o, lse, o_abs) if with_abs else (o, lse)

@@ -106,11 +106,18 @@ def check_fused_output(codes_gpu, scales_gpu, o_ref, o_abs, gs):
     where value/scale lies within err/scale of an e2m1 midpoint (or its
     block's scale differs).  Returns (scale mismatches, code mismatches)."""
     M, N = o_ref.shape
+    return check_fused_blocks(codes_gpu, swizzle.unswizzle_scales(scales_gpu, M, N // 16), o_ref, o_abs, gs)
+
+
+def check_fused_blocks(codes_gpu, sf_gpu, o_ref, o_abs, gs):
+    """check_fused_output with the kernel's scale bytes already in row-major
+    [M, N/16] order (used for sampled rows of a large output)."""
+    M, N = o_ref.shape
     K = N // 16
     x = o_ref.astype(np.float32)
     err = (P_ROUNDING * np.asarray(o_abs, dtype=np.float64) + 1e-6 * np.abs(o_ref)).reshape(M, N) + 1e-30
     codes_ref, sb_ref = nvfp4.quantize_blocks(x, gs)
-    sf_gpu = swizzle.unswizzle_scales(scales_gpu, M, K)
+    sf_gpu = np.asarray(sf_gpu).reshape(M, K)
     codes_g = nvfp4.unpack_e2m1(codes_gpu.reshape(M, N // 2))
     sb_ref = sb_ref.reshape(M, K)
     # scales

@@ -12,7 +12,7 @@ import torch
 import mla_attention_nvfp4_gb300 as mla
 from mla_attention_nvfp4_gb300 import workloads
 from oracle import attention, swizzle
-from tests.helpers import assert_lse_close, check_fused_output, f32, oracle_gs
+from tests.helpers import assert_lse_close, check_fused_blocks, check_fused_output, f32, oracle_gs
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
@@ -30,7 +30,9 @@ def _run(w, gs):
     return codes.cpu().numpy(), sf.cpu().numpy(), f32(lse)
 
 
-@pytest.mark.parametrize("lens,heads", [((1, 37, 128, 200), 4), ((129,), 2), ((64, 64, 1), 3)])
+@pytest.mark.parametrize("lens,heads", [((1, 37, 128, 200), 4), ((129,), 2), ((64, 64, 1), 3),
+                                       # several work items per CTA, an empty sequence, ragged tails
+                                       ((1000, 0, 2500, 300, 777, 1), 16)])
 def test_prefill_small(lens, heads):
     w = workloads.prefill("small", seq_lens=lens, heads=heads, seed=sum(lens))
     gs = oracle_gs(w.v)
@@ -51,3 +53,54 @@ def test_prefill_small(lens, heads):
     Mp = (T + 127) // 128 * 128
     m, k = np.meshgrid(np.arange(T, Mp), np.arange(heads * 8), indexing="ij")
     assert np.all(sf[swizzle.sf_offset(m, k, heads * 8)] == 0)
+
+
+def test_prefill_repeated_launches():
+    # the work counter returns to zero after every launch: many launches in a
+    # row (more than the counter slots) give identical outputs
+    w = workloads.prefill("small", seq_lens=(37, 300, 5), heads=3, seed=7)
+    gs = oracle_gs(w.v)
+    gst = torch.tensor([gs], device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    args = (w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), w.cu_seqlens.to(DEV), w.max_seqlen, w.softmax_scale, gst)
+    first = mla.mla_nvfp4_prefill_fused_out(*args, return_lse=True, error_word=err)
+    for _ in range(80):
+        again = mla.mla_nvfp4_prefill_fused_out(*args, return_lse=True, error_word=err)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
+def test_prefill_full_size_sampled():
+    """8 sequences x 4096 tokens x 128 heads (the benchmark's prefill): sampled
+    rows of three heads against the oracle, one row at a time."""
+    w = workloads.prefill_8x4096(device=DEV)
+    gs = oracle_gs(w.v[:4096, :8].cpu())
+    gst = torch.tensor([gs], device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    codes, sf, lse = mla.mla_nvfp4_prefill_fused_out(w.q, w.k, w.v, w.cu_seqlens, w.max_seqlen, w.softmax_scale,
+                                                    gst, return_lse=True, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    T, H = w.total_tokens, w.heads
+    rng = np.random.default_rng(11)
+    rows = set()
+    for s in range(8):
+        a = 4096 * s
+        rows.update([a, a + 1, a + 127, a + 128, a + 4095])  # tile edges, first and last rows
+        rows.update((a + rng.integers(0, 4096, 6)).tolist())
+    rows = sorted(rows)
+    cu = w.cu_seqlens.cpu().numpy()
+    sf_np = sf.cpu().numpy()
+    for h in (0, 57, 127):
+        # the oracle sees exactly the device's bf16 values of this head
+        q = f32(w.q[:, h:h + 1])
+        k = f32(w.k[:, h:h + 1])
+        v = f32(w.v[:, h:h + 1])
+        o_ref, l_ref, o_abs = attention.prefill_rows(q, k, v, cu, w.softmax_scale, rows, head=0, with_abs=True)
+        c_rows = codes[rows][:, h * 64:(h + 1) * 64].cpu().numpy()
+        m, kk = np.meshgrid(np.array(rows), np.arange(h * 8, h * 8 + 8), indexing="ij")
+        sf_rows = sf_np[swizzle.sf_offset(m, kk, H * 8)]
+        check_fused_blocks(c_rows, sf_rows, o_ref, o_abs, gs)
+        assert_lse_close(f32(lse[h, rows]), l_ref, f"prefill lse head {h}")

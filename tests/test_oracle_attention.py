@@ -193,6 +193,14 @@ def test_prefill_matches_causal_sdpa():
     orow, lrow = attention.prefill_rows(q, k, v, cu, SCALE, rows, head=2)
     np.testing.assert_allclose(orow, o[rows, 2], atol=1e-14)
     np.testing.assert_allclose(lrow, lse[2, rows], rtol=1e-14)
+    # the sampled |v| bound: >= |o| elementwise, and equal to the full
+    # oracle's; for the first row of a sequence it is |v| of that row
+    o_f, _, oabs_f = attention.prefill(q, k, v, cu, SCALE, heads=[2], with_abs=True)
+    orow2, _, oabs_rows = attention.prefill_rows(q, k, v, cu, SCALE, rows, head=2, with_abs=True)
+    np.testing.assert_allclose(orow2, orow, atol=0)
+    np.testing.assert_allclose(oabs_rows, oabs_f[rows, 2], atol=1e-14)
+    assert np.all(oabs_rows >= np.abs(orow2) - 1e-14)
+    np.testing.assert_allclose(oabs_rows[0], np.abs(v[0, 2].astype(np.float64)), atol=1e-15)
 
 
 def test_absorption_identity():
