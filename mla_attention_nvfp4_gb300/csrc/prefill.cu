@@ -19,29 +19,42 @@
 // stream, so the next item's first score product is issued before the
 // current item's last P.V and the tensor pipe does not drain between items;
 // a separate epilogue warpgroup quantises an item's output while the next
-// item runs.
-// Warp roles (448 threads):
+// item's first score products and softmax run.
+// Warp roles (512 threads, four warpgroups):
 //   warp 0       scheduler and TMA producer: takes items, hands their
 //                indices to the other roles through a shared-memory ring,
-//                loads K/V blocks of 128 keys into a two-stage ring
-//                (128-byte swizzled, K-major rows) and, per item, Q once the
-//                previous item's last score product has read it; the next
-//                item is taken one item ahead and its Q tile prefetched into
-//                L2.
-//   warp 1       TMEM owner and MMA issuer (one thread):
+//                loads K and V blocks of 128 keys into two-stage rings
+//                (128-byte swizzled rows; the K slot of block g is free once
+//                S_{g-2} completed, the V slot once P.V of block g-2 did)
+//                and, per item, Q once the previous item's last score
+//                products have read it; the next item is taken one item
+//                ahead and its Q tile prefetched into L2.
+//   warps 1, 3   MMA issuers, one thread each.  Issuer w takes the key
+//                blocks of parity w:
 //                  S_g = Q K_g^T   M=128 N=128 K=192, A and B from smem
-//                  O  += P_g V_g   M=128 N=128 K=128, A (P) from TMEM,
+//                  O_w += P_g V_g  M=128 N=128 K=128, A (P) from TMEM,
 //                                  B = V tile read MN-major
-//                in the order S_g, P.V of block g-1 (of any item).
-//   warps 2..9   softmax and O correction: two warpgroups, each thread one
-//                query row and one half (64 columns) of S.
-//   warps 10..13 epilogue: thread = query row of the finished item.
-// TMEM columns: S [0,128) [128,256) by block parity, O [256,384)
-// [384,512) by item parity.  P_g (bf16) overwrites the first 64 columns of
-// its S buffer after the row is read.  The running max is only raised when a
-// row's max grows by more than 8 (log2 units), so O is rarely rescaled; P
-// stays <= 2^8, exact enough in bf16, and numerator and denominator share the
-// same reference.
+//                in the order S_g, P.V of g, S_{g+2}: in-order issue from
+//                one thread keeps S_{g+2} behind the P.V that reads P_g in
+//                the same TMEM buffer.  A thread's barrier polls queue behind
+//                its own MMAs, so one issuer per parity keeps the tensor pipe
+//                fed from the other issuer while one waits.
+//   warps 4..11  softmax: warpgroup w takes the key blocks of parity w, one
+//                thread per query row over all 128 keys, with its own
+//                running max, row sum and partial O_w.  The two warpgroups
+//                never exchange data inside an item.  A warpgroup signals
+//                P_g ready only once V_g has landed, so the issuer waits on
+//                one barrier before P.V.
+//   warps 12..15 epilogue: thread = query row; merges the two partial
+//                results by their row maxima and sums (the split-K merge of
+//                online softmax), normalises, quantises to NVFP4 and stores.
+// Registers are moved to the softmax warpgroups with setmaxnreg.
+// TMEM columns: S/P of even and odd blocks [0,128) [128,256), partial O of
+// even and odd blocks [256,384) [384,512).  P_g (bf16) overwrites the first
+// 64 columns of its S buffer after the row is read.  A partial's reference
+// max is only raised when a row's max grows by more than 8 (log2 units), so
+// O_w is rarely rescaled; P stays <= 2^8, exact enough in bf16, and
+// numerator and denominator share the same reference.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -59,7 +72,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128, kBN = 128, kDqk = 192, kDv = 128;
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 constexpr uint32_t kQBytes = kBM * kDqk * 2;  // 49152
 constexpr uint32_t kKBytes = kBN * kDqk * 2;  // 49152
 constexpr uint32_t kVBytes = kBN * kDv * 2;   // 32768
@@ -96,18 +109,21 @@ constexpr int kRing = 4;  // item indices in flight from the producer to the oth
 
 struct alignas(8) Barriers {
   uint64_t q_full, q_empty;
-  uint64_t k_full[2], k_empty[2];
+  uint64_t k_full[2];  // a K slot is free again once S of its previous block completed (s_full)
   uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, mma_done;
-  uint64_t red[2];                            // the two softmax groups exchanging row maxima
-  uint64_t o_full[2], o_empty[2], l_full[2];  // by item parity: MMA/softmax -> epilogue -> MMA
+  uint64_t s_full[2], p_full[2];  // by block parity = softmax warpgroup = MMA issuer
+  uint64_t o_full;                // both issuers' P.V of an item retired
+  uint64_t mma_done[2];           // every MMA of issuer 0 / 1 retired
+  uint64_t o_empty[2], l_full[2];  // by item parity: epilogue -> MMA / softmax; softmax -> epilogue
   uint64_t item_full[kRing], item_empty[kRing];
 };
 
-// Work item idx: (sequence, head) major, then query tiles from the last one
-// down, so the items that read the same keys run at about the same time and
-// the heaviest tile of each (sequence, head) starts first.
+// Register split (setmaxnreg), per thread: the launch gives 128 to each of
+// the four warpgroups; producer/MMA and epilogue give some back to the two
+// softmax warpgroups, which keep a whole score row in registers.
+constexpr int kRegsCtl = 56, kRegsSoftmax = 176, kRegsEpi = 104;
+static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsEpi <= 4 * 128, "register split exceeds the launch's registers");
+
 struct Item {
   int h, seq_begin, n, row0, n_kv;
   bool valid;
@@ -167,10 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
-  __shared__ int ring_s[kRing];       // item index, -1 = no more items
-  __shared__ float red_s[2][2][kBM];  // per-group row maxima, by block parity
-  __shared__ float l_s[2][2][kBM];    // per-group row sums, by item parity
-  __shared__ float m_s[2][kBM];       // row reference maxima, by item parity
+  __shared__ int ring_s[kRing];     // item index, -1 = no more items
+  __shared__ float l_s[2][2][kBM];  // [item parity][warpgroup][row] partial row sums
+  __shared__ float m_s[2][2][kBM];  // matching reference maxima (log2 units)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t k_tiles_sf = (static_cast<int64_t>(p.num_heads) * 8 + 3) / 4;
@@ -193,25 +208,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_s = 0;
     mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, 1);
+    mbar_init(&bars.q_empty, 2);  // one arrival per MMA issuer
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.k_full[s], 1);
-      mbar_init(&bars.k_empty[s], 1);
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.p_full[s], 256);
-      mbar_init(&bars.red[s], 256);
-      mbar_init(&bars.o_full[s], 1);
+      mbar_init(&bars.p_full[s], 128);
+      mbar_init(&bars.mma_done[s], 1);
       mbar_init(&bars.o_empty[s], 128);
       mbar_init(&bars.l_full[s], 256);
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&bars.item_full[s], 1);
-      mbar_init(&bars.item_empty[s], 1 + 256 + 128);  // MMA thread, softmax, epilogue
+      mbar_init(&bars.item_empty[s], 2 + 256 + 128);  // MMA issuers, softmax, epilogue
     }
-    mbar_init(&bars.pv_done, 1);
-    mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.o_full, 2);  // one arrival per MMA issuer
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -222,18 +234,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t tS0 = tmem, tS1 = tmem + 128;
-  const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
+  // TMEM columns: S of the even / odd key blocks, and the two partial O
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO[2] = {tmem + 256, tmem + 384};
   uint32_t* err = p.error_word;
   bool bad = false;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------ scheduler, K and Q
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      int nq = 0, nk = 0, nv = 0;  // Q tiles, K blocks and V blocks whose copies were issued
+      int nq = 0, nk = 0, nv = 0;  // Q tiles, K and V blocks whose copies were issued
       int cur = grab_item(p, bad);
       for (int it = 0;; ++it) {
         // publish the item (or the end) to the other roles
@@ -251,13 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bool ok = true;
         for (int j = 0; j < w.n_kv; ++j) {
-          const int s = nk & 1;  // nk == nv here: global block index
+          const int s = nk & 1;  // global block index
           const uint32_t ph = (nk >> 1) & 1;
-          const int key0 = w.seq_begin + j * kBN;
-          if (!(ok = mbar_wait(&bars.k_empty[s], ph ^ 1, err, &abort_s))) break;
+          if (!(ok = mbar_wait(&bars.s_full[s], ph ^ 1, err, &abort_s))) break;
           mbar_expect_tx(&bars.k_full[s], kKBytes);
           for (int cb = 0; cb < 3; ++cb)
-            tma_load_3d(sK + s * kKBytes + cb * 16384, &tm_k, cb * 64, w.h, key0, &bars.k_full[s]);
+            tma_load_3d(sK + s * kKBytes + cb * 16384, &tm_k, cb * 64, w.h, w.seq_begin + j * kBN, &bars.k_full[s]);
           ++nk;
           if (j == 0) {  // Q of this item, once the previous item's last score product has read it
             if (!(ok = mbar_wait(&bars.q_empty, (nq & 1) ^ 1, err, &abort_s))) break;
@@ -269,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(&bars.v_empty[s], ph ^ 1, err, &abort_s))) break;
           mbar_expect_tx(&bars.v_full[s], kVBytes);
           for (int cb = 0; cb < 2; ++cb)
-            tma_load_3d(sV + s * kVBytes + cb * 16384, &tm_v, cb * 64, w.h, key0, &bars.v_full[s]);
+            tma_load_3d(sV + s * kVBytes + cb * 16384, &tm_v, cb * 64, w.h, w.seq_begin + j * kBN, &bars.v_full[s]);
           ++nv;
         }
         if (!ok) break;
@@ -279,107 +292,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nq > 0) mbar_wait(&bars.q_full, (nq - 1) & 1, err, nullptr);
       for (int g = max(0, nk - 2); g < nk; ++g) mbar_wait(&bars.k_full[g & 1], (g >> 1) & 1, err, nullptr);
       for (int g = max(0, nv - 2); g < nv; ++g) mbar_wait(&bars.v_full[g & 1], (g >> 1) & 1, err, nullptr);
-    }
-  } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+      // ------------------------------------------------------- MMA issuers
+      // Issuer w (warp 1: w = 0, warp 3: w = 1) takes the key blocks of
+      // parity w, which use only K/V slot w, S/P buffer w and partial O_w,
+      // and issues S_g then P.V of block g before S of block g+2: in-order
+      // issue from one thread keeps S_{g+2} behind the P.V that reads P_g.
+      // The two issuers' MMAs interleave on the tensor pipe.
+      const int w = warp == 1 ? 0 : 1;
       // Descriptors are built once; a K-step only adds its byte offset >> 4
       // to the start-address field (addresses stay below 256 KB, no carry).
-      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      const uint64_t dq = smem_desc_sw128(q_addr, 0, 1024);
-      const uint64_t dk0 = smem_desc_sw128(k_addr, 0, 1024), dk1 = smem_desc_sw128(k_addr + kKBytes, 0, 1024);
-      const uint64_t dv0 = smem_desc_sw128(v_addr, 16384, 1024), dv1 = smem_desc_sw128(v_addr + kVBytes, 16384, 1024);
-      // the P.V product of block g, its item's parity, first / last block of the item
-      struct PV {
-        int g, it;
-        bool first, last;
-      };
-      auto issue_pv = [&](const PV& b) -> bool {
-        const int s = b.g & 1;
-        const uint32_t ph = (b.g >> 1) & 1;
-        const int o = b.it & 1;
-        // the first P.V of an item overwrites O[o]: the epilogue of the item
-        // two before must have read it
-        if (b.first && !mbar_wait(&bars.o_empty[o], ((b.it >> 1) & 1) ^ 1, err, &abort_s)) return false;
-        if (!mbar_wait(&bars.p_full[s], ph, err, &abort_s)) return false;
-        if (!mbar_wait(&bars.v_full[s], ph, err, &abort_s)) return false;
-        tc_fence_after();
-        const uint64_t vd = s ? dv1 : dv0;
-        const uint32_t tO = o ? tO1 : tO0;
-        const uint32_t tP = s ? tS1 : tS0;
-        if (b.first) {
-          mma_ts(tO, tP, vd, kIdescPV, 0u);
-#pragma unroll
-          for (int kk = 1; kk < kBN / 16; ++kk) mma_ts(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, 1u);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) mma_ts(tO, tP + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, 1u);
-        }
-        mma_commit(&bars.v_empty[s]);
-        mma_commit(&bars.pv_done);
-        if (b.last) mma_commit(&bars.o_full[o]);
-        return true;
-      };
-      int gb = 0, nq = 0;
-      bool ok = true, pending = false;
-      PV pv{0, 0, false, false};
+      const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 0, 1024);
+      const uint64_t dk = smem_desc_sw128(smem_u32(sK) + w * kKBytes, 0, 1024);
+      const uint64_t dv = smem_desc_sw128(smem_u32(sV) + w * kVBytes, 16384, 1024);
+      const uint32_t sd = w ? tS[1] : tS[0];
+      const uint32_t od = w ? tO[1] : tO[0];
+      int gb = 0, cw = 0;  // global block counter; blocks of this issuer
+      bool ok = true;
       for (int it = 0; ok; ++it) {
         if (!mbar_wait(&bars.item_full[it % kRing], (it / kRing) & 1, err, &abort_s)) break;
         const int idx = ring_s[it % kRing];
         mbar_arrive(&bars.item_empty[it % kRing]);
         if (idx < 0) break;
         bool dummy = false;
-        const Item w = item_at(p, static_cast<uint32_t>(idx), dummy);
-        for (int j = 0; j < w.n_kv; ++j, ++gb) {
-          const int s = gb & 1;
-          const uint32_t ph = (gb >> 1) & 1;
-          if (j == 0 && !mbar_wait(&bars.q_full, nq & 1, err, &abort_s)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait(&bars.k_full[s], ph, err, &abort_s)) {
+        const Item wi = item_at(p, static_cast<uint32_t>(idx), dummy);
+        // this issuer's blocks of the item: j = j0, j0 + 2, ...
+        const int j0 = (gb & 1) == w ? 0 : 1;
+        const int j_last = j0 < wi.n_kv ? j0 + ((wi.n_kv - 1 - j0) & ~1) : -1;
+        for (int j = j0; j < wi.n_kv; j += 2, ++cw) {
+          const uint32_t ph = cw & 1;
+          if ((j == j0 && !mbar_wait(&bars.q_full, it & 1, err, &abort_s)) ||
+              !mbar_wait(&bars.k_full[w], ph, err, &abort_s)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t kd = s ? dk1 : dk0;
-          const uint32_t tS = s ? tS1 : tS0;
-          mma_ss(tS, dq, kd, kIdescS, 0u);
+          // 12 K-steps: three 64-feature chunks of 16 KB, 32 bytes per step
+#pragma unroll 1
+          for (int c = 0; c < kDqk / 64; ++c) {
+            const uint64_t a = dq + c * (16384 >> 4), bdesc = dk + c * (16384 >> 4);
 #pragma unroll
-          for (int kk = 1; kk < kDqk / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(tS, dq + off, kd + off, kIdescS, 1u);
+            for (int k4 = 0; k4 < 4; ++k4) mma_ss(sd, a + k4 * 2, bdesc + k4 * 2, kIdescS, (c | k4) != 0 ? 1u : 0u);
           }
-          mma_commit(&bars.s_full[s]);
-          mma_commit(&bars.k_empty[s]);
-          if (j == w.n_kv - 1) {
-            mma_commit(&bars.q_empty);
-            ++nq;
-          }
-          if (pending && !issue_pv(pv)) {
+          mma_commit(&bars.s_full[w]);
+          if (j == j_last) mma_commit(&bars.q_empty);
+          // P.V: the item's first one for this issuer overwrites O_w, which
+          // the previous item's epilogue must have read; P_g implies V_g landed
+          if ((j == j0 && it > 0 && !mbar_wait(&bars.o_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, err, &abort_s)) ||
+              !mbar_wait(&bars.p_full[w], ph, err, &abort_s)) {
             ok = false;
             break;
           }
-          pv = PV{gb, it, j == 0, j == w.n_kv - 1};
-          pending = true;
+          tc_fence_after();
+          // 8 K-steps of 16 keys: P columns +8, V rows +2048 bytes
+          const uint32_t first = j == j0 ? 1u : 0u;  // the item's first P.V overwrites O_w
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t bdesc = dv + h * ((4 * 2048) >> 4);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              mma_ts(od, sd + (4 * h + k4) * 8, bdesc + k4 * (2048 >> 4), kIdescPV, (first & (h == 0) & (k4 == 0)) ? 0u : 1u);
+          }
+          mma_commit(&bars.v_empty[w]);
+          if (j == j_last) mma_commit(&bars.o_full);
         }
+        if (!ok) break;
+        if (j_last < 0) {
+          // No block of this parity: nothing of this issuer reads Q or writes
+          // O_w.  Its arrivals wait until the previous item's phases of
+          // q_empty (implied by this item's Q having landed) and o_full
+          // (implied by that item's epilogue being done) are complete, so
+          // they cannot complete a phase that the other issuer still owes.
+          if (!mbar_wait(&bars.q_full, it & 1, err, &abort_s)) break;
+          mbar_arrive(&bars.q_empty);
+          if (it > 0 && !mbar_wait(&bars.o_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, err, &abort_s)) break;
+          mbar_arrive(&bars.o_full);
+        }
+        gb += wi.n_kv;
       }
-      if (ok && pending) issue_pv(pv);
-      if (gb > 0) {
-        mma_commit(&bars.mma_done);
-        mbar_wait(&bars.mma_done, 0, err, nullptr);  // every MMA retired
+      if (cw > 0) {
+        mma_commit(&bars.mma_done[w]);
+        mbar_wait(&bars.mma_done[w], 0, err, nullptr);  // every MMA of this issuer retired
       }
     }
-  } else if (warp < 10) {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ softmax
-    // Two warpgroups share each row: group g handles score columns
-    // [64g, 64g+64).  Row maxima are combined through shared memory.
-    const int g = (warp - 2) >> 2;
+    // Warpgroup wg takes the key blocks of global parity wg, one thread per
+    // query row over all 128 keys of the block, with its own running max,
+    // row sum and partial O; the epilogue merges the two partial results.
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int c0 = 64 * g;           // first score column of this group
-    int gb = 0;
+    const uint32_t my_s = wg ? tS[1] : tS[0];
+    const uint32_t my_o = wg ? tO[1] : tO[0];
+    int gb = 0, cw = 0;  // global block counter; blocks of this warpgroup
     bool ok = true;
     for (int it = 0; ok; ++it) {
       if (!warp_wait(&bars.item_full[it % kRing], (it / kRing) & 1, err, &abort_s)) break;
@@ -389,76 +397,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool dummy = false;
       const Item w = item_at(p, static_cast<uint32_t>(idx), dummy);
       const int qi = w.row0 + r;  // query index within the sequence
-      const uint32_t tO = (it & 1) ? tO1 : tO0;
       float m_run = -INFINITY, l_run = 0.f;
+      bool any = false;  // this warpgroup had a block of this item
       for (int j = 0; j < w.n_kv; ++j, ++gb) {
-        const int b = gb & 1;
-        const uint32_t ph = (gb >> 1) & 1;
-        if (!warp_wait(&bars.s_full[b], ph, err, &abort_s)) {
+        if ((gb & 1) != wg) continue;
+        if (!warp_wait(&bars.s_full[wg], cw & 1, err, &abort_s)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float x[64];
+        float x[128];
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < 128; c += 16) {
           uint32_t v[16];
-          tmem_ld16((b ? tS1 : tS0) + lane_off + c0 + c, v);
+          tmem_ld16(my_s + lane_off + c, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
         }
         tmem_ld_wait();
         // max of the raw scores (scale_log2 > 0); the scale is applied
         // inside the exponent below
-        const int key0 = j * kBN + c0;
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (key0 + 63 > qi) {  // diagonal block: mask keys after the query
+        const int key0 = j * kBN;
+        float mq[8];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+        for (int i = 0; i < 8; ++i) mq[i] = -INFINITY;
+        if (key0 + kBN - 1 > qi) {  // diagonal block: mask keys after the query
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
             x[c] = (key0 + c <= qi) ? x[c] : -INFINITY;
-            mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+            mq[c & 7] = fmaxf(mq[c & 7], x[c]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+          for (int c = 0; c < 128; ++c) mq[c & 7] = fmaxf(mq[c & 7], x[c]);
         }
-        // row max over both halves (also orders every S read before any P write)
-        red_s[b][g][r] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
-        mbar_arrive(&bars.red[b]);
-        if (!warp_wait(&bars.red[b], ph, err, &abort_s)) {
-          ok = false;
-          break;
-        }
-        const float mx = fmaxf(red_s[b][0][r], red_s[b][1][r]);
-        // lazy reference update (identical in both groups)
+        const float mx =
+            fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7]))) *
+            p.scale_log2;
+        // lazy reference update
         float m_use = m_run, alpha = 1.f;
         const bool raise = mx > m_run + kRescaleThreshold;
         if (raise) {
           m_use = mx;
-          alpha = ex2_approx(m_run - mx);  // 0 on the first block
+          alpha = ex2_approx(m_run - mx);  // 0 on this warpgroup's first block
         }
-        if (__any_sync(0xffffffffu, raise && j > 0)) {
-          // O must not be in flight: the previous P.V (block gb-1, this item)
-          if (!warp_wait(&bars.pv_done, (gb - 1) & 1, err, &abort_s)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        // The partial O holds only this warpgroup's earlier blocks, whose
+        // P.V retired before S of this block was committed.
+        if (__any_sync(0xffffffffu, raise && any)) {
 #pragma unroll
-          for (int c = 0; c < 64; c += 16) {
+          for (int c = 0; c < 128; c += 16) {
             uint32_t v[16];
-            tmem_ld16(tO + lane_off + c0 + c, v);
+            tmem_ld16(my_o + lane_off + c, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st16(tO + lane_off + c0 + c, v);
+            tmem_st16(my_o + lane_off + c, v);
           }
           tmem_st_wait();
         }
         m_run = m_use;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {  // P as bf16 pairs: columns [32g, 32g+32) of the S buffer
+        for (int c = 0; c < 128; c += 32) {  // P as bf16 pairs: columns [0, 64) of the S buffer
           uint32_t v[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -468,23 +468,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             v[i] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          tmem_st16((b ? tS1 : tS0) + lane_off + 32 * g + c / 2, v);
+          tmem_st16(my_s + lane_off + c / 2, v);
         }
         l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars.p_full[b]);
+        if (!warp_wait(&bars.v_full[wg], cw & 1, err, &abort_s)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive(&bars.p_full[wg]);
+        ++cw;
+        any = true;
       }
       if (!ok) break;
-      // row statistics for the epilogue; the slot of this item parity is
-      // free once the epilogue of the item two before has read it
+      // partial row statistics for the epilogue; the slot of this item
+      // parity is free once the epilogue of the item two before has read it
       if (!warp_wait(&bars.o_empty[it & 1], ((it >> 1) & 1) ^ 1, err, &abort_s)) break;
-      l_s[it & 1][g][r] = l_run;
-      if (g == 0) m_s[it & 1][r] = m_run;
+      l_s[it & 1][wg][r] = l_run;
+      m_s[it & 1][wg][r] = m_run;
       mbar_arrive(&bars.l_full[it & 1]);
     }
   } else {
     // ----------------------------------------------------------- epilogue
+    // thread = query row: merge the two partial results, normalise,
+    // quantise to NVFP4 and store codes, scales and the LSE
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -498,45 +507,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool dummy = false;
       const Item w = item_at(p, static_cast<uint32_t>(idx), dummy);
       const int o = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!warp_wait(&bars.o_full[o], ph, err, &abort_s) || !warp_wait(&bars.l_full[o], ph, err, &abort_s)) break;
+      if (!warp_wait(&bars.o_full, it & 1, err, &abort_s) || !warp_wait(&bars.l_full[o], (it >> 1) & 1, err, &abort_s))
+        break;
       tc_fence_after();
-      const float l_tot = l_s[o][0][r] + l_s[o][1][r];
-      const float m_row = m_s[o][r];
-      const int qi = w.row0 + r;
-      const uint32_t tO = o ? tO1 : tO0;
-      const int64_t m = w.seq_begin + qi;
+      const float l0 = l_s[o][0][r], l1 = l_s[o][1][r];
+      const float m0 = m_s[o][0][r], m1 = m_s[o][1][r];
+      const float m_row = fmaxf(m0, m1);
+      // a partial with no block (l = 0) carries no weight, and its O is not read
+      const float a0 = l0 > 0.f ? ex2_approx(m0 - m_row) : 0.f;
+      const float a1 = l1 > 0.f ? ex2_approx(m1 - m_row) : 0.f;
+      const float l_tot = a0 * l0 + a1 * l1;
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const float c0 = a0 * inv_l, c1 = a1 * inv_l;
+      const int qi = w.row0 + r;
+      const int64_t m = w.seq_begin + qi;
+      uint8_t* code_row = p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + w.h * 64;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        float ov[64];
+        uint32_t sbits = 0;
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(tO + lane_off + 64 * half + c, v);
+        for (int qq = 0; qq < 2; ++qq) {
+          const int col = 64 * half + 32 * qq;
+          float ov[32];
+          uint32_t v0[16], v1[16], u0[16], u1[16];
+          tmem_ld16(tO[0] + lane_off + col, v0);
+          tmem_ld16(tO[0] + lane_off + col + 16, v1);
+          tmem_ld16(tO[1] + lane_off + col, u0);
+          tmem_ld16(tO[1] + lane_off + col + 16, u1);
+          tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ov[c + i] = __uint_as_float(v[i]);
-        }
-        tmem_ld_wait();
-        if (qi < w.n) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) ov[c] *= inv_l;
-          uint32_t wd[8];
-          uint32_t sb[4];
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            float R = 0.f;
-            sb[blk] = gs_ok ? block_scale(fmaxf(amax8(ov + 16 * blk), amax8(ov + 16 * blk + 8)), kf, gs, R) : 0u;
-            wd[2 * blk] = gs_ok ? encode8(ov + 16 * blk, R) : 0u;
-            wd[2 * blk + 1] = gs_ok ? encode8(ov + 16 * blk + 8, R) : 0u;
+          for (int i = 0; i < 16; ++i) {
+            float y0 = c0 > 0.f ? c0 * __uint_as_float(v0[i]) : 0.f;
+            float y1 = c0 > 0.f ? c0 * __uint_as_float(v1[i]) : 0.f;
+            ov[i] = c1 > 0.f ? fmaf(c1, __uint_as_float(u0[i]), y0) : y0;
+            ov[16 + i] = c1 > 0.f ? fmaf(c1, __uint_as_float(u1[i]), y1) : y1;
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + w.h * 64 +
-                                                32 * half);
-          dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+          if (qi < w.n) {
+            uint32_t wd[4];
+            uint32_t sb[2];
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+              float R = 0.f;
+              sb[blk] = gs_ok ? block_scale(fmaxf(amax8(ov + 16 * blk), amax8(ov + 16 * blk + 8)), kf, gs, R) : 0u;
+              wd[2 * blk] = gs_ok ? encode8(ov + 16 * blk, R) : 0u;
+              wd[2 * blk + 1] = gs_ok ? encode8(ov + 16 * blk + 8, R) : 0u;
+            }
+            *reinterpret_cast<uint4*>(code_row + col / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            sbits |= (sb[0] | (sb[1] << 8)) << (16 * qq);
+          }
+        }
+        if (qi < w.n) {
           const int64_t kc = static_cast<int64_t>(w.h) * 8 + 4 * half;
-          *reinterpret_cast<uint32_t*>(p.scales + sf_offset(m, kc, k_tiles_sf)) =
-              sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+          *reinterpret_cast<uint32_t*>(p.scales + sf_offset(m, kc, k_tiles_sf)) = sbits;
         }
       }
       if (qi < w.n) {
