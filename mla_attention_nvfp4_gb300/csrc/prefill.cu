@@ -163,11 +163,45 @@ __device__ int grab_item(const Params& p, bool& bad) {
   }
 }
 
-// L2 prefetch of one box of a tensor map (no shared memory written).
-__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0), "r"(c1),
-               "r"(c2)
-               : "memory");
+// One copy per tile: the 4-D map (64 features, head, token, 64-feature chunk)
+// lands as smem [chunk][token][64 features], the three (or two) 16 KB
+// K-major 128-byte-swizzled chunks the MMAs read.
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+// L2 prefetch of one box of the same map (no shared memory written).
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(c0), "r"(c1),
+               "r"(c2), "r"(c3) : "memory");
+}
+
+// Packed fp32 pair arithmetic (one instruction for two lanes of work) and a
+// three-input max, to thin the softmax's instruction stream.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpk2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // A wait whose outcome is the same in every lane, so that the warp-wide
@@ -261,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nxt >= 0) {
           bool dummy = false;
           const Item w2 = item_at(p, static_cast<uint32_t>(nxt), dummy);
-          for (int cb = 0; cb < 3; ++cb) tma_prefetch_3d(&tm_q, cb * 64, w2.h, w2.seq_begin + w2.row0);
+          tma_prefetch_4d(&tm_q, 0, w2.h, w2.seq_begin + w2.row0, 0);
         }
         bool ok = true;
         for (int j = 0; j < w.n_kv; ++j) {
@@ -269,20 +303,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ph = (nk >> 1) & 1;
           if (!(ok = mbar_wait(&bars.s_full[s], ph ^ 1, err, &abort_s))) break;
           mbar_expect_tx(&bars.k_full[s], kKBytes);
-          for (int cb = 0; cb < 3; ++cb)
-            tma_load_3d(sK + s * kKBytes + cb * 16384, &tm_k, cb * 64, w.h, w.seq_begin + j * kBN, &bars.k_full[s]);
+          tma_load_4d(sK + s * kKBytes, &tm_k, 0, w.h, w.seq_begin + j * kBN, 0, &bars.k_full[s]);
           ++nk;
           if (j == 0) {  // Q of this item, once the previous item's last score product has read it
             if (!(ok = mbar_wait(&bars.q_empty, (nq & 1) ^ 1, err, &abort_s))) break;
             mbar_expect_tx(&bars.q_full, kQBytes);
-            for (int cb = 0; cb < 3; ++cb)
-              tma_load_3d(sQ + cb * 16384, &tm_q, cb * 64, w.h, w.seq_begin + w.row0, &bars.q_full);
+            tma_load_4d(sQ, &tm_q, 0, w.h, w.seq_begin + w.row0, 0, &bars.q_full);
             ++nq;
           }
           if (!(ok = mbar_wait(&bars.v_empty[s], ph ^ 1, err, &abort_s))) break;
           mbar_expect_tx(&bars.v_full[s], kVBytes);
-          for (int cb = 0; cb < 2; ++cb)
-            tma_load_3d(sV + s * kVBytes + cb * 16384, &tm_v, cb * 64, w.h, w.seq_begin + j * kBN, &bars.v_full[s]);
+          tma_load_4d(sV + s * kVBytes, &tm_v, 0, w.h, w.seq_begin + j * kBN, 0, &bars.v_full[s]);
           ++nv;
         }
         if (!ok) break;
@@ -423,14 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 8; ++i) mq[i] = -INFINITY;
         if (key0 + kBN - 1 > qi) {  // diagonal block: mask keys after the query
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            x[c] = (key0 + c <= qi) ? x[c] : -INFINITY;
-            mq[c & 7] = fmaxf(mq[c & 7], x[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) mq[c & 7] = fmaxf(mq[c & 7], x[c]);
+          for (int c = 0; c < 128; ++c) x[c] = (key0 + c <= qi) ? x[c] : -INFINITY;
         }
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) mq[(c >> 1) & 7] = max3(mq[(c >> 1) & 7], x[c], x[c + 1]);
         const float mx =
             fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7]))) *
             p.scale_log2;
@@ -456,21 +483,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
         }
         m_run = m_use;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // exponent arguments two at a time: x * scale_log2 - m_use
+        const uint64_t sc2 = pk2(p.scale_log2, p.scale_log2), nm2 = pk2(-m_use, -m_use);
+        uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial row sums
 #pragma unroll
         for (int c = 0; c < 128; c += 32) {  // P as bf16 pairs: columns [0, 64) of the S buffer
           uint32_t v[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(x[c + 2 * i], p.scale_log2, -m_use));
-            const float p1 = ex2_approx(fmaf(x[c + 2 * i + 1], p.scale_log2, -m_use));
-            ls[i & 3] += p0 + p1;
+            float a0, a1;
+            unpk2(fma2(pk2(x[c + 2 * i], x[c + 2 * i + 1]), sc2, nm2), a0, a1);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
             __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             v[i] = *reinterpret_cast<uint32_t*>(&h2);
           }
           tmem_st16(my_s + lane_off + c / 2, v);
         }
-        l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        float ls[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) unpk2(ls2[i], ls[2 * i], ls[2 * i + 1]);
+        l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
         tmem_st_wait();
         tc_fence_before();
         if (!warp_wait(&bars.v_full[wg], cw & 1, err, &abort_s)) {
@@ -606,16 +639,17 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [T, H, D] bf16 with element strides (st, sh, 1) as a 3-D map (D, H, T);
-// box = 64 elements x 1 head x 128 tokens, 128-byte swizzle.
+// [T, H, D] bf16 with element strides (st, sh, 1) as a 4-D map
+// (64 features, H, T, D/64 chunks of 128 bytes); box = 64 features x 1 head x
+// 128 tokens x all chunks, 128-byte swizzle: one copy per Q, K or V tile.
 bool make_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t T, int64_t st, int64_t sh) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(sh * 2), static_cast<cuuint64_t>(st * 2)};
-  cuuint32_t box[3] = {64, 1, 128};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(D / 64)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh * 2), static_cast<cuuint64_t>(st * 2), 128};
+  cuuint32_t box[4] = {64, 1, 128, static_cast<cuuint32_t>(D / 64)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
