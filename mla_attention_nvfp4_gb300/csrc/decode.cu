@@ -166,6 +166,32 @@ __device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t,
 // 16-byte read-only load issued where it is written (volatile): the raw
 // record bytes of the next tile must be in flight while this tile converts,
 // and an ordinary load may be scheduled next to its first use.
+// Packed fp32 pair arithmetic (one instruction for two lanes of work) and a
+// three-input max, to thin the softmax's instruction stream.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpk2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -646,17 +672,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         // max of the raw scores (score_scale > 0), padding keys at -inf; the
         // scale is applied inside the exponent below
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if ((va & vb) == 0xffffffffu) {
-#pragma unroll
-          for (int c = 0; c < kTok; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
-        } else {
+        if ((va & vb) != 0xffffffffu) {
 #pragma unroll
           for (int c = 0; c < kTok; ++c) {
             const unsigned m = c < 32 ? va : vb;
             x[c] = ((m >> (c & 31)) & 1u) ? x[c] : -INFINITY;
-            mq[c & 3] = fmaxf(mq[c & 3], x[c]);
           }
         }
+#pragma unroll
+        for (int c = 0; c < kTok; c += 2) mq[(c >> 1) & 3] = max3(mq[(c >> 1) & 3], x[c], x[c + 1]);
         const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * score_scale;  // log2 units
         float m_use = m_run, alpha = 1.f;
         const bool raise = mx > m_run + kRescaleThreshold;
@@ -687,16 +711,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         }
         m_run = m_use;
         const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;  // no valid key so far
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // exponent arguments and row sums two at a time
+        const uint64_t sc2 = pk2(score_scale, score_scale), nm2 = pk2(-m_ref, -m_ref);
+        uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial sums
         uint32_t pv[kTok / 2];
 #pragma unroll
         for (int i = 0; i < kTok / 2; ++i) {
-          const float p0 = ex2_approx(fmaf(x[2 * i], score_scale, -m_ref));
-          const float p1 = ex2_approx(fmaf(x[2 * i + 1], score_scale, -m_ref));
-          ls[i & 3] += p0 + p1;
+          float a0, a1;
+          unpk2(fma2(pk2(x[2 * i], x[2 * i + 1]), sc2, nm2), a0, a1);
+          const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+          ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
           pv[i] = pack_f16(p0, p1);  // P <= 2^14 (lazy reference), f16 operand
         }
-        l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+        float ls[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) unpk2(ls2[i], ls[2 * i], ls[2 * i + 1]);
+        l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
         // P(j) over S(j): the buffer's previous P was read by PV(j-2), which
         // ran before QK(j) wrote S(j)
         uint32_t v0[16], v1[16];
