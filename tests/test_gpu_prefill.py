@@ -104,3 +104,34 @@ def test_prefill_full_size_sampled():
         sf_rows = sf_np[swizzle.sf_offset(m, kk, H * 8)]
         check_fused_blocks(c_rows, sf_rows, o_ref, o_abs, gs)
         assert_lse_close(f32(lse[h, rows]), l_ref, f"prefill lse head {h}")
+
+
+@pytest.mark.parametrize("case", ["max_seqlen_short", "cu_past_total"])
+def test_prefill_bad_lengths_flagged(case):
+    # Device-side checks: a sequence longer than max_seqlen, or cu_seqlens
+    # reaching past the tokens given, is skipped and flagged BOUNDS (the
+    # kernel reads nothing outside q/k/v); the valid sequences still match.
+    w = workloads.prefill("small", seq_lens=(100, 300), heads=2, seed=5)
+    gs = oracle_gs(w.v)
+    gst = torch.tensor([gs], device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cu = w.cu_seqlens.clone()
+    max_seqlen = w.max_seqlen
+    if case == "max_seqlen_short":
+        max_seqlen = 128  # the 300-token sequence does not fit
+    else:
+        cu[2] = w.total_tokens + 64  # the second sequence ends past the last token
+    codes, sf, lse = mla.mla_nvfp4_prefill_fused_out(
+        w.q.to(DEV), w.k.to(DEV), w.v.to(DEV), cu.to(DEV), max_seqlen, w.softmax_scale, gst,
+        return_lse=True, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & mla.DEVERR_BOUNDS
+    # the first sequence (100 tokens, within both limits) is still correct
+    o_ref, l_ref, o_abs = attention.prefill(f32(w.q[:100]), f32(w.k[:100]), f32(w.v[:100]),
+                                             np.array([0, 100]), w.softmax_scale, with_abs=True)
+    H = w.heads
+    c = codes.cpu().numpy()[:100]
+    m, kk = np.meshgrid(np.arange(100), np.arange(H * 8), indexing="ij")
+    s = sf.cpu().numpy()[swizzle.sf_offset(m, kk, H * 8)]
+    check_fused_blocks(c, s, o_ref.reshape(100, H * 128), o_abs.reshape(100, H * 128), gs)
+    assert_lse_close(f32(lse[:, :100]), l_ref, "prefill lse, valid sequence")
