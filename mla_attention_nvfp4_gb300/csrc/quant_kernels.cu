@@ -49,19 +49,13 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
   const float k = scale_factor(gs);
   if (!gs_valid && warp == 0 && lane == 0) flag_error(error_word, MLA_DEVERR_SCALE);
 
-  for (int64_t t = warp; t < num_tokens; t += n_warps) {
-    const int64_t slot = slot_mapping[t];
-    if (slot < 0) continue;
+  // Quantise one token's record from its loaded row, latent and rope parts.
+  auto emit = [&](int64_t t, int64_t slot, const uint4& va, const uint4& vb, const uint4& vr) {
+    if (slot < 0) return;
     if (slot >= num_slots) {
       if (lane == 0) flag_error(error_word, MLA_DEVERR_BOUNDS);
-      continue;
+      return;
     }
-    const __nv_bfloat16* row = kv_c + t * kv_stride;
-    const uint4 va = ldg_stream(row + 8 * lane);
-    const uint4 vb = ldg_stream(row + 256 + 8 * lane);
-    uint4 vr = make_uint4(0, 0, 0, 0);
-    if (lane < 8) vr = ldg_stream(k_pe + t * pe_stride + 8 * lane);
-
     float xa[8], xb[8];
     unpack8_bf16(va, xa);
     unpack8_bf16(vb, xb);
@@ -96,6 +90,27 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     } else if (lane == 8) {
       *reinterpret_cast<uint4*>(rec + kRecord - 16) = make_uint4(0, 0, 0, 0);
     }
+  };
+  // Two tokens per iteration, both tokens' loads issued before either is
+  // quantised: twice the bytes in flight per warp.
+  for (int64_t t0 = warp; t0 < num_tokens; t0 += 2 * n_warps) {
+    const int64_t t1 = t0 + n_warps;
+    const bool has1 = t1 < num_tokens;
+    const int64_t slot0 = slot_mapping[t0];
+    const int64_t slot1 = has1 ? slot_mapping[t1] : -1;
+    const __nv_bfloat16* row0 = kv_c + t0 * kv_stride;
+    const uint4 va0 = ldg_stream(row0 + 8 * lane);
+    const uint4 vb0 = ldg_stream(row0 + 256 + 8 * lane);
+    uint4 vr0 = make_uint4(0, 0, 0, 0), va1 = vr0, vb1 = vr0, vr1 = vr0;
+    if (lane < 8) vr0 = ldg_stream(k_pe + t0 * pe_stride + 8 * lane);
+    if (has1) {
+      const __nv_bfloat16* row1 = kv_c + t1 * kv_stride;
+      va1 = ldg_stream(row1 + 8 * lane);
+      vb1 = ldg_stream(row1 + 256 + 8 * lane);
+      if (lane < 8) vr1 = ldg_stream(k_pe + t1 * pe_stride + 8 * lane);
+    }
+    emit(t0, slot0, va0, vb0, vr0);
+    if (has1) emit(t1, slot1, va1, vb1, vr1);
   }
 }
 
