@@ -214,7 +214,7 @@ def run_ours(args, rank, world):
                                         out_codes=codes, out_scales=scales, error_word=err)
 
     legs = [("cache_write", leg_cache_write), ("decode", leg_decode), ("prefill", leg_prefill)]
-    launches_per_step = mla.LAUNCHES_PER_CALL["cache_write"] + mla.LAUNCHES_PER_CALL["decode"] + \
+    launches_per_step = mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(w.batch, w.heads, decode_splits) + \
         mla.LAUNCHES_PER_CALL["prefill"]
 
     def step(record=None):

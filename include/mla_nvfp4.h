@@ -113,6 +113,15 @@ int mla_nvfp4_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_p
 size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits);
 
 /*
+ * The number of key splits mla_nvfp4_decode uses for (batch, num_heads)
+ * when given num_splits <= 0, on the current device (a value > 0 is
+ * returned as given).  With one split the decode writes out and lse from
+ * its own kernel (one launch); with more, a merge kernel follows (two
+ * launches).  Returns 0 for invalid sizes.
+ */
+int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits);
+
+/*
  * Absorbed MLA decode over the NVFP4 latent cache, split along the keys and
  * merged by natural-log LSE.
  * Source: "#2244", first commit message (split-K absorbed decode over the

@@ -19,7 +19,8 @@ from . import build as _build
 
 __all__ = [
     "load_library", "MLAError", "mla_nvfp4_global_scale", "mla_nvfp4_cache_write",
-    "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode", "mla_nvfp4_prefill_fused_out",
+    "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode_default_splits", "decode_launches",
+    "mla_nvfp4_decode", "mla_nvfp4_prefill_fused_out",
     "mla_nvfp4_quantize_rows", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
     "LAUNCHES_PER_CALL",
 ]
@@ -28,7 +29,9 @@ RECORD_BF16_ROPE = 432
 RECORD_FP8_ROPE = 368
 DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE = 0x1, 0x2, 0x4
 
-# Kernels each entry point launches (for launch accounting in the benchmark).
+# Kernels each entry point launches (for launch accounting in the benchmark);
+# decode launches one kernel with one key split and two (plus the merge)
+# with more, see decode_launches().
 LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 2, "prefill": 1, "global_scale": 2}
 # What bounds each hot kernel as built: "hbm", "tensor" (tcgen05 MMA) or
 # "alu" (CUDA-core arithmetic).
@@ -55,6 +58,7 @@ _SIGS = {
     "mla_nvfp4_cache_write": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64,
                                        _c_int, _c_vp, _c_vp, _c_vp]),
     "mla_nvfp4_decode_workspace_size": (ctypes.c_size_t, [_c_int, _c_int, _c_int]),
+    "mla_nvfp4_decode_default_splits": (_c_int, [_c_int, _c_int, _c_int]),
     "mla_nvfp4_decode": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64, _c_int,
                                   _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp, _c_vp,
                                   ctypes.c_size_t, _c_int, _c_vp, _c_vp]),
@@ -172,6 +176,18 @@ def mla_nvfp4_cache_write(kv_c, k_pe, slot_mapping, cache, global_scale, error_w
 
 def mla_nvfp4_decode_workspace_size(batch: int, num_heads: int, num_splits: int = 0) -> int:
     return int(load_library().mla_nvfp4_decode_workspace_size(batch, num_heads, num_splits))
+
+
+def mla_nvfp4_decode_default_splits(batch: int, num_heads: int, num_splits: int = 0) -> int:
+    """Key splits a decode of (batch, num_heads) uses (num_splits <= 0: the
+    library default on the current device)."""
+    return int(load_library().mla_nvfp4_decode_default_splits(batch, num_heads, num_splits))
+
+
+def decode_launches(batch: int, num_heads: int, num_splits: int = 0) -> int:
+    """Kernels one mla_nvfp4_decode call launches: the decode, plus the merge
+    when there is more than one key split."""
+    return 1 if mla_nvfp4_decode_default_splits(batch, num_heads, num_splits) == 1 else 2
 
 
 def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, seq_lens=None,

@@ -105,6 +105,13 @@ size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits)
   return mla::decode_workspace_bytes(batch, num_heads, num_splits);
 }
 
+int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits) {
+  if (batch < 1 || num_heads < 1) return 0;
+  if (num_splits > 0) return num_splits;
+  const int sms = device_sms();
+  return mla::decode_default_splits(batch, num_heads, sms > 0 ? sms : 152);
+}
+
 int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cache,
                      int64_t num_slots, int record_bytes, const int32_t* page_table,
                      int64_t page_table_stride, int page_size, const int32_t* seq_lens,

@@ -112,6 +112,8 @@ struct Params {
   float* part_o;    // [batch, splits, heads, 512]
   float* part_lse;  // [batch, splits, heads]
   int splits;
+  __nv_bfloat16* out;  // [batch, heads, 512]: written here directly when splits == 1
+  float* lse;          // [batch, heads] or null (same)
   uint32_t* error_word;
 };
 
@@ -750,7 +752,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
     const bool have = live && l_run > 0.f;
     const float f = have ? gs / l_run : 0.f;
     const int64_t row = (static_cast<int64_t>(b) * p.splits + split) * p.num_heads + head;
+    // With one split the merge is the identity (weight exp(0) = 1, sum 1):
+    // the final bf16 output and the LSE are written here and no merge runs.
+    const bool direct = p.splits == 1;
     float4* dst = reinterpret_cast<float4*>(p.part_o + row * 512 + 256 * rank);
+    uint4* dst_bf = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + head) * 512 + 256 * rank);
     if (live) tc_fence_after();
 #pragma unroll 2
     for (int c = 0; c < 256; c += 16) {
@@ -763,13 +769,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         for (int i = 0; i < 16; ++i) v[i] = 0u;
       }
       if (head_ok) {
+        if (direct) {
+          uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[c / 4 + i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
-                                       __uint_as_float(v[4 * i + 2]) * f, __uint_as_float(v[4 * i + 3]) * f);
+          for (int i = 0; i < 8; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
+            w[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          dst_bf[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst_bf[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[c / 4 + i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
+                                         __uint_as_float(v[4 * i + 2]) * f, __uint_as_float(v[4 * i + 3]) * f);
+        }
       }
     }
-    if (head_ok && rank == 0) p.part_lse[row] = have ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    if (head_ok && rank == 0) {
+      const float l = have ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      if (!direct)
+        p.part_lse[row] = l;
+      else if (p.lse != nullptr)
+        p.lse[static_cast<int64_t>(b) * p.num_heads + head] = l;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -847,6 +870,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int /*num_sms*/) {
   p.softmax_scale = a.softmax_scale;
   p.gs = a.gs;
   p.splits = a.num_splits;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
   p.error_word = a.error_word;
   const size_t rows = static_cast<size_t>(a.batch) * a.num_splits * a.num_heads;
   p.part_o = static_cast<float*>(a.workspace);
@@ -864,6 +889,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int /*num_sms*/) {
     decode_tc_kernel<368><<<grid, kThreads, kSmAlloc, stream>>>(p);
   }
   if (const int st = launch_status()) return st;
+  if (a.num_splits == 1) return MLA_OK;  // the decode kernel wrote out and lse
   decode_merge_kernel<<<a.batch * a.num_heads, 128, 0, stream>>>(
       p.part_o, p.part_lse, a.num_splits, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);
   return launch_status();
