@@ -135,3 +135,23 @@ def test_prefill_bad_lengths_flagged(case):
     s = sf.cpu().numpy()[swizzle.sf_offset(m, kk, H * 8)]
     check_fused_blocks(c, s, o_ref.reshape(100, H * 128), o_abs.reshape(100, H * 128), gs)
     assert_lse_close(f32(lse[:, :100]), l_ref, "prefill lse, valid sequence")
+
+
+@pytest.mark.parametrize("seed", [21, 22, 23, 24])
+def test_prefill_random_mixes(seed):
+    # seeded random length mixes (empty, single-token, ragged, several tiles)
+    # and head counts: the work-item order and the block parities differ per case
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 7))
+    lens = tuple(int(x) for x in rng.choice([0, 1, 2, 127, 128, 129, 255, 300, 511, 700, 900], size=n))
+    if sum(lens) == 0:
+        lens = lens + (65,)
+    heads = int(rng.integers(1, 9))
+    w = workloads.prefill("mix", seq_lens=lens, heads=heads, seed=seed)
+    gs = oracle_gs(w.v)
+    codes, sf, lse = _run(w, gs)
+    o_ref, l_ref, o_abs = attention.prefill(f32(w.q), f32(w.k), f32(w.v), w.cu_seqlens.numpy(),
+                                             w.softmax_scale, with_abs=True)
+    T = w.total_tokens
+    check_fused_output(codes, sf, o_ref.reshape(T, heads * 128), o_abs.reshape(T, heads * 128), gs)
+    assert_lse_close(lse, l_ref, f"prefill lse mix {lens} H{heads}")
