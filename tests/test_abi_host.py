@@ -71,3 +71,17 @@ def test_bad_sizes_rejected():
     # non-positive softmax scale
     assert lib.mla_nvfp4_prefill_fused_out(p, p, p, 192, 192, 192, 192, 128, 128, p, 1, 4, 4, 1, 0.0, p,
                                            p, p, None, None, None) == 1
+
+
+def test_decode_default_splits_and_launch_count():
+    # an explicit split count is returned as given; invalid sizes give 0; the
+    # default is at least 1; one split means one launch (no merge kernel)
+    assert mla.mla_nvfp4_decode_default_splits(4, 128, 5) == 5
+    assert mla.mla_nvfp4_decode_default_splits(0, 128, 0) == 0
+    assert mla.mla_nvfp4_decode_default_splits(4, 0, 0) == 0
+    d = mla.mla_nvfp4_decode_default_splits(64, 128, 0)
+    assert d >= 1
+    assert mla.decode_launches(64, 128, 1) == 1
+    assert mla.decode_launches(64, 128, 3) == 2
+    # the workspace the default needs is the one its split count needs
+    assert mla.mla_nvfp4_decode_workspace_size(64, 128, 0) == mla.mla_nvfp4_decode_workspace_size(64, 128, d)
