@@ -46,6 +46,18 @@ int cuda_status(cudaError_t e) {
 int launch_status() { return cuda_status(cudaGetLastError()); }
 void set_last_error(const char* message) { t_last_error = message; }
 int current_device_sms() { return device_sms(); }
+int smem_limit_once(const void* kernel, int bytes, int slot) {
+  static std::atomic<uint64_t> done[16];  // bit d: set on device d
+  int dev = 0;
+  if (const int st = cuda_status(cudaGetDevice(&dev))) return st;
+  if (slot < 0 || slot >= 16 || dev < 0 || dev >= 64) return MLA_ERR_LAUNCH;
+  const uint64_t bit = uint64_t(1) << dev;
+  if (done[slot].load(std::memory_order_acquire) & bit) return MLA_OK;
+  if (const int st = cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return st;
+  done[slot].fetch_or(bit, std::memory_order_acq_rel);
+  return MLA_OK;
+}
 }  // namespace mla
 
 extern "C" {

@@ -880,12 +880,12 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int /*num_sms*/) {
   dim3 grid(2 * a.num_splits, a.batch, (a.num_heads + kHeads - 1) / kHeads);
   if (grid.y > 65535u || grid.z > 65535u) return MLA_ERR_INVALID_ARG;
   if (a.record_bytes == 432) {
-    if (const int st = cuda_status(cudaFuncSetAttribute(decode_tc_kernel<432>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmAlloc)))) return st;
+    if (const int st = smem_limit_once(reinterpret_cast<const void*>(decode_tc_kernel<432>), static_cast<int>(kSmAlloc), 1))
+      return st;
     decode_tc_kernel<432><<<grid, kThreads, kSmAlloc, stream>>>(p);
   } else {
-    if (const int st = cuda_status(cudaFuncSetAttribute(decode_tc_kernel<368>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmAlloc)))) return st;
+    if (const int st = smem_limit_once(reinterpret_cast<const void*>(decode_tc_kernel<368>), static_cast<int>(kSmAlloc), 2))
+      return st;
     decode_tc_kernel<368><<<grid, kThreads, kSmAlloc, stream>>>(p);
   }
   if (const int st = launch_status()) return st;

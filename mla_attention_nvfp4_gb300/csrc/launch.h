@@ -20,6 +20,11 @@ void set_last_error(const char* message);
 // SM count of the current device, or -MLA_ERR_UNSUPPORTED_DEVICE when it
 // is not sm_103.
 int current_device_sms();
+// Raise `kernel`'s dynamic shared memory limit to `bytes` on the current
+// device, once per device and kernel slot (the attribute persists), so that
+// launches inside a stream capture make no attribute calls.  `slot` names
+// the kernel (0 .. 15).
+int smem_limit_once(const void* kernel, int bytes, int slot);
 
 int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, int64_t pe_stride,
                        const int64_t* slot_mapping, int64_t num_tokens, uint8_t* cache,

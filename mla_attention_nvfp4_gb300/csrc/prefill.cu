@@ -23,23 +23,26 @@
 // Warp roles (512 threads, four warpgroups):
 //   warp 0       scheduler and TMA producer: takes items, hands their
 //                indices to the other roles through a shared-memory ring,
-//                loads K and V blocks of 128 keys into two-stage rings
-//                (128-byte swizzled rows; the K slot of block g is free once
-//                S_{g-2} completed, the V slot once P.V of block g-2 did)
+//                loads K and V blocks of 128 keys into two-stage rings by
+//                the CTA's global block count g (128-byte swizzled rows; the
+//                K slot of block g is free once S of block g-2 completed,
+//                the V slot once its P.V did)
 //                and, per item, Q once the previous item's last score
 //                products have read it; the next item is taken one item
 //                ahead and its Q tile prefetched into L2.
 //   warps 1, 3   MMA issuers, one thread each.  Issuer w takes the key
-//                blocks of parity w:
+//                blocks j of each item with j mod 2 = w:
 //                  S_g = Q K_g^T   M=128 N=128 K=192, A and B from smem
 //                  O_w += P_g V_g  M=128 N=128 K=128, A (P) from TMEM,
 //                                  B = V tile read MN-major
-//                in the order S_g, P.V of g, S_{g+2}: in-order issue from
-//                one thread keeps S_{g+2} behind the P.V that reads P_g in
-//                the same TMEM buffer.  A thread's barrier polls queue behind
+//                in the order S_j, P.V of j, S_{j+2}: in-order issue from
+//                one thread keeps S_{j+2} behind the P.V that reads P_j in
+//                the same TMEM buffer.  The split depends only on j, so an
+//                item's arithmetic is the same whichever CTA runs it and the
+//                output is identical from run to run.  A thread's barrier polls queue behind
 //                its own MMAs, so one issuer per parity keeps the tensor pipe
 //                fed from the other issuer while one waits.
-//   warps 4..11  softmax: warpgroup w takes the key blocks of parity w, one
+//   warps 4..11  softmax: warpgroup w takes the same blocks as issuer w, one
 //                thread per query row over all 128 keys, with its own
 //                running max, row sum and partial O_w.  The two warpgroups
 //                never exchange data inside an item.  A warpgroup signals
@@ -109,7 +112,7 @@ constexpr int kRing = 4;  // item indices in flight from the producer to the oth
 
 struct alignas(8) Barriers {
   uint64_t q_full, q_empty;
-  uint64_t k_full[2];  // a K slot is free again once S of its previous block completed (s_full)
+  uint64_t k_full[2], k_empty[2];  // K slots by global block parity
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2];  // by block parity = softmax warpgroup = MMA issuer
   uint64_t o_full;                // both issuers' P.V of an item retired
@@ -245,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.q_empty, 2);  // one arrival per MMA issuer
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < w.n_kv; ++j) {
           const int s = nk & 1;  // global block index
           const uint32_t ph = (nk >> 1) & 1;
-          if (!(ok = mbar_wait(&bars.s_full[s], ph ^ 1, err, &abort_s))) break;
+          if (!(ok = mbar_wait(&bars.k_empty[s], ph ^ 1, err, &abort_s))) break;
           mbar_expect_tx(&bars.k_full[s], kKBytes);
           tma_load_4d(sK + s * kKBytes, &tm_k, 0, w.h, w.seq_begin + j * kBN, 0, &bars.k_full[s]);
           ++nk;
@@ -325,17 +329,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int g = max(0, nv - 2); g < nv; ++g) mbar_wait(&bars.v_full[g & 1], (g >> 1) & 1, err, nullptr);
     } else if ((warp == 1 || warp == 3) && lane == 0) {
       // ------------------------------------------------------- MMA issuers
-      // Issuer w (warp 1: w = 0, warp 3: w = 1) takes the key blocks of
-      // parity w, which use only K/V slot w, S/P buffer w and partial O_w,
-      // and issues S_g then P.V of block g before S of block g+2: in-order
-      // issue from one thread keeps S_{g+2} behind the P.V that reads P_g.
-      // The two issuers' MMAs interleave on the tensor pipe.
+      // Issuer w (warp 1: w = 0, warp 3: w = 1) takes the key blocks j of
+      // each item with j mod 2 = w, which use S/P buffer w and partial O_w,
+      // and issues S_j then P.V of block j before S of block j+2: in-order
+      // issue from one thread keeps S_{j+2} behind the P.V that reads P_j.
+      // The split depends only on j, so an item's arithmetic is the same
+      // whichever CTA runs it.  K/V slots follow the CTA's global block
+      // count.  The two issuers' MMAs interleave on the tensor pipe.
       const int w = warp == 1 ? 0 : 1;
       // Descriptors are built once; a K-step only adds its byte offset >> 4
       // to the start-address field (addresses stay below 256 KB, no carry).
       const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 0, 1024);
-      const uint64_t dk = smem_desc_sw128(smem_u32(sK) + w * kKBytes, 0, 1024);
-      const uint64_t dv = smem_desc_sw128(smem_u32(sV) + w * kVBytes, 16384, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
+      const uint64_t dk1 = smem_desc_sw128(smem_u32(sK) + kKBytes, 0, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), 16384, 1024);
+      const uint64_t dv1 = smem_desc_sw128(smem_u32(sV) + kVBytes, 16384, 1024);
       const uint32_t sd = w ? tS[1] : tS[0];
       const uint32_t od = w ? tO[1] : tO[0];
       int gb = 0, cw = 0;  // global block counter; blocks of this issuer
@@ -347,18 +355,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx < 0) break;
         bool dummy = false;
         const Item wi = item_at(p, static_cast<uint32_t>(idx), dummy);
-        // this issuer's blocks of the item: j = j0, j0 + 2, ...
-        const int j0 = (gb & 1) == w ? 0 : 1;
+        // this issuer's blocks of the item: j = w, w + 2, ...
+        const int j0 = w;
         const int j_last = j0 < wi.n_kv ? j0 + ((wi.n_kv - 1 - j0) & ~1) : -1;
         for (int j = j0; j < wi.n_kv; j += 2, ++cw) {
           const uint32_t ph = cw & 1;
+          const int g = gb + j;  // global block: K/V slot g mod 2
+          const int s = g & 1;
           if ((j == j0 && !mbar_wait(&bars.q_full, it & 1, err, &abort_s)) ||
-              !mbar_wait(&bars.k_full[w], ph, err, &abort_s)) {
+              !mbar_wait(&bars.k_full[s], (g >> 1) & 1, err, &abort_s)) {
             ok = false;
             break;
           }
           tc_fence_after();
           // 12 K-steps: three 64-feature chunks of 16 KB, 32 bytes per step
+          const uint64_t dk = s ? dk1 : dk0;
 #pragma unroll 1
           for (int c = 0; c < kDqk / 64; ++c) {
             const uint64_t a = dq + c * (16384 >> 4), bdesc = dk + c * (16384 >> 4);
@@ -366,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k4 = 0; k4 < 4; ++k4) mma_ss(sd, a + k4 * 2, bdesc + k4 * 2, kIdescS, (c | k4) != 0 ? 1u : 0u);
           }
           mma_commit(&bars.s_full[w]);
+          mma_commit(&bars.k_empty[s]);
           if (j == j_last) mma_commit(&bars.q_empty);
           // P.V: the item's first one for this issuer overwrites O_w, which
           // the previous item's epilogue must have read; P_g implies V_g landed
@@ -377,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // 8 K-steps of 16 keys: P columns +8, V rows +2048 bytes
           const uint32_t first = j == j0 ? 1u : 0u;  // the item's first P.V overwrites O_w
+          const uint64_t dv = s ? dv1 : dv0;
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
             const uint64_t bdesc = dv + h * ((4 * 2048) >> 4);
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k4 = 0; k4 < 4; ++k4)
               mma_ts(od, sd + (4 * h + k4) * 8, bdesc + k4 * (2048 >> 4), kIdescPV, (first & (h == 0) & (k4 == 0)) ? 0u : 1u);
           }
-          mma_commit(&bars.v_empty[w]);
+          mma_commit(&bars.v_empty[s]);
           if (j == j_last) mma_commit(&bars.o_full);
         }
         if (!ok) break;
@@ -408,9 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ softmax
-    // Warpgroup wg takes the key blocks of global parity wg, one thread per
-    // query row over all 128 keys of the block, with its own running max,
-    // row sum and partial O; the epilogue merges the two partial results.
+    // Warpgroup wg takes the key blocks j of each item with j mod 2 = wg, one
+    // thread per query row over all 128 keys of the block, with its own
+    // running max, row sum and partial O; the epilogue merges the two
+    // partial results.
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
@@ -431,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_run = -INFINITY, l_run = 0.f;
       bool any = false;  // this warpgroup had a block of this item
       for (int j = 0; j < w.n_kv; ++j, ++gb) {
-        if ((gb & 1) != wg) continue;
+        if ((j & 1) != wg) continue;
         if (!warp_wait(&bars.s_full[wg], cw & 1, err, &abort_s)) {
           ok = false;
           break;
@@ -506,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
         tmem_st_wait();
         tc_fence_before();
-        if (!warp_wait(&bars.v_full[wg], cw & 1, err, &abort_s)) {
+        if (!warp_wait(&bars.v_full[gb & 1], (gb >> 1) & 1, err, &abort_s)) {
           ok = false;
           break;
         }
@@ -709,8 +723,8 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms) {
   p.scales = a.out_scales;
   p.lse = a.lse;
   p.error_word = a.error_word;
-  if (const int st = cuda_status(cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemAlloc)))) return st;
+  if (const int st = smem_limit_once(reinterpret_cast<const void*>(prefill_tc_kernel), static_cast<int>(kSmemAlloc), 0))
+    return st;
   if (p.num_items == 0) return MLA_OK;
   // persistent: one CTA per SM
   const int grid = p.num_items < static_cast<uint32_t>(num_sms) ? static_cast<int>(p.num_items) : num_sms;
