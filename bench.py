@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -87,7 +88,14 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # raw samples: $MLA_BENCH_CLOCKS_DIR/clocks_gpu<i>.csv when set (kept), else a temporary file
+        keep = os.environ.get("MLA_BENCH_CLOCKS_DIR")
+        self.temporary = not keep
+        if keep:
+            self.path = os.path.join(keep, f"clocks_gpu{gpu_index}.csv")
+        else:
+            fd, self.path = tempfile.mkstemp(prefix=f"mla_clocks_gpu{gpu_index}_", suffix=".csv")
+            os.close(fd)
 
     def __enter__(self):
         try:
@@ -110,6 +118,13 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        try:
+            return self._summary()
+        finally:
+            if self.temporary and os.path.exists(self.path):
+                os.remove(self.path)
+
+    def _summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm, smax, reasons = [], None, set()
