@@ -582,6 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16(tO[1] + lane_off + col, u0);
           tmem_ld16(tO[1] + lane_off + col + 16, u1);
           tmem_ld_wait();
+          if (half == 1 && qq == 1) {
+            // last read of O: the issuers may start the next item's PV
+            // while this quarter is quantised and stored
+            tc_fence_before();
+            mbar_arrive(&bars.o_empty[o]);
+          }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float y0 = c0 > 0.f ? c0 * __uint_as_float(v0[i]) : 0.f;
@@ -613,8 +619,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[static_cast<int64_t>(w.h) * p.total + m] = l_tot > 0.f ? (m_row + log2f(l_tot)) * kLn2 : -INFINITY;
         if (!gs_ok && qi == 0) flag_error(err, MLA_DEVERR_SCALE);
       }
-      tc_fence_before();
-      mbar_arrive(&bars.o_empty[o]);
     }
   }
   if (bad) flag_error(err, MLA_DEVERR_BOUNDS);
