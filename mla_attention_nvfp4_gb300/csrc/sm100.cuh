@@ -1,5 +1,5 @@
 // Blackwell (sm_100 family, built for sm_103a) primitives in inline PTX:
-// mbarriers with bounded waits, bulk and tensor async copies, tcgen05 MMA
+// mbarriers with bounded waits, tensor-map (TMA) copies, tcgen05 MMA
 // with TMEM accumulators, TMEM loads/stores, shared-memory matrix and
 // instruction descriptors.
 //
@@ -22,19 +22,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Explicit shared-memory accesses on 32-bit shared addresses (the dynamic
-// shared-memory base is realigned through integer arithmetic, after which
-// the compiler no longer knows a pointer's address space).
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -101,27 +88,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
-// ----------------------------------------------------------- async copies
-// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
-// src, dst 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// 3-D tiled tensor copy global -> shared (coordinates innermost first).
-__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
+// --------------------------------------------------------- tensor maps
+// Pull a kernel-parameter tensor map into the descriptor cache ahead of its
+// first TMA copy.
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -247,66 +216,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// ------------------------------------------------------------- swizzle
-// Byte offset of element (row, k) of a bf16 tile stored as 128-byte-swizzled
-// atoms: 64 elements (128 B) per row, 8-row atoms of 1024 B; the 16-byte
-// chunk index is XOR-ed with row % 8.  Column block kb = k / 64 lies at
-// kb * rows * 128.
-__host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t k, uint32_t rows) {
-  return (k >> 6) * rows * 128u + row * 128u + ((((k & 63u) >> 3) ^ (row & 7u)) << 4) + ((k & 7u) << 1);
-}
-
-}  // namespace sm100
-}  // namespace mla
-
-namespace mla {
-namespace sm100 {
-
-// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// ------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Shared address of the same variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-// 16-byte store into a peer CTA's shared memory, counted in bytes on the
-// peer's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          remote_addr),
-      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
-      : "memory");
-}
-
-// ----------------------------------------------------------- cp.async
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-
-// One arrival on `bar` once every cp.async this thread issued has landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 }  // namespace sm100
 }  // namespace mla
