@@ -297,22 +297,21 @@ def run_ours(args, rank, world):
     }
     dominant = max(leg_ms, key=lambda n: leg_ms[n])
 
-    # --- end to end through the public API with pinned host buffers -------
+    # --- end to end through the C-ABI call with pinned host buffers -------
     e2e = None
     if args.e2e:
-        h_q = w.q.cpu().pin_memory()
-        h_pt = w.page_table.cpu().pin_memory()
+        h_q = w.q.cpu().contiguous().pin_memory()
+        h_pt = w.page_table.cpu().contiguous().pin_memory()
         h_sl = w.seq_lens.cpu().pin_memory()
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         d_q, d_pt, d_sl = torch.empty_like(w.q), torch.empty_like(w.page_table), torch.empty_like(w.seq_lens)
 
         def e2e_decode():
-            d_q.copy_(h_q, non_blocking=True)
-            d_pt.copy_(h_pt, non_blocking=True)
-            d_sl.copy_(h_sl, non_blocking=True)
-            mla.mla_nvfp4_decode(d_q, cache, gs, w.softmax_scale, page_table=d_pt, seq_lens=d_sl, out=out,
-                                 workspace=ws, error_word=err, num_splits=decode_splits)
-            h_out.copy_(out, non_blocking=True)
+            # one library call: H2D of q / page table / lengths, decode, D2H of out
+            mla.mla_nvfp4_decode_host(h_q, d_q, cache, gs, w.softmax_scale, h_out, out,
+                                      page_table_host=h_pt, page_table_dev=d_pt, seq_lens_host=h_sl,
+                                      seq_lens_dev=d_sl, workspace=ws, error_word=err,
+                                      num_splits=decode_splits)
 
         for _ in range(args.warmup):
             e2e_decode()
@@ -332,8 +331,8 @@ def run_ours(args, rank, world):
         d2h = h_out.numel() * 2
         e2e = {"value": world * dec_b / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms": ms,
-               "what": "decode leg through the public API: H2D q/page table/lengths from pinned memory, "
-                       "decode, D2H of out; cache resident"}
+               "what": "decode leg through the C-ABI call mla_nvfp4_decode_host: H2D q/page table/lengths "
+                       "from pinned memory, decode, D2H of out; cache resident"}
 
     torch.cuda.synchronize()
     if int(err.item()) != 0:

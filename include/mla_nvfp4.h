@@ -202,6 +202,45 @@ int mla_nvfp4_decode_noalloc(const void* q, int batch, int num_heads, const uint
                              uint32_t* error_word, void* stream);
 
 /*
+ * mla_nvfp4_decode from and to host memory: the form a serving loop calls
+ * once per step when the step's queries and page table are produced on the
+ * host and its output is read there.  The pages describe no such entry
+ * point; it keeps a step's host traffic inside one library call.  Enqueued
+ * on `stream`, in order: one cudaMemcpyAsync per input from host memory
+ * into the caller's device buffer for it (q; then page_table and seq_lens,
+ * or topk), the decode of mla_nvfp4_decode on those device copies, and one
+ * cudaMemcpyAsync per output back to host memory (out; then lse when both
+ * lse pointers are given).
+ *   *_host       : host memory with the shapes and types of the matching
+ *                  mla_nvfp4_decode argument: q_host bf16 [batch, num_heads,
+ *                  576]; page_table_host int32 [batch, page_table_stride]
+ *                  (contiguous) and seq_lens_host int32 [batch], or
+ *                  topk_host int32 [batch, topk]; out_host bf16 [batch,
+ *                  num_heads, 512]; lse_host fp32 [batch, num_heads] or NULL.
+ *                  Page-locked memory makes the copies asynchronous; with
+ *                  pageable memory a copy may finish before the call returns.
+ *   *_dev        : device buffers of the same sizes, owned by the caller,
+ *                  that receive the inputs and hold the outputs before their
+ *                  copy back (q_dev and out_dev 16-byte aligned).  Each host
+ *                  pointer comes with its device pointer (both NULL or both
+ *                  set).
+ *   Other arguments and the result are those of mla_nvfp4_decode.
+ *   Return       : argument checks run before anything is enqueued; a copy
+ *                  that cannot be enqueued returns MLA_ERR_LAUNCH (see
+ *                  mla_nvfp4_last_error).  The host buffers must stay
+ *                  untouched until the stream has passed the call.
+ */
+int mla_nvfp4_decode_host(const void* q_host, void* q_dev, int batch, int num_heads,
+                          const uint8_t* cache, int64_t num_slots, int record_bytes,
+                          const int32_t* page_table_host, int32_t* page_table_dev,
+                          int64_t page_table_stride, int page_size, const int32_t* seq_lens_host,
+                          int32_t* seq_lens_dev, const int32_t* topk_host, int32_t* topk_dev,
+                          int topk, float softmax_scale, const float* global_scale,
+                          void* out_host, void* out_dev, float* lse_host, float* lse_dev,
+                          void* workspace, size_t workspace_bytes, int num_splits,
+                          uint32_t* error_word, void* stream);
+
+/*
  * Causal varlen MLA prefill whose epilogue writes NVFP4 directly.
  * Source: "feat: MLA prefill NVFP4 fused output - #8" (PR description:
  * packed e2m1 output plus the global scale plus the 128x4-swizzled e4m3

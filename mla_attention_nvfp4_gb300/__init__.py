@@ -65,6 +65,10 @@ _SIGS = {
     "mla_nvfp4_decode_noalloc": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64,
                                           _c_int, _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp,
                                           _c_int, _c_vp, _c_vp]),
+    "mla_nvfp4_decode_host": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_vp,
+                                       _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_f, _c_vp,
+                                       _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, ctypes.c_size_t, _c_int, _c_vp,
+                                       _c_vp]),
     "mla_nvfp4_prefill_fused_out": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64,
                                              _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_int, _c_int,
                                              _c_f, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
@@ -227,6 +231,63 @@ def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, 
             _ptr(global_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
             num_splits, _ptr(error_word), _stream(q)))
     return (out, lse) if return_lse else out
+
+
+def _host_dev_pair(h, d, name, dtype, dev, shape):
+    """A host tensor and its device buffer: both or neither, same shape."""
+    if (h is None) != (d is None):
+        raise ValueError(f"{name}_host and {name}_dev go together")
+    if h is None:
+        return
+    if h.device.type != "cpu" or not h.is_contiguous() or h.dtype != dtype:
+        raise ValueError(f"{name}_host must be a contiguous {dtype} CPU tensor")
+    if d.device != dev or not d.is_contiguous() or d.dtype != dtype:
+        raise ValueError(f"{name}_dev must be a contiguous {dtype} tensor on {dev}")
+    if tuple(h.shape) != tuple(d.shape) or (shape is not None and tuple(h.shape) != tuple(shape)):
+        raise ValueError(f"{name}_host and {name}_dev must both have shape {shape or tuple(h.shape)}")
+
+
+def mla_nvfp4_decode_host(q_host, q_dev, cache, global_scale, softmax_scale, out_host, out_dev, *,
+                          page_table_host=None, page_table_dev=None, seq_lens_host=None,
+                          seq_lens_dev=None, page_size=64, topk_host=None, topk_dev=None,
+                          lse_host=None, lse_dev=None, workspace=None, num_splits=0,
+                          error_word=None):
+    """mla_nvfp4_decode from host tensors to host tensors through one C-ABI
+    call: the library copies the inputs into the given device buffers, runs
+    the decode and copies ``out`` (and ``lse``) back, all on the current
+    stream of ``cache``'s device.  Use pinned host tensors for asynchronous
+    copies and synchronise the stream before reading ``out_host``."""
+    dev = cache.device
+    _need(cache, "cache", torch.uint8, dev)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    if q_host.dim() != 3 or q_host.shape[2] != 576:
+        raise ValueError("q_host must be [B, H, 576]")
+    B, H, _ = q_host.shape
+    _host_dev_pair(q_host, q_dev, "q", torch.bfloat16, dev, (B, H, 576))
+    _host_dev_pair(out_host, out_dev, "out", torch.bfloat16, dev, (B, H, 512))
+    for t, name in ((page_table_host, "page_table_host"), (topk_host, "topk_host")):
+        if t is not None and (t.dim() != 2 or t.shape[0] != B):
+            raise ValueError(f"{name} must be [B, n]")
+    _host_dev_pair(page_table_host, page_table_dev, "page_table", torch.int32, dev, None)
+    _host_dev_pair(seq_lens_host, seq_lens_dev, "seq_lens", torch.int32, dev, (B,))
+    _host_dev_pair(topk_host, topk_dev, "topk", torch.int32, dev, None)
+    _host_dev_pair(lse_host, lse_dev, "lse", torch.float32, dev, (B, H))
+    lib = load_library()
+    with torch.cuda.device(dev):
+        need = lib.mla_nvfp4_decode_workspace_size(B, H, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(int(need), 256), dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, dev)
+        pt_stride = page_table_host.shape[1] if page_table_host is not None else 0
+        topk = topk_host.shape[1] if topk_host is not None else 0
+        _check("mla_nvfp4_decode_host", lib.mla_nvfp4_decode_host(
+            _ptr(q_host), _ptr(q_dev), B, H, _ptr(cache), cache.shape[0], cache.shape[1],
+            _ptr(page_table_host), _ptr(page_table_dev), pt_stride, page_size, _ptr(seq_lens_host),
+            _ptr(seq_lens_dev), _ptr(topk_host), _ptr(topk_dev), topk, float(softmax_scale),
+            _ptr(global_scale), _ptr(out_host), _ptr(out_dev), _ptr(lse_host), _ptr(lse_dev),
+            _ptr(workspace), workspace.numel(), num_splits, _ptr(error_word), _stream(cache)))
+    return out_host
 
 
 def mla_nvfp4_decode_noalloc(q, cache, global_scale, softmax_scale, out, *, page_table=None,

@@ -124,12 +124,18 @@ int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits) {
   return mla::decode_default_splits(batch, num_heads, sms > 0 ? sms : 152);
 }
 
-int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cache,
-                     int64_t num_slots, int record_bytes, const int32_t* page_table,
-                     int64_t page_table_stride, int page_size, const int32_t* seq_lens,
-                     const int32_t* topk_indices, int topk, float softmax_scale,
-                     const float* global_scale, void* out, float* lse, void* workspace,
-                     size_t workspace_bytes, int num_splits, uint32_t* error_word, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The argument checks of mla_nvfp4_decode, run before anything is enqueued;
+// on MLA_OK the launch arguments are in *a and the SM count in *sms.
+int decode_prepare(const void* q, int batch, int num_heads, const uint8_t* cache, int64_t num_slots,
+                   int record_bytes, const int32_t* page_table, int64_t page_table_stride,
+                   int page_size, const int32_t* seq_lens, const int32_t* topk_indices, int topk,
+                   float softmax_scale, const float* global_scale, void* out, float* lse,
+                   void* workspace, size_t workspace_bytes, int num_splits, uint32_t* error_word,
+                   mla::DecodeArgs* a, int* sms_out) {
   if (record_bytes != MLA_RECORD_BF16_ROPE && record_bytes != MLA_RECORD_FP8_ROPE)
     return MLA_ERR_RECORD_BYTES;
   if (batch < 0 || num_heads < 1 || num_slots < 0) return MLA_ERR_INVALID_ARG;
@@ -140,7 +146,10 @@ int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cac
                 page_table_stride < 1))
     return MLA_ERR_INVALID_ARG;
   if (sparse && topk < 0) return MLA_ERR_INVALID_ARG;
-  if (batch == 0) return MLA_OK;
+  if (batch == 0) {
+    *sms_out = 0;
+    return MLA_OK;
+  }
   if (q == nullptr || cache == nullptr || global_scale == nullptr || out == nullptr)
     return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !(softmax_scale < 3.0e38f)) return MLA_ERR_INVALID_ARG;
@@ -153,10 +162,82 @@ int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cac
   if (workspace == nullptr || workspace_bytes < need ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MLA_ERR_WORKSPACE;
-  mla::DecodeArgs a{q, batch, num_heads, cache, num_slots, record_bytes, page_table,
-                    page_table_stride, page_size, seq_lens, topk_indices, sparse ? topk : 0,
-                    softmax_scale, global_scale, out, lse, workspace, num_splits, error_word};
+  *a = mla::DecodeArgs{q, batch, num_heads, cache, num_slots, record_bytes, page_table,
+                       page_table_stride, page_size, seq_lens, topk_indices, sparse ? topk : 0,
+                       softmax_scale, global_scale, out, lse, workspace, num_splits, error_word};
+  *sms_out = sms;
+  return MLA_OK;
+}
+
+int copy_async(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cudaStream_t stream) {
+  if (bytes == 0) return MLA_OK;
+  return mla::cuda_status(cudaMemcpyAsync(dst, src, bytes, kind, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cache,
+                     int64_t num_slots, int record_bytes, const int32_t* page_table,
+                     int64_t page_table_stride, int page_size, const int32_t* seq_lens,
+                     const int32_t* topk_indices, int topk, float softmax_scale,
+                     const float* global_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, int num_splits, uint32_t* error_word, void* stream) {
+  mla::DecodeArgs a;
+  int sms = 0;
+  if (const int st = decode_prepare(q, batch, num_heads, cache, num_slots, record_bytes, page_table,
+                                    page_table_stride, page_size, seq_lens, topk_indices, topk,
+                                    softmax_scale, global_scale, out, lse, workspace,
+                                    workspace_bytes, num_splits, error_word, &a, &sms))
+    return st;
+  if (batch == 0) return MLA_OK;
   return mla::launch_decode(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+int mla_nvfp4_decode_host(const void* q_host, void* q_dev, int batch, int num_heads,
+                          const uint8_t* cache, int64_t num_slots, int record_bytes,
+                          const int32_t* page_table_host, int32_t* page_table_dev,
+                          int64_t page_table_stride, int page_size, const int32_t* seq_lens_host,
+                          int32_t* seq_lens_dev, const int32_t* topk_host, int32_t* topk_dev,
+                          int topk, float softmax_scale, const float* global_scale,
+                          void* out_host, void* out_dev, float* lse_host, float* lse_dev,
+                          void* workspace, size_t workspace_bytes, int num_splits,
+                          uint32_t* error_word, void* stream) {
+  // every host buffer comes with the device buffer that receives (or feeds) it
+  if ((q_host == nullptr) != (q_dev == nullptr) || (out_host == nullptr) != (out_dev == nullptr) ||
+      (page_table_host == nullptr) != (page_table_dev == nullptr) ||
+      (seq_lens_host == nullptr) != (seq_lens_dev == nullptr) ||
+      (topk_host == nullptr) != (topk_dev == nullptr) || (lse_host == nullptr) != (lse_dev == nullptr))
+    return record_bytes != MLA_RECORD_BF16_ROPE && record_bytes != MLA_RECORD_FP8_ROPE
+               ? MLA_ERR_RECORD_BYTES
+               : MLA_ERR_INVALID_ARG;
+  mla::DecodeArgs a;
+  int sms = 0;
+  if (const int st = decode_prepare(q_dev, batch, num_heads, cache, num_slots, record_bytes,
+                                    page_table_dev, page_table_stride, page_size, seq_lens_dev,
+                                    topk_dev, topk, softmax_scale, global_scale, out_dev, lse_dev,
+                                    workspace, workspace_bytes, num_splits, error_word, &a, &sms))
+    return st;
+  if (batch == 0) return MLA_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t b = static_cast<size_t>(batch), h = static_cast<size_t>(num_heads);
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  if (const int st = copy_async(q_dev, q_host, b * h * (MLA_D_LATENT + MLA_D_ROPE) * 2, h2d, s)) return st;
+  if (page_table_dev != nullptr) {
+    if (const int st = copy_async(page_table_dev, page_table_host,
+                                  b * static_cast<size_t>(page_table_stride) * 4, h2d, s))
+      return st;
+    if (const int st = copy_async(seq_lens_dev, seq_lens_host, b * 4, h2d, s)) return st;
+  } else {
+    if (const int st = copy_async(topk_dev, topk_host, b * static_cast<size_t>(topk) * 4, h2d, s))
+      return st;
+  }
+  if (const int st = mla::launch_decode(a, s, sms)) return st;
+  if (const int st = copy_async(out_host, out_dev, b * h * MLA_D_LATENT * 2, d2h, s)) return st;
+  if (lse_dev != nullptr)
+    if (const int st = copy_async(lse_host, lse_dev, b * h * 4, d2h, s)) return st;
+  return MLA_OK;
 }
 
 int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,

@@ -85,3 +85,22 @@ def test_decode_default_splits_and_launch_count():
     assert mla.decode_launches(64, 128, 3) == 2
     # the workspace the default needs is the one its split count needs
     assert mla.mla_nvfp4_decode_workspace_size(64, 128, 0) == mla.mla_nvfp4_decode_workspace_size(64, 128, d)
+
+
+def test_decode_host_pairs_checked_before_any_copy():
+    # every host buffer needs its device buffer: a missing one is rejected on
+    # the host, as is a bad record width, before anything is enqueued
+    lib = mla.load_library()
+    p = ctypes.c_void_p(16)
+
+    def call(q_host=p, q_dev=p, rb=432, out_dev=p, lse_host=None, lse_dev=None):
+        return lib.mla_nvfp4_decode_host(q_host, q_dev, 1, 1, p, 1, rb, p, p, 1, 64, p, p, None, None,
+                                         0, 1.0, p, p, out_dev, lse_host, lse_dev, p, 1 << 20, 1,
+                                         None, None)
+
+    assert call(q_dev=None) == 1
+    assert call(out_dev=None) == 1
+    assert call(lse_host=p) == 1
+    assert call(lse_dev=p) == 1
+    assert call(q_dev=None, rb=400) == 2
+    assert call(rb=433) == 2

@@ -99,3 +99,41 @@ def test_decode_query_range_scaling(case):
     o_ref, l_ref, o_abs = run_oracle(w, gs)
     assert_attention_close(out, o_ref, f"decode query range {case}", o_abs)
     assert_lse_close(lse, l_ref, f"decode query range {case} lse")
+
+
+@pytest.mark.parametrize("mode", ["paged", "topk"])
+def test_decode_host_buffers_match_device_call(mode):
+    # the host-buffer entry runs the same kernels on device copies of the
+    # inputs: its output and LSE equal the device call's bit for bit
+    if mode == "paged":
+        w = workloads.decode_paged("host", 3, 128, (700, 64, 1500), 432, perm_pages=True, seed=12)
+    else:
+        w = workloads.decode_topk(batch=3, heads=64, context=4096, topk=300, max_pad=8, seed=13)
+    gs = oracle_gs(w.kv_c)
+    cache = torch.zeros((w.num_slots, w.record_bytes), dtype=torch.uint8, device=DEV)
+    gst = torch.tensor([gs], device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.mla_nvfp4_cache_write(w.kv_c.to(DEV), w.k_pe.to(DEV), w.slot_mapping.to(DEV), cache, gst, err)
+    if w.paged:
+        kw = dict(page_table=w.page_table.to(DEV), seq_lens=w.seq_lens.to(DEV))
+        hw = dict(page_table_host=w.page_table.contiguous().pin_memory(),
+                  page_table_dev=torch.empty_like(w.page_table, device=DEV),
+                  seq_lens_host=w.seq_lens.pin_memory(), seq_lens_dev=torch.empty_like(w.seq_lens, device=DEV))
+    else:
+        kw = dict(topk_indices=w.topk_indices.to(DEV))
+        hw = dict(topk_host=w.topk_indices.contiguous().pin_memory(),
+                  topk_dev=torch.empty_like(w.topk_indices, device=DEV))
+    out_d, lse_d = mla.mla_nvfp4_decode(w.q.to(DEV), cache, gst, w.softmax_scale, error_word=err,
+                                        return_lse=True, **kw)
+    B, H, _ = w.q.shape
+    q_host = w.q.contiguous().pin_memory()
+    out_host = torch.empty((B, H, 512), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    mla.mla_nvfp4_decode_host(q_host, torch.empty_like(q_host, device=DEV), cache, gst, w.softmax_scale,
+                              out_host, torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV),
+                              lse_host=lse_host, lse_dev=torch.empty((B, H), dtype=torch.float32, device=DEV),
+                              error_word=err, **hw)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out_host, out_d.cpu())
+    assert torch.equal(lse_host, lse_d.cpu())
