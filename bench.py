@@ -22,6 +22,7 @@ import argparse
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -366,6 +367,36 @@ def run_ours(args, rank, world):
 # ---------------------------------------------------------------------------
 # CPU oracle (test infrastructure): the cpu_baseline leg and --impl reference
 # ---------------------------------------------------------------------------
+def host_cpu_info():
+    """(CPU model, BLAS threads) of the host running the oracle: the oracle's
+    heavy steps are NumPy matmuls, so the BLAS pool is the thread count it uses."""
+    model = platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                model = f"{ln.split(':', 1)[1].strip()} ({platform.machine()})"
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        blas = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if blas:
+            threads = max(int(i["num_threads"]) for i in blas)
+    except ImportError:
+        pass
+    if threads is None:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                threads = int(os.environ[var])
+                break
+    if threads is None:
+        threads = len(os.sched_getaffinity(0))  # BLAS default: one thread per available core
+    return model, threads
+
+
 def oracle_decode_sample(budget_s: float, device_w=None):
     """Time the float64 oracle on whole sequences of the decode batch until
     the time budget is spent; returns (GB/s in the decode metric, sample)."""
@@ -405,13 +436,14 @@ def run_reference(args, rank, world):
         if i >= args.warmup:
             vals.append(v)
     value = statistics.mean(vals)
-    cores = len(os.sched_getaffinity(0))
+    model, cores = host_cpu_info()
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": WORKLOAD},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu_model": model, "affinity_cores": len(os.sched_getaffinity(0))},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -447,8 +479,9 @@ def main():
     if rank == 0 and world == 1 and args.cpu_baseline:
         # oracle before any CUDA work, so that no forked worker sees a CUDA context
         v, sample = oracle_decode_sample(args.cpu_budget)
-        cpu_line = {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-                    "sample": sample}
+        model, cores = host_cpu_info()
+        cpu_line = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                    "cpu_model": model, "affinity_cores": len(os.sched_getaffinity(0))}
     line = run_ours(args, rank, world)
     if args.case != "full":
         what = "prefill 2x4096" if args.case == "profile" else "decode 16x4096, one split"
