@@ -102,3 +102,24 @@ def test_global_scale_exact():
     torch.cuda.synchronize()
     assert gs.item() == float(oracle_gs(x))
     assert gs.item() == float(np.float32(77.5) / np.float32(2688))
+
+
+@pytest.mark.parametrize("rb", [432, 368])
+def test_cache_write_many_tokens_per_warp_bit_exact(rb):
+    # 50,003 tokens: the grid is one wave of resident blocks, so every warp
+    # loops over about ten tokens (two per iteration, ragged last iteration);
+    # records land in a permuted slot order
+    rng = np.random.default_rng(11)
+    T = 50_003
+    kv = torch.from_numpy(rng.standard_normal((T, 512)).astype(np.float32)).to(torch.bfloat16)
+    pe = torch.from_numpy(rng.standard_normal((T, 64)).astype(np.float32)).to(torch.bfloat16)
+    slots = torch.from_numpy(rng.permutation(T).astype(np.int64))
+    gs = oracle_gs(kv)
+    ref = np.zeros((T, rb), dtype=np.uint8)
+    ocache.write_cache(ref, f32(kv), f32(pe), slots.numpy(), gs, rb)
+    cache = torch.zeros((T, rb), dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.mla_nvfp4_cache_write(kv.to(DEV), pe.to(DEV), slots.to(DEV), cache, torch.tensor([gs], device=DEV), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(cache.cpu().numpy(), ref)
