@@ -285,6 +285,23 @@ int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
                                 void* stream);
 
 /*
+ * Self-test of the bounded waits (test hook; no counterpart on the pages).
+ * Every wait of the library's pipelined kernels (decode, prefill) gives up
+ * after a time limit, ORs MLA_DEVERR_TIMEOUT into the error word and raises
+ * an abort flag that ends the CTA's other waits, so a stalled pipeline ends
+ * its kernel with a status instead of holding the GPU.  This call launches
+ * one CTA whose first wait, on a barrier nothing arrives on, runs out after
+ * limit_ns, and whose second wait, with the kernels' full 2 s limit, must
+ * then end through the abort flag.
+ *   error_word   : device uint32, receives MLA_DEVERR_TIMEOUT.
+ *   limit_ns     : the first wait's limit, 1 us .. 1 s.
+ *   elapsed_ns   : device uint64 [2] or NULL: how long each wait ran.
+ * Returns MLA_ERR_INVALID_ARG for a null error word or a limit out of range.
+ */
+int mla_nvfp4_selftest_wait(uint32_t* error_word, int64_t limit_ns, unsigned long long* elapsed_ns,
+                            void* stream);
+
+/*
  * The prefill epilogue's quantiser on its own (test hook): fp32 [M, N]
  * row-major, N a multiple of 16, into packed codes uint8 [M, N/2] and the
  * swizzled scale buffer of a [M, N/16] scale matrix (layout as for

@@ -73,6 +73,7 @@ _SIGS = {
                                              _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_int, _c_int,
                                              _c_f, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_nvfp4_quantize_rows": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_nvfp4_selftest_wait": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp]),
 }
 
 
@@ -288,6 +289,19 @@ def mla_nvfp4_decode_host(q_host, q_dev, cache, global_scale, softmax_scale, out
             _ptr(global_scale), _ptr(out_host), _ptr(out_dev), _ptr(lse_host), _ptr(lse_dev),
             _ptr(workspace), workspace.numel(), num_splits, _ptr(error_word), _stream(cache)))
     return out_host
+
+
+def mla_nvfp4_selftest_wait(error_word, limit_ns, elapsed_ns=None):
+    """Test hook: one CTA whose wait on a barrier nothing arrives on runs
+    out after ``limit_ns`` (flagging DEVERR_TIMEOUT in ``error_word``) and
+    whose second, 2-second wait then ends through the CTA's abort flag;
+    ``elapsed_ns`` (int64 [2] on the device) receives both waits' times."""
+    _need(error_word, "error_word", torch.int32)
+    _need(elapsed_ns, "elapsed_ns", torch.int64, error_word.device)
+    lib = load_library()
+    with torch.cuda.device(error_word.device):
+        _check("mla_nvfp4_selftest_wait", lib.mla_nvfp4_selftest_wait(
+            _ptr(error_word), int(limit_ns), _ptr(elapsed_ns), _stream(error_word)))
 
 
 def mla_nvfp4_decode_noalloc(q, cache, global_scale, softmax_scale, out, *, page_table=None,

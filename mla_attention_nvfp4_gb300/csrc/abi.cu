@@ -290,4 +290,12 @@ int mla_nvfp4_quantize_rows(const float* x, int64_t M, int64_t N, const float* g
                                    static_cast<cudaStream_t>(stream));
 }
 
+int mla_nvfp4_selftest_wait(uint32_t* error_word, int64_t limit_ns, unsigned long long* elapsed_ns,
+                            void* stream) {
+  if (error_word == nullptr || limit_ns < 1000 || limit_ns > 1000000000) return MLA_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  return mla::launch_selftest_wait(error_word, limit_ns, elapsed_ns, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

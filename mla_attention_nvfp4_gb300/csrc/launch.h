@@ -31,6 +31,8 @@ int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, in
                        int64_t num_slots, int record_bytes, const float* gs,
                        uint32_t* error_word, cudaStream_t stream, int num_sms);
 
+int launch_selftest_wait(uint32_t* error_word, int64_t limit_ns, unsigned long long* elapsed_ns,
+                         cudaStream_t stream);
 int launch_quantize_rows(const float* x, int64_t M, int64_t N, const float* gs, uint8_t* codes,
                          uint8_t* scales, uint32_t* error_word, cudaStream_t stream);
 

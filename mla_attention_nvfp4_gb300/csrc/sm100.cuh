@@ -66,10 +66,10 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Wait for the phase with the given parity to complete.  Returns false
 // (after flagging MLA_DEVERR_TIMEOUT and raising `abort`) if it does not
-// within kWaitLimitNs or kSpinLimit polls, or at once if another thread of
-// the CTA has raised `abort`.
+// within limit_ns (kWaitLimitNs unless given) or kSpinLimit polls, or at
+// once if another thread of the CTA has raised `abort`.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* error_word,
-                                          volatile int* abort) {
+                                          volatile int* abort, uint64_t limit_ns = kWaitLimitNs) {
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_test(bar, parity)) return true;
@@ -78,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
       const uint64_t now = global_timer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns) {
         break;
       }
     }

@@ -104,3 +104,11 @@ def test_decode_host_pairs_checked_before_any_copy():
     assert call(lse_dev=p) == 1
     assert call(q_dev=None, rb=400) == 2
     assert call(rb=433) == 2
+
+
+def test_selftest_wait_arguments_checked():
+    lib = mla.load_library()
+    p = ctypes.c_void_p(16)
+    assert lib.mla_nvfp4_selftest_wait(None, 50_000_000, None, None) == 1   # no error word
+    assert lib.mla_nvfp4_selftest_wait(p, 0, None, None) == 1               # limit below 1 us
+    assert lib.mla_nvfp4_selftest_wait(p, 2_000_000_000, None, None) == 1   # limit above 1 s
