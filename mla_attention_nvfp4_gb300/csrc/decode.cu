@@ -262,11 +262,6 @@ __device__ __forceinline__ void dequant_segment(const uint4& c, uint32_t s0, uin
   }
 }
 
-__device__ __forceinline__ void zero_units(uint32_t tile, int u0, int n, int row) {
-  for (int u = u0; u < u0 + n; ++u)
-    sts128(tile + (u >> 3) * kChunk + row * 128 + (((u & 7) ^ (row & 7)) << 4), make_uint4(0, 0, 0, 0));
-}
-
 // ------------------------------------------------------------ dequantisation
 // Thread = (key k of the tile, part Q): Q = 0 writes V units 0..23, Q = 1
 // T units 0..15 and V units 24..31, Q = 2 T units 16..31 and the RoPE chunk
@@ -317,7 +312,7 @@ struct DeqCtx {
 // Convert part Q of key k of tile j (raw bytes in r, or zeros for a padding
 // key) into the tile's operand buffers.  False if a wait gave up.
 template <int Q, int kRecord>
-__device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPart<Q, kRecord>& r, bool valid) {
+__device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPart<Q, kRecord>& r) {
   uint32_t* err = c.p.error_word;
   Barriers& bars = *c.bars;
   const int k = c.k;
@@ -325,38 +320,26 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
   const uint32_t ph = ((j >> 1) & 1) ^ 1;  // phase in which the previous user released the buffer
   if constexpr (Q == 0) {
     if (!mbar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
-    if (valid) {
 #pragma unroll
-      for (int i = 0; i < 6; ++i) dequant_segment(r.v[i], byte_of(r.v[6], 2 * i), byte_of(r.v[6], 2 * i + 1), tV, 4 * i, k);
-    } else {
-      zero_units(tV, 0, 24, k);
-    }
+    for (int i = 0; i < 6; ++i) dequant_segment(r.v[i], byte_of(r.v[6], 2 * i), byte_of(r.v[6], 2 * i + 1), tV, 4 * i, k);
     fence_async_smem();
     mbar_arrive(&bars.v_full[j & 1]);
   } else if constexpr (Q == 1) {
     if (!mbar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
-    if (valid) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dequant_segment(r.v[i], byte_of(r.v[4], 2 * i), byte_of(r.v[4], 2 * i + 1), tT, 4 * i, k);
-    } else {
-      zero_units(tT, 0, 16, k);
-    }
+    for (int i = 0; i < 4; ++i) dequant_segment(r.v[i], byte_of(r.v[4], 2 * i), byte_of(r.v[4], 2 * i + 1), tT, 4 * i, k);
     fence_async_smem();
     mbar_arrive(&bars.t_full[j & 1]);
     if (!mbar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
-    if (valid) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-        dequant_segment(r.v[5 + i], byte_of(r.v[7], 12 + 2 * i), byte_of(r.v[7], 13 + 2 * i), tV, 24 + 4 * i, k);
-    } else {
-      zero_units(tV, 24, 8, k);
-    }
+    for (int i = 0; i < 2; ++i)
+      dequant_segment(r.v[5 + i], byte_of(r.v[7], 12 + 2 * i), byte_of(r.v[7], 13 + 2 * i), tV, 24 + 4 * i, k);
     fence_async_smem();
     mbar_arrive(&bars.v_full[j & 1]);
   } else {
     if (!mbar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
     const uint32_t rope_row = tT + 4 * kChunk + k * 128;
-    if (valid) {
+    {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         dequant_segment(r.v[i], byte_of(r.v[4], 8 + 2 * i), byte_of(r.v[4], 9 + 2 * i), tT, 16 + 4 * i, k);
@@ -381,9 +364,6 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
                  make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w)));
         }
       }
-    } else {
-      zero_units(tT, 16, 16, k);
-      zero_units(tT, 32, 8, k);
     }
     fence_async_smem();
     mbar_arrive(&bars.t_full[j & 1]);
@@ -405,14 +385,23 @@ __device__ bool dequant_role(const DeqCtx& c) {
   int64_t s_nxt = nt > 1 ? slot_of(1, index_of(1)) : -1;  // tile j + 1
   int32_t i_2 = nt > 2 ? index_of(2) : -1;                // index of tile j + 2
   RawPart<Q, kRecord> ra, rb;
-  if (s_cur >= 0) load_part(ra, p.cache + s_cur * kRecord, c.rank);
+  // a padding key converts from zero bytes: codes and scale 0 give +0, the
+  // bits of an empty operand row
+  auto load_or_zero = [&](RawPart<Q, kRecord>& r, int64_t slot) {
+    if (slot >= 0) {
+      load_part(r, p.cache + slot * kRecord, c.rank);
+    } else {
+#pragma unroll
+      for (int i = 0; i < RawPart<Q, kRecord>::kN; ++i) r.v[i] = make_uint4(0, 0, 0, 0);
+    }
+  };
+  load_or_zero(ra, s_cur);
   // convert tile j from `cur` while tile j+1's bytes load into `nxt`
   auto step = [&](int j, RawPart<Q, kRecord>& cur, RawPart<Q, kRecord>& nxt) -> bool {
-    const bool valid = s_cur >= 0;
-    if (j + 1 < nt && s_nxt >= 0) load_part(nxt, p.cache + s_nxt * kRecord, c.rank);
+    if (j + 1 < nt) load_or_zero(nxt, s_nxt);
     const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
     i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
-    const bool ok = convert_part<Q, kRecord>(c, j, cur, valid);
+    const bool ok = convert_part<Q, kRecord>(c, j, cur);
     s_cur = s_nxt;
     s_nxt = s_2;
     return ok;
