@@ -481,16 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       auto latent = [&](int c, uint64_t kd, uint32_t d) {
         if (c < 3) {
           const uint32_t a0 = tmem + kTQLat + 32 * c;
-          mma_ts(d, a0, kd, kIdescQK, 1u);
-          mma_ts(d, a0 + 8, kd + 2, kIdescQK, 1u);
-          mma_ts(d, a0 + 16, kd + 4, kIdescQK, 1u);
-          mma_ts(d, a0 + 24, kd + 6, kIdescQK, 1u);
+#pragma unroll 1
+          for (int ks = 0; ks < 4; ++ks) mma_ts(d, a0 + 8 * ks, kd + 2 * ks, kIdescQK, 1u);
         } else {
           const uint64_t a0 = dq + static_cast<uint64_t>((c - 3) * (kQChunk / 16));
-          mma_ss(d, a0, kd, kIdescQK, 1u);
-          mma_ss(d, a0 + 2, kd + 2, kIdescQK, 1u);
-          mma_ss(d, a0 + 4, kd + 4, kIdescQK, 1u);
-          mma_ss(d, a0 + 6, kd + 6, kIdescQK, 1u);
+#pragma unroll 1
+          for (int ks = 0; ks < 4; ++ks) mma_ss(d, a0 + 2 * ks, kd + 2 * ks, kIdescQK, 1u);
         }
       };
       auto issue_qk_t = [&](int j) -> bool {
@@ -499,9 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         tc_fence_after();
         const uint32_t d = tmem + col_s(tb);
         const uint64_t td = dt + tb * (kTBytes / 16);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < 4; ++kk)
           mma_ts(d, tmem + kTQRope + 8 * kk, td + (4 * kChunk + 32 * kk) / 16, kIdescQK, kk > 0 ? 1u : 0u);
+#pragma unroll 1
         for (int i = 0; i < 4; ++i) latent(4 * (1 - rank) + i, td + i * (kChunk / 16), d);
         mma_commit(&bars.t_empty[tb]);
         return true;
@@ -512,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         tc_fence_after();
         const uint32_t d = tmem + col_s(vb);
         const uint64_t vd = dv + vb * (kVBytes / 16);
+#pragma unroll 1
         for (int i = 0; i < 4; ++i) latent(4 * rank + i, vd + i * (kChunk / 16), d);
         mma_commit(&bars.s_full[vb]);
         return true;
@@ -521,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         if (!mbar_wait(&bars.p_full[pb], (t >> 1) & 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint64_t vd = dpv + pb * (kVBytes / 16);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kTok / 16; ++kk)
           mma_ts(tmem + kTO, tmem + col_s(pb) + 8 * kk, vd + (2048 * kk) / 16, kIdescPV, 1u);  // O starts at 0
         mma_commit(&bars.v_empty[pb]);
