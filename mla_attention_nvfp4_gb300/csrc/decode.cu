@@ -117,6 +117,16 @@ struct Params {
   uint32_t* error_word;
 };
 
+// The kernel's waits: the first test inline, the polling loop (bounded as
+// in sm100::mbar_wait) one out-of-line copy shared by every wait, which
+// keeps the roles' hot code small.
+__device__ __noinline__ bool bar_wait_poll(uint64_t* bar, uint32_t parity, uint32_t* error_word, volatile int* abort) {
+  return mbar_wait(bar, parity, error_word, abort);
+}
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint32_t* error_word, volatile int* abort) {
+  return mbar_test(bar, parity) || bar_wait_poll(bar, parity, error_word, abort);
+}
+
 struct alignas(8) Barriers {
   uint64_t q_ready;
   uint64_t t_full[2], t_empty[2];
@@ -319,25 +329,25 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
   const uint32_t tV = c.sV + (j & 1) * kVBytes, tT = c.sT + (j & 1) * kTBytes;
   const uint32_t ph = ((j >> 1) & 1) ^ 1;  // phase in which the previous user released the buffer
   if constexpr (Q == 0) {
-    if (!mbar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
+    if (!bar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
 #pragma unroll
     for (int i = 0; i < 6; ++i) dequant_segment(r.v[i], byte_of(r.v[6], 2 * i), byte_of(r.v[6], 2 * i + 1), tV, 4 * i, k);
     fence_async_smem();
     mbar_arrive(&bars.v_full[j & 1]);
   } else if constexpr (Q == 1) {
-    if (!mbar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
+    if (!bar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
 #pragma unroll
     for (int i = 0; i < 4; ++i) dequant_segment(r.v[i], byte_of(r.v[4], 2 * i), byte_of(r.v[4], 2 * i + 1), tT, 4 * i, k);
     fence_async_smem();
     mbar_arrive(&bars.t_full[j & 1]);
-    if (!mbar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
+    if (!bar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       dequant_segment(r.v[5 + i], byte_of(r.v[7], 12 + 2 * i), byte_of(r.v[7], 13 + 2 * i), tV, 24 + 4 * i, k);
     fence_async_smem();
     mbar_arrive(&bars.v_full[j & 1]);
   } else {
-    if (!mbar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
+    if (!bar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
     const uint32_t rope_row = tT + 4 * kChunk + k * 128;
     {
 #pragma unroll
@@ -472,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       const uint64_t dv = smem_desc_sw128(sV, 0, 1024);
       const uint64_t dt = smem_desc_sw128(sT, 0, 1024);
       const uint64_t dpv = smem_desc_sw128(sV, kChunk, 1024);
-      bool ok = mbar_wait(&bars.q_ready, 0, err, &abort_s);
+      bool ok = bar_wait(&bars.q_ready, 0, err, &abort_s);
       tc_fence_after();
       // latent chunk c of Q (TMEM for c < 3, shared memory otherwise) times
       // the K chunk at descriptor kd, into scores d.  The operand-form test
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       };
       auto issue_qk_t = [&](int j) -> bool {
         const int tb = j & 1;
-        if (!mbar_wait(&bars.t_full[tb], (j >> 1) & 1, err, &abort_s)) return false;
+        if (!bar_wait(&bars.t_full[tb], (j >> 1) & 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t d = tmem + col_s(tb);
         const uint64_t td = dt + tb * (kTBytes / 16);
@@ -505,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       };
       auto issue_qk_v = [&](int j) -> bool {
         const int vb = j & 1;
-        if (!mbar_wait(&bars.v_full[vb], (j >> 1) & 1, err, &abort_s)) return false;
+        if (!bar_wait(&bars.v_full[vb], (j >> 1) & 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t d = tmem + col_s(vb);
         const uint64_t vd = dv + vb * (kVBytes / 16);
@@ -516,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       };
       auto issue_pv = [&](int t) -> bool {
         const int pb = t & 1;
-        if (!mbar_wait(&bars.p_full[pb], (t >> 1) & 1, err, &abort_s)) return false;
+        if (!bar_wait(&bars.p_full[pb], (t >> 1) & 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint64_t vd = dpv + pb * (kVBytes / 16);
 #pragma unroll 1
@@ -530,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       // softmax has written P; the other issuer's tile fills the wait
       for (int j = par; ok && j < nt; j += 2) ok = issue_qk_t(j) && issue_qk_v(j) && issue_pv(j);
       mma_commit(&bars.o_full);
-      mbar_wait(&bars.o_full, 0, err, nullptr);  // both issuers' MMAs retired
+      bar_wait(&bars.o_full, 0, err, nullptr);  // both issuers' MMAs retired
     }
   } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
     // ---------------------------------------------------------- dequantise
@@ -643,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
           ia = load_index(p, b, key + kTok);
           ib = load_index(p, b, key + kTok + 32);
         }
-        if (!mbar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
+        if (!bar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
           ok = false;
           break;
         }
@@ -681,8 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         // PV(j-1) and PV(j-2) come from different issuers; each issuer's
         // earlier P.V products retire before its later ones.
         if (__any_sync(0xffffffffu, raise && j > 0)) {
-          if (!mbar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s) ||
-              (j >= 2 && !mbar_wait(&bars.pv_done[j & 1], ((j - 2) >> 1) & 1, err, &abort_s))) {
+          if (!bar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s) ||
+              (j >= 2 && !bar_wait(&bars.pv_done[j & 1], ((j - 2) >> 1) & 1, err, &abort_s))) {
             ok = false;
             break;
           }
@@ -730,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
         tc_fence_before();
         mbar_arrive(&bars.p_full[pb]);
       }
-      if (ok) ok = mbar_wait(&bars.o_full, 0, err, &abort_s);
+      if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
     }
     // partial output of this split: O half / l (scaled by gs), lse.  TMEM
     // loads are warp-collective, so every lane loads; only stores depend on
