@@ -46,7 +46,8 @@
 //   warps 4, 11  MMA issuers (one thread each) for even and odd tiles;
 //                warp 4 owns the TMEM allocation.
 //   warps 5..10  dequantisation: thread = (key, third of the record), 16-byte
-//                loads straight from global memory a tile ahead, e2m1 -> f16
+//                loads straight from global memory as soon as the previous
+//                tile is converted, e2m1 -> f16
 //                conversion times the block scale, stores into the swizzled
 //                operand tiles.
 #include <cuda_runtime.h>
@@ -277,9 +278,12 @@ __device__ __forceinline__ void dequant_segment(const uint4& c, uint32_t s0, uin
 // T units 0..15 and V units 24..31, Q = 2 T units 16..31 and the RoPE chunk
 // (V = latent features [256 rank, +256), T = the other 256; a unit is 8
 // features).  Each thread loads the raw bytes of its part with 16-byte loads
-// straight from global memory, one tile (about 3 us) ahead of their
-// conversion.  (A bulk L2 prefetch of each record, issued per key, held the
-// issuing thread for thousands of cycles per tile and was dropped.)
+// straight from global memory into one register buffer, right after it has
+// converted the previous tile: the loads land while the thread waits for the
+// next tile's operand buffers (one buffer, and one copy of the conversion
+// code, ran faster than two buffers a tile apart).  (A bulk L2 prefetch of
+// each record, issued per key, held the issuing thread for thousands of
+// cycles per tile and was dropped.)
 
 template <int Q, int kRecord>
 struct RawPart {
@@ -391,10 +395,10 @@ __device__ bool dequant_role(const DeqCtx& c) {
   auto index_of = [&](int j) { return load_index(p, c.b, (c.tile0 + j) * kTok + c.k); };
 
   const int nt = c.nt;
-  int64_t s_cur = nt > 0 ? slot_of(0, index_of(0)) : -1;  // tile j
+  const int64_t s_cur = nt > 0 ? slot_of(0, index_of(0)) : -1;  // tile 0
   int64_t s_nxt = nt > 1 ? slot_of(1, index_of(1)) : -1;  // tile j + 1
   int32_t i_2 = nt > 2 ? index_of(2) : -1;                // index of tile j + 2
-  RawPart<Q, kRecord> ra, rb;
+  RawPart<Q, kRecord> ra;
   // a padding key converts from zero bytes: codes and scale 0 give +0, the
   // bits of an empty operand row
   auto load_or_zero = [&](RawPart<Q, kRecord>& r, int64_t slot) {
@@ -406,19 +410,15 @@ __device__ bool dequant_role(const DeqCtx& c) {
     }
   };
   load_or_zero(ra, s_cur);
-  // convert tile j from `cur` while tile j+1's bytes load into `nxt`
-  auto step = [&](int j, RawPart<Q, kRecord>& cur, RawPart<Q, kRecord>& nxt) -> bool {
-    if (j + 1 < nt) load_or_zero(nxt, s_nxt);
+  // one buffer: tile j converts from `ra`, then tile j+1's bytes load into
+  // it; the loads land while the thread waits for the next tile's buffers
+#pragma unroll 1
+  for (int j = 0; j < nt; ++j) {
     const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
     i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
-    const bool ok = convert_part<Q, kRecord>(c, j, cur);
-    s_cur = s_nxt;
+    if (!convert_part<Q, kRecord>(c, j, ra)) break;
+    if (j + 1 < nt) load_or_zero(ra, s_nxt);
     s_nxt = s_2;
-    return ok;
-  };
-  for (int j = 0; j < nt; j += 2) {
-    if (!step(j, ra, rb) || j + 1 >= nt) break;
-    if (!step(j + 1, rb, ra)) break;
   }
   return bad;
 }
