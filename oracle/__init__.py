@@ -23,10 +23,11 @@ three pages it restates:
   ``kernel.py``); the per-layer fp32 outer scale restored on read (PR
   description).
 
-Floating point is float64 except where a rounding decides an integer (a
-quantisation code or scale byte): those steps are taken in float32 with the
-operation order the library documents, so both sides take the decision in
-the same precision.
+Floating point is float64.  The NVFP4 quantisation decisions (scale byte,
+codes) are taken exactly, by comparing each input with grid midpoints times
+the scale, so they are the exact rounding of the definition's quotients; a
+kernel that evaluates the quotients in float32 may differ from them only
+where the exact quotient lies within its float32 error of a midpoint.
 
 Modules:
   nvfp4      e2m1 / e4m3 codecs, block quantisation, global scale.

@@ -138,3 +138,143 @@ def test_lossless_on_grid():
     assert np.array_equal(got_s, sbytes)
     xh = nvfp4.dequantize_blocks(got_c, got_s, gs)
     assert np.array_equal(xh, x.reshape(256, 64).astype(np.float64))
+
+
+def _nearest_even_argmin(d):
+    """Row-wise index of the smallest distance; of two equal smallest
+    distances the even index (round half to even on the code)."""
+    dmin = d.min(axis=-1, keepdims=True)
+    hit = d == dmin
+    lo = np.argmax(hit, axis=-1)
+    hi = d.shape[-1] - 1 - np.argmax(hit[..., ::-1], axis=-1)
+    return np.where(lo % 2 == 0, lo, hi)
+
+
+def _brute_force_quantize(x, gs):
+    """Nearest e4m3 scale to amax/6/gs, then nearest e2m1 magnitude to
+    |x|/S, both by exhaustive search over the grid (ties to the even code).
+    Distances are taken as |amax - 6*gs*g| and ||x| - g*S|: the products are
+    exact in float64 and so are the differences for the two grid points
+    around the value, which are the only ones a tie can involve."""
+    gs = np.float64(np.float32(gs))
+    blocks = np.asarray(x, dtype=np.float32).astype(np.float64).reshape(-1, 16)
+    amax = np.abs(blocks).max(axis=1)
+    grid = nvfp4.e4m3_decode(np.arange(0x7F))
+    sb = _nearest_even_argmin(np.abs(amax[:, None] - 6.0 * gs * grid[None, :]))
+    S = grid[sb] * gs
+    mags = nvfp4.E2M1_MAGNITUDES
+    d = np.abs(np.abs(blocks)[..., None] - mags[None, None, :] * S[:, None, None])
+    mag = _nearest_even_argmin(d)
+    codes = np.where(S[:, None] > 0, mag | (np.signbit(blocks).astype(np.int64) << 3), 0)
+    return codes.astype(np.uint8).reshape(np.shape(x)), sb.astype(np.uint8)
+
+
+def _tie_blocks(rng, n, gs):
+    """Blocks whose scale or codes sit exactly on a rounding midpoint.  gs has
+    at most 16 significant bits, so 6*gs*midpoint (scale ties) and
+    e2m1-midpoint*e4m3*gs (code ties) are float32 values."""
+    grid = nvfp4.e4m3_decode(np.arange(0x7F))
+    mids = (grid[:-1] + grid[1:]) / 2
+    out = np.zeros((2 * n, 16), dtype=np.float32)
+    # scale ties: amax exactly 6*gs*midpoint, the rest of the block below it
+    k = rng.integers(0, len(mids), n)
+    amax = 6.0 * float(gs) * mids[k]
+    out[:n] = (rng.uniform(-1, 1, (n, 16)) * amax[:, None]).astype(np.float32)
+    out[np.arange(n), rng.integers(0, 16, n)] = (amax * rng.choice([-1, 1], n)).astype(np.float32)
+    # code ties: amax = 6*S reproduces the scale byte, the other elements are
+    # +-(e2m1 midpoint)*S
+    sb = rng.integers(1, 0x7F, n)
+    S = grid[sb] * float(gs)
+    e_mids = (nvfp4.E2M1_MAGNITUDES[:-1] + nvfp4.E2M1_MAGNITUDES[1:]) / 2
+    vals = e_mids[rng.integers(0, 7, (n, 16))] * rng.choice([-1, 1], (n, 16)) * S[:, None]
+    vals[:, 0] = 6.0 * S
+    out[n:] = vals.astype(np.float32)
+    assert np.array_equal(out[n:].astype(np.float64), vals)  # the ties are exact
+    return out
+
+
+def _f32_16bit(v) -> np.float32:
+    """v as float32 with its mantissa cut to 16 significant bits."""
+    u = np.array([v], dtype=np.float32).view(np.uint32) & np.uint32(0xFFFFFF80)
+    return u.view(np.float32)[0]
+
+
+@pytest.mark.parametrize("gs", [1.0, 0.37, 2.0 ** -20, 4.5e-3])
+def test_quantize_blocks_against_brute_force(gs):
+    # >= 10^5 random blocks at magnitudes spanning the e4m3 range (subnormal
+    # scales, saturation, zero blocks) plus exact scale and code ties
+    rng = np.random.default_rng(20)
+    g = np.float32(gs)
+    n = 100_000
+    mag = np.exp2(rng.uniform(-14, 14, (n, 1))) * float(g) * 6
+    x = (rng.standard_normal((n, 16)) * mag).astype(np.float32)
+    x[:50] = 0.0
+    x[50:100] = (rng.standard_normal((50, 16)) * 1e4 * 6 * 448 * float(g)).astype(np.float32)  # saturating
+    g_tie = _f32_16bit(gs)
+    ties = _tie_blocks(rng, 5000, g_tie)
+    for xs, gg in ((x, g), (ties, g_tie)):
+        codes, sb = nvfp4.quantize_blocks(xs, gg)
+        bc, bsb = _brute_force_quantize(xs, gg)
+        assert np.array_equal(sb.reshape(-1), bsb)
+        assert np.array_equal(codes.reshape(-1, 16), bc.reshape(-1, 16))
+    # the code-tie blocks really sit on ties: every tied element took an even
+    # magnitude code (0.25 -> 0, 0.75 -> 2, 1.25 -> 2, 1.75 -> 4, 2.5 -> 4,
+    # 3.5 -> 6, 5 -> 6)
+    codes, _ = nvfp4.quantize_blocks(ties[5000:], g_tie)
+    assert np.all((codes[:, 1:] & 7) % 2 == 0)
+    assert np.all((codes[:, 0] & 7) == 7)
+
+
+def test_quantize_blocks_exact_definition_spot_values():
+    # amax/6/gs exactly halfway between e4m3 0x30 (0.5) and 0x31 (0.5625):
+    # the tie goes to the even code 0x30; a hair above goes up
+    gs = np.float32(1.0)
+    half = (0.5 + 0.5625) / 2 * 6  # 3.1875, exact in float32
+    x = np.zeros((2, 16), dtype=np.float32)
+    x[0, 0] = half
+    x[1, 0] = np.nextafter(np.float32(half), np.float32(10))
+    _, sb = nvfp4.quantize_blocks(x, gs)
+    assert sb[:, 0].tolist() == [0x30, 0x31]
+    # with S = 0.5 (sb 0x30, gs 1): x/S = 0.75 is a tie between codes 1 and 2
+    # (0.5, 1.0) and goes to 2; 1.25 between 2 and 3 goes to 2
+    y = np.array([[3.0, 0.375, 0.625, -0.375] + [0.0] * 12], dtype=np.float32)
+    codes, sb = nvfp4.quantize_blocks(y, gs)
+    assert sb[0, 0] == 0x30
+    assert codes[0, :4].tolist() == [0x7, 0x2, 0x2, 0xA]
+
+
+def _reciprocal_form(x, gs):
+    """A float32 model of a kernel that evaluates the quotients as products
+    with reciprocals: k = 1/(6 gs), s_raw = amax16 * k, r = 1/S, q = x * r
+    (each an IEEE float32 operation), then the same roundings."""
+    x = np.asarray(x, dtype=np.float32).reshape(-1, 16)
+    g = np.float32(gs)
+    k = np.float32(np.float32(1) / np.float32(np.float32(6) * g))
+    s_raw = (np.abs(x).max(1) * k).astype(np.float32)
+    sb = nvfp4.e4m3_encode(s_raw.astype(np.float64))
+    S = (nvfp4.e4m3_decode(sb).astype(np.float32) * g).astype(np.float32)
+    r = (np.float32(1) / np.where(S > 0, S, np.float32(1))).astype(np.float32)
+    q = (x * r[:, None]).astype(np.float32)
+    codes = np.where((S > 0)[:, None], nvfp4.e2m1_encode(q.astype(np.float64)), 0).astype(np.uint8)
+    return codes, sb
+
+
+def test_tie_flip_rule_accepts_float32_kernels_and_rejects_errors():
+    # Tie blocks with a gs whose reciprocals are inexact: the float32
+    # reciprocal form rounds some exact ties the other way; the comparison
+    # rule accepts exactly those (counted) and rejects a planted wrong code.
+    from tests.helpers import quant_flips
+    rng = np.random.default_rng(30)
+    g = _f32_16bit(0.37)
+    x = np.concatenate([_tie_blocks(rng, 2000, g),
+                        (rng.standard_normal((20000, 16)) * 3).astype(np.float32)]).reshape(-1, 64)
+    codes, sb = _reciprocal_form(x, g)
+    flips, n = quant_flips(x, g, codes.reshape(x.shape), sb.reshape(x.shape[0], 4), "reciprocal model", budget=1.0)
+    assert 0 < flips < n  # some exact ties do round the other way
+    # a code one magnitude step off on a random (non-tie) element is rejected
+    bad = codes.copy().reshape(x.shape)
+    row, col = 3000, 5  # rows >= 1000 hold the random blocks
+    m = bad[row, col] & 7
+    bad[row, col] = (bad[row, col] & 8) | (m + 1 if m < 7 else 6)
+    with pytest.raises(AssertionError):
+        quant_flips(x, g, bad, sb.reshape(x.shape[0], 4), "planted error", budget=1.0)
