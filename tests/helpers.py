@@ -11,8 +11,16 @@ from oracle import attention, cache as ocache, nvfp4, swizzle
 # against the float64 oracle.
 MAX_ABS = 2e-2
 MEAN_REL = 5e-3
-# Rounding-tie budget for codes where both sides do not see the same input.
+# Rounding-tie budget: mismatching codes (a mismatching scale byte counts as
+# 17: itself and its block's 16 codes) per code compared.
 TIE_BUDGET = 1e-4
+# The kernels evaluate the NVFP4 quotients in float32 as products with
+# reciprocals (1/(6 gs), then amax16 times it; 1/S, then x times it): three
+# roundings of 2^-24 relative each, so their pre-rounding value lies within
+# 3 * 2^-24 < 2^-22 (relative) of the exact quotient, and a decision can
+# differ from the exact one only where the exact quotient lies that close to
+# a grid midpoint.
+NEAR_TIE = 2.0 ** -22
 
 
 def f32(t: torch.Tensor) -> np.ndarray:
@@ -62,8 +70,12 @@ def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str, o_abs=No
     if o_abs is not None:
         excess = excess - P16_ROUNDING * np.asarray(o_abs, dtype=np.float64)
     max_abs = float(excess.max()) if err.size else 0.0
+    raw = float(err.max()) if err.size else 0.0
+    allowance = float((err - excess).max()) if err.size else 0.0
     denom = float(np.abs(ref).sum())
     mean_rel = float(err.sum() / denom) if denom > 0 else float(err.sum())
+    print(f"[attention] {what}: raw max-abs {raw:.3e}, largest rounding allowance {allowance:.3e}, "
+          f"max-abs beyond it {max_abs:.3e} (bar {MAX_ABS}), mean rel {mean_rel:.3e} (bar {MEAN_REL})")
     assert max_abs <= MAX_ABS and mean_rel <= MEAN_REL, \
         f"{what}: max_abs beyond output rounding={max_abs:.3e} (<= {MAX_ABS}), " \
         f"mean_rel={mean_rel:.3e} (<= {MEAN_REL})"
@@ -97,21 +109,26 @@ def code_boundary_distance(q: np.ndarray) -> np.ndarray:
 P_ROUNDING = 2.0 ** -8
 
 
-def check_fused_output(codes_gpu, scales_gpu, o_ref, o_abs, gs):
+def check_fused_output(codes_gpu, scales_gpu, o_ref, o_abs, gs, what="fused output"):
     """End-to-end NVFP4 output check where the kernel quantises its own fp32
     attention output.  Each output element may differ from the exact one by
     err = P_ROUNDING * o_abs (+1e-6 relative).  A scale byte may differ from
     the oracle's quantisation of the exact output only where the block's raw
     scale lies within the error of an e4m3 rounding midpoint, and a code only
     where value/scale lies within err/scale of an e2m1 midpoint (or its
-    block's scale differs).  Returns (scale mismatches, code mismatches)."""
+    block's scale differs); a code of magnitude 0 may differ in its sign bit
+    only (a value within err of zero).  Returns the counts (check_fused_blocks)."""
     M, N = o_ref.shape
-    return check_fused_blocks(codes_gpu, swizzle.unswizzle_scales(scales_gpu, M, N // 16), o_ref, o_abs, gs)
+    return check_fused_blocks(codes_gpu, swizzle.unswizzle_scales(scales_gpu, M, N // 16), o_ref, o_abs, gs,
+                              what)
 
 
-def check_fused_blocks(codes_gpu, sf_gpu, o_ref, o_abs, gs):
+def check_fused_blocks(codes_gpu, sf_gpu, o_ref, o_abs, gs, what="fused output"):
     """check_fused_output with the kernel's scale bytes already in row-major
-    [M, N/16] order (used for sampled rows of a large output)."""
+    [M, N/16] order (used for sampled rows of a large output).  Returns a
+    dict: scale bytes that differ, codes that differ in a block whose scale
+    agrees (magnitude flips at a boundary), codes that differ only in the
+    sign of a zero, and the number of codes compared; prints it."""
     M, N = o_ref.shape
     K = N // 16
     x = o_ref.astype(np.float32)
@@ -129,17 +146,83 @@ def check_fused_blocks(codes_gpu, sf_gpu, o_ref, o_abs, gs):
     mids = (grid[:-1] + grid[1:]) / 2
     near_s = np.min(np.abs(s_raw[..., None] - mids), axis=-1) <= ds
     bad_s = (sf_gpu != sb_ref)
-    assert not np.any(bad_s & ~near_s), f"{int((bad_s & ~near_s).sum())} scale bytes differ away from a tie"
+    assert not np.any(bad_s & ~near_s), f"{what}: {int((bad_s & ~near_s).sum())} scale bytes differ away from a tie"
     # codes (only in blocks whose scale agrees)
     S = (nvfp4.e4m3_decode(sb_ref) * float(gs)).repeat(16, axis=1)
     safe = np.where(S > 0, S, 1.0)
     q = np.where(S > 0, x.astype(np.float64) / safe, 0)
     near_c = code_boundary_distance(q) <= err / safe
     same_scale = (~bad_s).repeat(16, axis=1)
-    diff = (codes_g != codes_ref)
-    # the sign of a value that rounds to zero may differ
-    zero_both = ((codes_g & 7) == 0) & ((codes_ref & 7) == 0)
-    diff &= ~zero_both
-    bad = diff & same_scale & ~near_c
-    assert not np.any(bad), f"{int(bad.sum())} codes differ away from a rounding boundary"
-    return int(bad_s.sum()), int((diff & same_scale).sum())
+    diff = (codes_g != codes_ref) & same_scale
+    # a zero magnitude on both sides may differ in its sign bit, only for a
+    # value within its error of zero
+    zero_sign = diff & ((codes_g & 7) == 0) & ((codes_ref & 7) == 0)
+    assert np.all(np.abs(x[zero_sign]) <= err[zero_sign]), f"{what}: sign of a zero code differs away from zero"
+    flips = diff & ~zero_sign
+    bad = flips & ~near_c
+    assert not np.any(bad), f"{what}: {int(bad.sum())} codes differ away from a rounding boundary"
+    counts = {"scale_flips": int(bad_s.sum()), "code_flips": int(flips.sum()), "zero_sign": int(zero_sign.sum()),
+              "codes": int(codes_g.size)}
+    rate = (17 * counts["scale_flips"] + counts["code_flips"] + counts["zero_sign"]) / max(1, counts["codes"])
+    print(f"[fused] {what}: {counts} -> mismatch rate {rate:.2e}")
+    counts["rate"] = rate
+    return counts
+
+
+def _near_midpoint(v, mids, rel):
+    """|v - nearest midpoint| <= rel * v (v >= 0, float64)."""
+    return np.min(np.abs(v[..., None] - mids), axis=-1) <= rel * v
+
+
+def quant_flips(x, gs, codes_gpu, sb_gpu, what: str, budget: float = TIE_BUDGET):
+    """The kernel's NVFP4 quantisation of float32 x ([..., 16*nb]; unpacked
+    codes [..., 16*nb], scale bytes [..., nb]) against the oracle's exact
+    definition.  A scale byte may differ only by one code and only where
+    amax16/6/gs lies within NEAR_TIE of an e4m3 midpoint; a code only by one
+    magnitude step, with the same sign, where x/S lies within NEAR_TIE of an
+    e2m1 midpoint (codes of a block whose scale differs are compared with the
+    definition under the kernel's scale).  Asserts all of that and that the
+    mismatches (a scale byte counting 17) are at most `budget` of the codes;
+    returns (mismatches, codes compared) and prints them."""
+    x = np.asarray(x, dtype=np.float32)
+    nb = x.shape[-1] // 16
+    blocks = x.reshape(-1, nb, 16)
+    codes_gpu = np.asarray(codes_gpu, dtype=np.uint8).reshape(blocks.shape)
+    sb_gpu = np.asarray(sb_gpu, dtype=np.uint8).reshape(blocks.shape[:-1])
+    codes_ref, sb_ref = nvfp4.quantize_blocks(blocks.reshape(-1, nb * 16), gs)
+    codes_ref = codes_ref.reshape(blocks.shape)
+    sb_ref = sb_ref.reshape(sb_gpu.shape)
+    g = float(np.float32(gs))
+    bad_s = sb_gpu != sb_ref
+    if bad_s.any():
+        amax = np.abs(blocks).max(-1).astype(np.float64)[bad_s]
+        grid = nvfp4.e4m3_decode(np.arange(0x7F))
+        near = _near_midpoint(amax / 6.0 / g, (grid[:-1] + grid[1:]) / 2, NEAR_TIE)
+        step = np.abs(sb_gpu[bad_s].astype(int) - sb_ref[bad_s].astype(int)) == 1
+        assert np.all(near & step), f"{what}: {int((~(near & step)).sum())} scale bytes differ away from a tie"
+        # the differing blocks' codes follow the definition under the kernel's scale
+        codes_ref[bad_s] = nvfp4.encode_with_scale(blocks[bad_s], sb_gpu[bad_s], gs)
+    diff = codes_gpu != codes_ref
+    if diff.any():
+        S = (nvfp4.e4m3_decode(sb_gpu) * g)[..., None] * np.ones(16)
+        q = np.abs(blocks.astype(np.float64))[diff] / S[diff]
+        mids = (nvfp4.E2M1_MAGNITUDES[:-1] + nvfp4.E2M1_MAGNITUDES[1:]) / 2
+        cg, cr = codes_gpu[diff].astype(int), codes_ref[diff].astype(int)
+        ok = _near_midpoint(q, mids, NEAR_TIE) & ((cg >> 3) == (cr >> 3)) & (np.abs((cg & 7) - (cr & 7)) == 1)
+        assert np.all(ok), f"{what}: {int((~ok).sum())} codes differ away from a tie"
+    n_codes = codes_gpu.size
+    flips = 17 * int(bad_s.sum()) + int((diff & ~bad_s[..., None]).sum())
+    print(f"[quant] {what}: {flips} tie flips in {n_codes} codes (budget {budget:g} = {budget * n_codes:.1f})")
+    assert flips <= budget * n_codes, f"{what}: {flips} tie flips exceed {budget:g} of {n_codes} codes"
+    return flips, n_codes
+
+
+def record_flips(rec_gpu, kv_c, k_pe, gs, record_bytes: int, what: str):
+    """Cache records from the kernel against the oracle's encoder: the RoPE
+    part and the padding bit-exact, the codes and scales up to counted tie
+    flips (quant_flips).  kv_c / k_pe: the tokens' bf16 values as float32."""
+    rec_gpu = np.asarray(rec_gpu, dtype=np.uint8)
+    ref = ocache.encode_records(kv_c, k_pe, gs, record_bytes)
+    assert np.array_equal(rec_gpu[:, ocache.ROPE_OFF:], ref[:, ocache.ROPE_OFF:]), f"{what}: RoPE part or padding differs"
+    codes = nvfp4.unpack_e2m1(rec_gpu[:, ocache.CODES_OFF:ocache.SCALES_OFF])
+    return quant_flips(kv_c, gs, codes, rec_gpu[:, ocache.SCALES_OFF:ocache.ROPE_OFF], what)
