@@ -1,28 +1,37 @@
 #!/usr/bin/env python
 """Benchmark of the MLA NVFP4 hot path on GB300.
 
-One step = one pass of the whole path over one batch of synthetic input:
-  1. cache write: the 262,144 latent tokens of the DeepSeek-V3-shaped decode
-     batch (64 x 4096) quantised into 432-byte records of a paged cache;
-  2. decode: absorbed decode of that batch (64 sequences x 128 heads x 4096
-     keys, 576-d bf16 queries, random page permutation, split-K + LSE merge);
-  3. prefill: causal varlen prefill of 8 x 4096 tokens x 128 heads (q/k 192,
-     v 128) with the fused NVFP4 output.
+One step = one pass of the whole path over one batch of synthetic input of
+every workload the path is specified on:
+  1. cache write of the 262,144 latent tokens of the DeepSeek-V3-shaped
+     decode batch (64 x 4096) into 432-byte records (bf16 RoPE);
+  2. decode of that batch (64 sequences x 128 heads x 4096 keys, 576-d bf16
+     queries, random page permutation, length-aware split plan);
+  3. causal varlen prefill of 8 x 4096 tokens x 128 heads (q/k 192, v 128)
+     with the fused NVFP4 output;
+  4. cache write of the mixed-length batch's ~1.17M tokens into 368-byte
+     records (fp8 RoPE);
+  5. decode of the mixed-length batch (128 sequences, lengths log-uniform
+     1k..32k, 128 heads, 368-byte records);
+  6. sparse top-k decode (32 queries x 128 heads, 2048 of 65,536 context
+     tokens each, a few -1 entries).
 Legs are timed with CUDA events on the launching stream; L2 is flushed (a
-256 MB write) before every leg.  `value` is the decode leg's algorithmic
-HBM throughput (the metric's first part); the prefill TFLOP/s and the
-cache-write GB/s are reported beside it.
+256 MB write) before every leg.  `value` is the DeepSeek-V3-shaped decode
+leg's algorithmic HBM throughput (the metric's first part); every leg's
+GB/s, TFLOP/s and roofline fractions are reported beside it.
 
 --impl reference times the CPU oracle (test infrastructure) on a bounded
-sample of the same workload instead.
+sample of the decode workload instead.
 """
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
 import platform
+import socket
 import statistics
 import subprocess
 import sys
@@ -35,10 +44,13 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA NVFP4 decode HBM GB/s (% peak); prefill TFLOP/s with fused NVFP4 output"
 UNIT = "GB/s"
 WORKLOAD = ("decode_dsv3: B64 H128 L4096 paged 432B NVFP4 cache (cache write of its 262144 tokens + "
-            "split-K decode) + prefill_8x4096: causal varlen H128 qk192 v128 fused NVFP4 out")
+            "planned split-K decode) + prefill_8x4096: causal varlen H128 qk192 v128 fused NVFP4 out + "
+            "decode_mixed: B128 H128 L~logU(1k,32k) 368B fp8-RoPE records (cache write + decode) + "
+            "decode_topk: B32 H128 2048 of 65536 tokens, 432B")
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SM_COUNT, SM_MAX_MHZ, FP32_LANES = 152, 2070.0, 128
+CLOCK_SAMPLE_MS = 50
 
 
 def _peaks():
@@ -81,8 +93,9 @@ def prefill_bytes(p) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling; summary() keeps the samples
+    taken inside the wall-clock window it is given (the timed region)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -103,7 +116,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(CLOCK_SAMPLE_MS)],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -118,35 +131,41 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
         try:
-            return self._summary()
+            return summarize_clocks(open(self.path).read().splitlines() if self.proc is not None and
+                                    os.path.exists(self.path) else None, t0, t1)
         finally:
             if self.temporary and os.path.exists(self.path):
                 os.remove(self.path)
 
-    def _summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["unsampled"]}
-        loaded = sorted(sm)[len(sm) // 4:] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "samples": len(sm),
-                "reasons": sorted(reasons)}
+
+def summarize_clocks(lines, t0=None, t1=None):
+    """Median SM clock, max clock and the throttle reasons seen, over the
+    nvidia-smi samples whose timestamp lies in [t0, t1] (epoch seconds)."""
+    if lines is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+    sm, smax, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            mhz, mx = float(parts[2]), float(parts[3])
+        except ValueError:
+            continue
+        if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+            continue
+        sm.append(mhz)
+        smax = mx
+        for n, v in zip(names, parts[6:10]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": smax, "samples": 0, "reasons": ["unsampled"]}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "samples": len(sm), "reasons": sorted(reasons)}
 
 
 def _traffic(kernel: str):
@@ -186,6 +205,119 @@ def whole_job_rate(units_per_rank, world, ms):
     return world * units_per_rank / (ms * 1e-3)
 
 
+class CudaTimer:
+    """Per-leg CUDA events on the launching stream."""
+
+    def __init__(self, stream):
+        import torch
+        self.torch, self.stream, self.pairs = torch, stream, []
+
+    def start(self):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        return e
+
+    def stop(self, e0):
+        e1 = self.torch.cuda.Event(enable_timing=True)
+        e1.record(self.stream)
+        return (e0, e1)
+
+    def sync(self):
+        self.torch.cuda.synchronize()
+
+    @staticmethod
+    def ms(mark):
+        return mark[0].elapsed_time(mark[1])
+
+
+class HostTimer:
+    """Wall-clock stand-in for CudaTimer (host-only legs, CPU tests)."""
+
+    def start(self):
+        return time.perf_counter()
+
+    def stop(self, t0):
+        return (t0, time.perf_counter())
+
+    def sync(self):
+        pass
+
+    @staticmethod
+    def ms(mark):
+        return (mark[1] - mark[0]) * 1e3
+
+
+def time_legs(legs, steps, warmup, timer, before_leg=None, barrier=None):
+    """Run `warmup` untimed steps, then `steps` timed ones; a step runs every
+    leg once in order, `before_leg` (the L2 flush) before each, outside the
+    leg's timing.  Returns (mean ms per leg, wall-clock window (t0, t1) of
+    the timed steps)."""
+    def step(marks=None):
+        for name, fn in legs:
+            if before_leg is not None:
+                before_leg()
+            if marks is None:
+                fn()
+            else:
+                e0 = timer.start()
+                fn()
+                marks[name].append(timer.stop(e0))
+
+    for _ in range(warmup):
+        step()
+    timer.sync()
+    marks = {name: [] for name, _ in legs}
+    if barrier is not None:
+        barrier()
+    timer.sync()
+    t0 = time.time()
+    for _ in range(steps):
+        step(marks)
+    timer.sync()
+    t1 = time.time()
+    return {n: sum(timer.ms(m) for m in marks[n]) / steps for n in marks}, (t0, t1)
+
+
+def summarize(leg_ms, meta, world, peaks, peak_src, headline="decode_dsv3"):
+    """Bench-line fields from per-leg mean times (already max over ranks).
+    meta[leg] = {"bytes", "flops", "bound", "dtype", "kernel"}: algorithmic
+    bytes and flops of one launch sequence on one rank.  Rates are whole-job
+    (weak scaling: world x units over the slowest rank's time); roofline
+    fractions are per GPU against the measured peaks."""
+    hbm = float(peaks["hbm_gbs"])
+    bf16 = float(peaks["bf16_tflops"])
+    legs = {}
+    for name, ms in leg_ms.items():
+        m = meta[name]
+        gbs = whole_job_rate(m["bytes"], world, ms) / 1e9
+        tflops = whole_job_rate(m["flops"], world, ms) / 1e12 if m["flops"] else None
+        leg = {"ms": ms, "gbs": gbs, "hbm_frac": gbs / world / hbm, "dtype": m["dtype"], "bytes": m["bytes"],
+               "flops": m["flops"]}
+        if tflops is not None:
+            leg["tflops"] = tflops
+            leg["tensor_frac"] = tflops / world / bf16
+        traffic = _traffic(m["kernel"]) if m.get("kernel") else None
+        if m["bound"] == "hbm":
+            roof = {"bound": "hbm", "achieved": gbs / world, "peak": hbm, "unit": "GB/s"}
+            if traffic is not None:
+                leg["dram_gbs"] = traffic / (ms * 1e-3) / 1e9
+                leg["dram_frac"] = leg["dram_gbs"] / hbm
+        else:
+            roof = {"bound": "tensor", "achieved": tflops / world, "peak": bf16, "unit": "TFLOP/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["peak_source"] = peak_src
+        roof["traffic"] = traffic
+        leg["roofline"] = roof
+        legs[name] = leg
+    dominant = max(leg_ms, key=lambda n: leg_ms[n])
+    return {
+        "value": legs[headline]["gbs"],
+        "ms_per_step": sum(leg_ms.values()),
+        "legs": legs,
+        "roofline": dict(legs[dominant]["roofline"], kernel=dominant),
+    }
+
+
 def run_ours(args, rank, world):
     import torch
     import mla_attention_nvfp4_gb300 as mla
@@ -196,107 +328,89 @@ def run_ours(args, rank, world):
     mla.load_library()
     peaks, peak_src = _peaks()
     stream = torch.cuda.current_stream()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    # --- workload (device-resident), seed 0 -----------------------------
-    w = workloads.decode_dsv3(device=dev, batch=16 if args.case == "decode-steady" else 64)
-    decode_splits = 1 if args.case == "decode-steady" else 0
+    # --- workloads (device-resident), seed 0 ----------------------------
+    steady = args.case == "decode-steady"
+    w = workloads.decode_dsv3(device=dev, batch=16 if steady else 64)
+    decode_splits = 1 if steady else 0
     if args.case == "profile":
         # the same legs on a prefill of 2 x 4096 tokens (about 1.8 GB on the
         # device in all), for ncu captures; never a bench value
         p = workloads.prefill("prefill_2x4096", seq_lens=(4096, 4096), device=dev)
     else:
         p = workloads.prefill_8x4096(device=dev)
-    gs = mla.mla_nvfp4_global_scale(w.kv_c)
+    full = args.case == "full"
+    wm = workloads.decode_mixed(device=dev) if full else None
+    wt = workloads.decode_topk(device=dev) if full else None
+
+    def decode_setup(wl, splits):
+        gs = mla.mla_nvfp4_global_scale(wl.kv_c)
+        cache = torch.zeros((wl.num_slots, wl.record_bytes), dtype=torch.uint8, device=dev)
+        out = torch.empty((wl.batch, wl.heads, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((wl.batch, wl.heads), dtype=torch.float32, device=dev)
+        need = mla.mla_nvfp4_decode_workspace_size(wl.batch, wl.heads, splits)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+        kw = dict(page_table=wl.page_table, seq_lens=wl.seq_lens) if wl.paged else \
+            dict(topk_indices=wl.topk_indices)
+        return dict(w=wl, gs=gs, cache=cache, out=out, lse=lse, ws=ws, kw=kw, splits=splits)
+
+    def cache_write(d):
+        wl = d["w"]
+        return lambda: mla.mla_nvfp4_cache_write(wl.kv_c, wl.k_pe, wl.slot_mapping, d["cache"], d["gs"], err)
+
+    def decode(d):
+        wl = d["w"]
+        return lambda: mla.mla_nvfp4_decode(wl.q, d["cache"], d["gs"], wl.softmax_scale, out=d["out"], lse=d["lse"],
+                                            workspace=d["ws"], error_word=err, num_splits=d["splits"], **d["kw"])
+
+    ds = decode_setup(w, decode_splits)
     gsp = mla.mla_nvfp4_global_scale(p.v)
-    cache = torch.zeros((w.num_slots, w.record_bytes), dtype=torch.uint8, device=dev)
-    out = torch.empty((w.batch, w.heads, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.batch, w.heads), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(256, mla.mla_nvfp4_decode_workspace_size(w.batch, w.heads, decode_splits)), dtype=torch.uint8,
-                     device=dev)
     codes = torch.empty((p.total_tokens, p.heads * 64), dtype=torch.uint8, device=dev)
     scales = torch.empty(mla.prefill_scale_bytes(p.total_tokens, p.heads), dtype=torch.uint8, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def leg_cache_write():
-        mla.mla_nvfp4_cache_write(w.kv_c, w.k_pe, w.slot_mapping, cache, gs, err)
-
-    def leg_decode():
-        mla.mla_nvfp4_decode(w.q, cache, gs, w.softmax_scale, page_table=w.page_table, seq_lens=w.seq_lens,
-                             out=out, lse=lse, workspace=ws, error_word=err, num_splits=decode_splits)
 
     def leg_prefill():
         mla.mla_nvfp4_prefill_fused_out(p.q, p.k, p.v, p.cu_seqlens, p.max_seqlen, p.softmax_scale, gsp,
                                         out_codes=codes, out_scales=scales, error_word=err)
 
-    legs = [("cache_write", leg_cache_write), ("decode", leg_decode), ("prefill", leg_prefill)]
-    launches_per_step = mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(w.batch, w.heads, decode_splits) + \
-        mla.LAUNCHES_PER_CALL["prefill"]
-
-    def step(record=None):
-        for name, fn in legs:
-            flush.zero_()
-            if record is None:
-                fn()
-            else:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                record[name].append((e0, e1))
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item()):#x} after warm-up")
-
-    rec = {n: [] for n, _ in legs}
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            step(rec)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-    leg_ms = {n: sum(a.elapsed_time(b) for a, b in rec[n]) / args.steps for n in rec}
-    step_ms = sum(leg_ms.values())
-    step_ms, leg_ms["decode"], leg_ms["prefill"], leg_ms["cache_write"] = max_over_ranks(
-        [step_ms, leg_ms["decode"], leg_ms["prefill"], leg_ms["cache_write"]], world, dev)
-
-    dec_b, cw_b = decode_bytes(w), cache_write_bytes(w)
-    pf_flops, dec_flops = prefill_flops(p), decode_flops(w)
-    decode_gbs = whole_job_rate(dec_b, world, leg_ms["decode"]) / 1e9
-    prefill_tflops = whole_job_rate(pf_flops, world, leg_ms["prefill"]) / 1e12
-    cw_gbs = whole_job_rate(cw_b, world, leg_ms["cache_write"]) / 1e9
-    hbm = float(peaks["hbm_gbs"])
-    bf16_burst = float(peaks["bf16_tflops"])
-    fp32_alu = SM_COUNT * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12  # CUDA-core fp32 FMA peak
-
-    kinds = {k: mla.kernel_kind(k) for k in ("decode", "prefill", "cache_write")}
-
-    def roof(kind, achieved_gbs=None, achieved_tflops=None, kernel=None):
-        if kind == "hbm":
-            r = {"bound": "hbm", "achieved": achieved_gbs / world, "peak": hbm, "unit": "GB/s"}
-        elif kind == "tensor":
-            r = {"bound": "tensor", "achieved": achieved_tflops / world, "peak": bf16_burst, "unit": "TFLOP/s"}
-        else:
-            r = {"bound": "alu", "achieved": achieved_tflops / world, "peak": fp32_alu, "unit": "TFLOP/s"}
-        r["frac"] = r["achieved"] / r["peak"]
-        r["peak_source"] = f"{peak_src}" if kind != "alu" else "derived: 152 SM x 128 fp32 lanes x 2 x 2070 MHz"
-        r["traffic"] = _traffic(kernel) if kernel else None
-        return r
-
-    legs_roof = {
-        "cache_write": roof("hbm", achieved_gbs=cw_gbs, kernel="cache_write"),
-        "decode": roof(kinds["decode"], achieved_gbs=decode_gbs, achieved_tflops=world * dec_flops /
-                       (leg_ms["decode"] * 1e-3) / 1e12, kernel="decode"),
-        "prefill": roof(kinds["prefill"], achieved_tflops=prefill_tflops, kernel="prefill"),
+    legs = [("cache_write_432", cache_write(ds)), ("decode_dsv3", decode(ds)), ("prefill", leg_prefill)]
+    meta = {
+        "cache_write_432": dict(bytes=cache_write_bytes(w), flops=0, bound="hbm", dtype="fp32->nvfp4",
+                                kernel="cache_write"),
+        "decode_dsv3": dict(bytes=decode_bytes(w), flops=decode_flops(w), bound=mla.kernel_kind("decode"),
+                            dtype=mla.operand_dtype("decode"), kernel="decode"),
+        "prefill": dict(bytes=prefill_bytes(p), flops=prefill_flops(p), bound=mla.kernel_kind("prefill"),
+                        dtype=mla.operand_dtype("prefill"), kernel="prefill"),
     }
-    dominant = max(leg_ms, key=lambda n: leg_ms[n])
+    launches = mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(w.batch, w.heads, decode_splits) + \
+        mla.LAUNCHES_PER_CALL["prefill"]
+    if full:
+        dm, dt = decode_setup(wm, 0), decode_setup(wt, 0)
+        cache_write(dt)()  # the top-k cache is written once, outside the timed legs
+        legs += [("cache_write_368", cache_write(dm)), ("decode_mixed", decode(dm)), ("decode_topk", decode(dt))]
+        meta.update({
+            # the committed traffic figure is for the 432-byte launch only
+            "cache_write_368": dict(bytes=cache_write_bytes(wm), flops=0, bound="hbm", dtype="fp32->nvfp4",
+                                    kernel=None),
+            "decode_mixed": dict(bytes=decode_bytes(wm), flops=decode_flops(wm), bound=mla.kernel_kind("decode"),
+                                 dtype=mla.operand_dtype("decode"), kernel=None),
+            "decode_topk": dict(bytes=decode_bytes(wt), flops=decode_flops(wt), bound=mla.kernel_kind("decode"),
+                                dtype=mla.operand_dtype("decode"), kernel=None),
+        })
+        launches += mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(wm.batch, wm.heads, 0) + \
+            mla.decode_launches(wt.batch, wt.heads, 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else None
+    with ClockSampler(dev.index) as clk:
+        leg_ms, (t0, t1) = time_legs(legs, args.steps, args.warmup, CudaTimer(stream),
+                                     before_leg=flush.zero_, barrier=barrier)
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error word {int(err.item()):#x}")
+    clocks = clk.summary(t0, t1)
+    names = list(leg_ms)
+    leg_ms = dict(zip(names, max_over_ranks([leg_ms[n] for n in names], world, dev)))
+    line = summarize(leg_ms, meta, world, peaks, peak_src)
 
     # --- end to end through the C-ABI call with pinned host buffers -------
     e2e = None
@@ -304,64 +418,51 @@ def run_ours(args, rank, world):
         h_q = w.q.cpu().contiguous().pin_memory()
         h_pt = w.page_table.cpu().contiguous().pin_memory()
         h_sl = w.seq_lens.cpu().pin_memory()
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_out = torch.empty(ds["out"].shape, dtype=torch.bfloat16).pin_memory()
         d_q, d_pt, d_sl = torch.empty_like(w.q), torch.empty_like(w.page_table), torch.empty_like(w.seq_lens)
 
         def e2e_decode():
             # one library call: H2D of q / page table / lengths, decode, D2H of out
-            mla.mla_nvfp4_decode_host(h_q, d_q, cache, gs, w.softmax_scale, h_out, out,
+            mla.mla_nvfp4_decode_host(h_q, d_q, ds["cache"], ds["gs"], w.softmax_scale, h_out, ds["out"],
                                       page_table_host=h_pt, page_table_dev=d_pt, seq_lens_host=h_sl,
-                                      seq_lens_dev=d_sl, workspace=ws, error_word=err,
+                                      seq_lens_dev=d_sl, workspace=ds["ws"], error_word=err,
                                       num_splits=decode_splits)
 
-        for _ in range(args.warmup):
-            e2e_decode()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(args.steps):
-            flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            e2e_decode()
-            e1.record(stream)
-            times.append((e0, e1))
-        torch.cuda.synchronize()
-        ms = sum(a.elapsed_time(b) for a, b in times) / args.steps
+        e2e_ms, _ = time_legs([("e2e", e2e_decode)], args.steps, args.warmup, CudaTimer(stream),
+                              before_leg=flush.zero_, barrier=barrier)
+        ms = max_over_ranks([e2e_ms["e2e"]], world, dev)[0]
         h2d = h_q.numel() * 2 + h_pt.numel() * 4 + h_sl.numel() * 4
         d2h = h_out.numel() * 2
-        e2e = {"value": world * dec_b / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_rate(decode_bytes(w), world, ms) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms": ms,
-               "what": "decode leg through the C-ABI call mla_nvfp4_decode_host: H2D q/page table/lengths "
+               "what": "decode_dsv3 leg through the C-ABI call mla_nvfp4_decode_host: H2D q/page table/lengths "
                        "from pinned memory, decode, D2H of out; cache resident"}
 
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x}")
 
-    line = {
-        "metric": METRIC, "value": decode_gbs, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": mla.compute_dtype(), "data": "synthetic (seeded, generated on device)",
+    out = {
+        "metric": METRIC, "value": line["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": line["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": mla.operand_dtype("decode"),
+        "data": "synthetic (seeded, generated on device)",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "l2": "flushed by a 256 MB write before every leg", "decode_batch": w.batch,
                    "heads": w.heads, "seq_len": 4096, "record_bytes": w.record_bytes,
                    "prefill_tokens": p.total_tokens},
-        "decode": {"ms": leg_ms["decode"], "gbs": decode_gbs, "hbm_frac": decode_gbs / world / hbm,
-                   "tflops": world * dec_flops / (leg_ms["decode"] * 1e-3) / 1e12,
-                   "bytes": dec_b, "flops": dec_flops},
-        "prefill": {"ms": leg_ms["prefill"], "tflops": prefill_tflops,
-                    "bf16_frac": prefill_tflops / world / bf16_burst, "flops": pf_flops},
-        "cache_write": {"ms": leg_ms["cache_write"], "gbs": cw_gbs, "hbm_frac": cw_gbs / world / hbm,
-                        "bytes": cw_b},
-        "roofline": dict(legs_roof[dominant], kernel=dominant),
-        "roofline_legs": legs_roof,
-        "gpu_launches": launches_per_step * args.steps,
-        "wall_s_timed_region": wall,
+        "legs": line["legs"],
+        "roofline": line["roofline"],
+        "gpu_launches": launches * args.steps,
+        "wall_s_timed_region": t1 - t0,
         "e2e": e2e,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
-    return line
+    # the former top-level leg keys, kept for readers of earlier lines
+    out["decode"] = line["legs"]["decode_dsv3"]
+    out["prefill"] = line["legs"]["prefill"]
+    out["cache_write"] = line["legs"]["cache_write_432"]
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -462,10 +563,25 @@ def run_reference(args, rank, world):
     }
 
 
-def main():
+def _free_port():
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(n: int, argv) -> int:
+    """Run this script as n ranks (one process per GPU) through
+    torch.distributed.run on 127.0.0.1; returns their exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
@@ -473,18 +589,27 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default="full", choices=["full", "profile", "decode-steady"],
                     help="profile: smaller prefill input; decode-steady: decode of 16 x 4096 keys in one "
-                         "split (64 tiles per CTA); both for ncu captures, not bench values")
-    args = ap.parse_args()
+                         "split (64 tiles per CTA); both without the mixed-length and top-k legs, for ncu "
+                         "captures, not bench values")
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # not started by a launcher: start one rank per GPU ourselves
+        return launch_ranks(args.gpus, argv)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        return 2
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:
             print(json.dumps(line))
-        return
+        return 0
 
     if world > 1:
         import torch
@@ -506,7 +631,8 @@ def main():
     if world > 1:
         import torch
         torch.distributed.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define MLA_NVFP4_ABI_VERSION 1
+#define MLA_NVFP4_ABI_VERSION 2
 
 typedef enum mla_status {
   MLA_OK = 0,
@@ -52,6 +52,8 @@ typedef enum mla_status {
 #define MLA_DEVERR_BOUNDS 0x1u  /* slot, page or index out of range: skipped */
 #define MLA_DEVERR_TIMEOUT 0x2u /* a bounded pipeline wait gave up           */
 #define MLA_DEVERR_SCALE 0x4u   /* global scale <= 0 or not finite           */
+#define MLA_DEVERR_RANGE 0x8u   /* a value outside the kernel's operand range
+                                   (decode: |k_pe| > 65504), saturated     */
 
 /* Fixed MLA dimensions (DeepSeek-style absorbed MLA). */
 #define MLA_D_LATENT 512   /* kv_c, the NVFP4 latent; also the decode V dim */
@@ -105,19 +107,25 @@ int mla_nvfp4_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_p
                           const float* global_scale, uint32_t* error_word, void* stream);
 
 /*
- * Bytes of decode workspace needed for (batch, num_heads, num_splits);
- * num_splits <= 0 selects the library default, which is also what
- * mla_nvfp4_decode uses when given num_splits <= 0.  Never fails: returns 0
- * for invalid sizes.
+ * Bytes of decode workspace mla_nvfp4_decode needs for (batch, num_heads,
+ * num_splits) on the current device:
+ *   num_splits <= 0 : the length-aware plan (see mla_nvfp4_decode): a small
+ *                     header and work list plus room for the split partials
+ *                     of batch + SMs items, each num_heads x 2052 bytes;
+ *   num_splits == 1 : 0 (one split per sequence needs no workspace);
+ *   num_splits > 1  : batch * num_splits * num_heads * 2048 bytes of partial
+ *                     outputs plus their LSE (256-byte rounded).
+ * Never fails: returns 0 for invalid sizes.
  */
 size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits);
 
 /*
- * The number of key splits mla_nvfp4_decode uses for (batch, num_heads)
- * when given num_splits <= 0, on the current device (a value > 0 is
- * returned as given).  With one split the decode writes out and lse from
- * its own kernel (one launch); with more, a merge kernel follows (two
- * launches).  Returns 0 for invalid sizes.
+ * How mla_nvfp4_decode splits the keys for a given num_splits: the value
+ * itself when > 0 (every sequence cut into that many equal ranges of key
+ * tiles), 0 when the split is planned on the device per call from the
+ * sequence lengths (num_splits <= 0), -1 for invalid sizes.  Launches per
+ * call: one with one split, two (decode, merge) with uniform splits > 1,
+ * three (plan, decode, merge) when planned.
  */
 int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits);
 
@@ -143,9 +151,23 @@ int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits);
  *   lse          : fp32 [batch, num_heads] natural-log LSE of the scaled
  *                  scores, or NULL.  A sequence with no keys gives out = 0 and
  *                  lse = -inf.
+ *   num_splits   : > 0: every sequence's key tiles (64 keys each) are cut
+ *                  into num_splits equal ranges, one CTA pair each, merged
+ *                  by LSE.  <= 0 with a workspace: length-aware plan, made
+ *                  on the device from the lengths: every sequence is cut
+ *                  into chunks of C tiles (C chosen per call from the tile
+ *                  counts, the SM count and the workspace room), the CTA
+ *                  pairs take the chunks longest first, and sequences with
+ *                  one chunk are written directly.  <= 0 without a
+ *                  workspace (NULL): one split per sequence.
  *   workspace    : >= mla_nvfp4_decode_workspace_size(batch, num_heads,
- *                  num_splits) bytes, 256-byte aligned, contents ignored.
+ *                  num_splits) bytes, 256-byte aligned, contents ignored;
+ *                  may be NULL for one split.  A planned call given less
+ *                  than the full size uses fewer chunks (down to one per
+ *                  sequence), as long as the work list itself fits.
  * scores = softmax_scale * q . [x_hat (512), k_pe (64)], out = softmax . x_hat.
+ * k_pe values (432-byte records) enter the tensor cores as f16: a |k_pe|
+ * above 65504 saturates there and is flagged MLA_DEVERR_RANGE.
  */
 int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cache,
                      int64_t num_slots, int record_bytes, const int32_t* page_table,
@@ -154,9 +176,9 @@ int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cac
                      const float* global_scale, void* out, float* lse, void* workspace,
                      size_t workspace_bytes, int num_splits, uint32_t* error_word, void* stream);
 
-/* Largest decode the library's built-in scratch holds: batch * splits *
- * num_heads partial rows, and the bytes those rows take (the value of
- * mla_nvfp4_decode_workspace_size for that many rows). */
+/* Size of the library's built-in decode scratch: MLA_DECODE_STATIC_ROWS
+ * partial rows (one head of one split each) and the bytes those rows take
+ * (the value of mla_nvfp4_decode_workspace_size for that many rows). */
 #define MLA_DECODE_STATIC_ROWS 16384
 #define MLA_DECODE_STATIC_WORKSPACE_BYTES 33619968u /* 16384*2048 + 65536 */
 
@@ -170,24 +192,30 @@ int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cac
  * It takes the same arguments as mla_nvfp4_decode minus workspace and
  * workspace_bytes, and computes the same result with the same kernels.
  *
- *   Scratch      : the split partials live in a file-scope __device__ array
- *                  of MLA_DECODE_STATIC_WORKSPACE_BYTES bytes (one copy per
+ *   Scratch      : the split partials and the work list live in a
+ *                  file-scope __device__ array of
+ *                  MLA_DECODE_STATIC_WORKSPACE_BYTES bytes (one copy per
  *                  device, 256-byte aligned).  The call allocates nothing:
  *                  no cudaMalloc, no cudaFree, no allocating library call.
  *                  Nothing in the scratch needs to start at zero: every
- *                  call writes each partial row before its merge reads it.
- *   Limit        : batch * num_splits * num_heads (num_splits after the
- *                  default for <= 0 is applied) must not exceed
- *                  MLA_DECODE_STATIC_ROWS; larger calls return
- *                  MLA_ERR_WORKSPACE without launching, and
- *                  mla_nvfp4_last_error() names the row count and the limit.
- *                  Pass fewer splits or use mla_nvfp4_decode.
- *   First call   : the first call on a device, with that device current,
- *                  looks up the scratch's device address
- *                  (cudaGetSymbolAddress, which may load the library's
- *                  device code) and keeps it for later calls on that
- *                  device; make that first call before any stream capture
- *                  begins.  A failed lookup returns MLA_ERR_LAUNCH.
+ *                  call writes the work list and each partial row before
+ *                  they are read.
+ *   Limit        : num_splits > 1: batch * num_splits * num_heads must not
+ *                  exceed MLA_DECODE_STATIC_ROWS.  num_splits <= 0: the
+ *                  plan cuts the sequences into no more chunks than the
+ *                  scratch holds, and its work list (about 16 bytes per
+ *                  sequence) must fit.  num_splits == 1 uses no scratch.
+ *                  Calls beyond the limit return MLA_ERR_WORKSPACE without
+ *                  launching, and mla_nvfp4_last_error() names the sizes.
+ *   First call   : the first call on a device that uses the scratch, with
+ *                  that device current, looks up the scratch's device
+ *                  address (cudaGetSymbolAddress, which may load the
+ *                  library's device code) and keeps it for later calls on
+ *                  that device; make that first call before any stream
+ *                  capture begins.  A failed lookup returns MLA_ERR_LAUNCH.
+ *                  The address belongs to the device's current context: after
+ *                  cudaDeviceReset the kept address is stale, so do not call
+ *                  this entry point on a device that has been reset.
  *   Concurrency  : all calls on one device share the one scratch, so calls
  *                  whose work may overlap on the device (different
  *                  streams, or several host threads without ordering) race

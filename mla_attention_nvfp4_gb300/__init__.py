@@ -27,25 +27,28 @@ __all__ = [
 
 RECORD_BF16_ROPE = 432
 RECORD_FP8_ROPE = 368
-DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE = 0x1, 0x2, 0x4
+DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE, DEVERR_RANGE = 0x1, 0x2, 0x4, 0x8
 
 # Kernels each entry point launches (for launch accounting in the benchmark);
-# decode launches one kernel with one key split and two (plus the merge)
-# with more, see decode_launches().
-LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 2, "prefill": 1, "global_scale": 2}
+# decode launches one kernel with one key split, two (plus the merge) with
+# uniform splits and three (plan, decode, merge) when planned, see
+# decode_launches().
+LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 3, "prefill": 1, "global_scale": 2}
 # What bounds each hot kernel as built: "hbm", "tensor" (tcgen05 MMA) or
 # "alu" (CUDA-core arithmetic).
 KERNEL_BOUND = {"cache_write": "hbm", "decode": "tensor", "prefill": "tensor"}
-# Operand type of the tensor-core attention products (fp32 accumulation).
-COMPUTE_DTYPE = "bf16"
+# Operand type of each kernel's tensor-core products (fp32 accumulation):
+# the decode multiplies f16 operands (the dequantised latent c*s is exact in
+# f16), the prefill bf16 inputs as given.
+OPERAND_DTYPE = {"decode": "f16", "prefill": "bf16"}
 
 
 def kernel_kind(name: str) -> str:
     return KERNEL_BOUND[name]
 
 
-def compute_dtype() -> str:
-    return COMPUTE_DTYPE
+def operand_dtype(name: str) -> str:
+    return OPERAND_DTYPE[name]
 
 _LIB = None
 
@@ -184,15 +187,18 @@ def mla_nvfp4_decode_workspace_size(batch: int, num_heads: int, num_splits: int 
 
 
 def mla_nvfp4_decode_default_splits(batch: int, num_heads: int, num_splits: int = 0) -> int:
-    """Key splits a decode of (batch, num_heads) uses (num_splits <= 0: the
-    library default on the current device)."""
+    """Uniform key splits a decode of (batch, num_heads) uses: num_splits
+    when > 0, 0 when the split is planned on the device from the lengths,
+    -1 for invalid sizes."""
     return int(load_library().mla_nvfp4_decode_default_splits(batch, num_heads, num_splits))
 
 
 def decode_launches(batch: int, num_heads: int, num_splits: int = 0) -> int:
-    """Kernels one mla_nvfp4_decode call launches: the decode, plus the merge
-    when there is more than one key split."""
-    return 1 if mla_nvfp4_decode_default_splits(batch, num_heads, num_splits) == 1 else 2
+    """Kernels one mla_nvfp4_decode call (with a workspace) launches: the
+    decode alone with one split, plus the merge with uniform splits, plus
+    the planning kernel when planned."""
+    s = mla_nvfp4_decode_default_splits(batch, num_heads, num_splits)
+    return 3 if s == 0 else (1 if s == 1 else 2)
 
 
 def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, seq_lens=None,
@@ -218,9 +224,9 @@ def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, 
     _need(lse, "lse", torch.float32, dev)
     lib = load_library()
     with torch.cuda.device(dev):
-        need = lib.mla_nvfp4_decode_workspace_size(B, H, num_splits)
-        if workspace is None:
-            workspace = torch.empty(max(int(need), 256), dtype=torch.uint8, device=dev)
+        need = int(lib.mla_nvfp4_decode_workspace_size(B, H, num_splits))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _need(workspace, "workspace", torch.uint8, dev)
         pt_stride = page_table.stride(0) if page_table is not None else 0
         topk = topk_indices.shape[1] if topk_indices is not None else 0
@@ -229,8 +235,8 @@ def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, 
         _check("mla_nvfp4_decode", lib.mla_nvfp4_decode(
             _ptr(q), B, H, _ptr(cache), cache.shape[0], cache.shape[1], _ptr(page_table), pt_stride,
             page_size, _ptr(seq_lens), _ptr(topk_indices), topk, float(softmax_scale),
-            _ptr(global_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-            num_splits, _ptr(error_word), _stream(q)))
+            _ptr(global_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() if workspace is not None else 0, num_splits, _ptr(error_word), _stream(q)))
     return (out, lse) if return_lse else out
 
 
@@ -276,9 +282,9 @@ def mla_nvfp4_decode_host(q_host, q_dev, cache, global_scale, softmax_scale, out
     _host_dev_pair(lse_host, lse_dev, "lse", torch.float32, dev, (B, H))
     lib = load_library()
     with torch.cuda.device(dev):
-        need = lib.mla_nvfp4_decode_workspace_size(B, H, num_splits)
-        if workspace is None:
-            workspace = torch.empty(max(int(need), 256), dtype=torch.uint8, device=dev)
+        need = int(lib.mla_nvfp4_decode_workspace_size(B, H, num_splits))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _need(workspace, "workspace", torch.uint8, dev)
         pt_stride = page_table_host.shape[1] if page_table_host is not None else 0
         topk = topk_host.shape[1] if topk_host is not None else 0
@@ -287,7 +293,8 @@ def mla_nvfp4_decode_host(q_host, q_dev, cache, global_scale, softmax_scale, out
             _ptr(page_table_host), _ptr(page_table_dev), pt_stride, page_size, _ptr(seq_lens_host),
             _ptr(seq_lens_dev), _ptr(topk_host), _ptr(topk_dev), topk, float(softmax_scale),
             _ptr(global_scale), _ptr(out_host), _ptr(out_dev), _ptr(lse_host), _ptr(lse_dev),
-            _ptr(workspace), workspace.numel(), num_splits, _ptr(error_word), _stream(cache)))
+            _ptr(workspace), workspace.numel() if workspace is not None else 0, num_splits,
+            _ptr(error_word), _stream(cache)))
     return out_host
 
 

@@ -110,18 +110,17 @@ int mla_nvfp4_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_p
 
 size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits) {
   if (batch < 1 || num_heads < 1) return 0;
+  if (num_splits == 1) return 0;
   if (num_splits <= 0) {
     const int sms = device_sms();
-    num_splits = mla::decode_default_splits(batch, num_heads, sms > 0 ? sms : 152);
+    return mla::decode_plan_layout(batch, num_heads, sms > 0 ? sms : 152, 0).total;
   }
   return mla::decode_workspace_bytes(batch, num_heads, num_splits);
 }
 
 int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits) {
-  if (batch < 1 || num_heads < 1) return 0;
-  if (num_splits > 0) return num_splits;
-  const int sms = device_sms();
-  return mla::decode_default_splits(batch, num_heads, sms > 0 ? sms : 152);
+  if (batch < 1 || num_heads < 1) return -1;
+  return num_splits > 0 ? num_splits : 0;
 }
 
 }  // extern "C"
@@ -156,15 +155,24 @@ int decode_prepare(const void* q, int batch, int num_heads, const uint8_t* cache
   if (!aligned16(q) || !aligned16(cache) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
   const int sms = device_sms();
   if (sms < 0) return -sms;
-  if (num_splits <= 0) num_splits = mla::decode_default_splits(batch, num_heads, sms);
   if (num_splits > 4096) return MLA_ERR_INVALID_ARG;
-  const size_t need = mla::decode_workspace_bytes(batch, num_heads, num_splits);
-  if (workspace == nullptr || workspace_bytes < need ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return MLA_ERR_WORKSPACE;
+  // num_splits <= 0 with a workspace: the length-aware plan; without one,
+  // one split per sequence.  One split needs no workspace.
+  const bool planned = num_splits <= 0 && workspace != nullptr;
+  if (num_splits <= 0 && !planned) num_splits = 1;
+  if (planned || num_splits > 1) {
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLA_ERR_WORKSPACE;
+    if (planned) {
+      const mla::DecodePlanLayout l = mla::decode_plan_layout(batch, num_heads, sms, workspace_bytes);
+      if (workspace_bytes < l.total) return MLA_ERR_WORKSPACE;
+    } else if (workspace_bytes < mla::decode_workspace_bytes(batch, num_heads, num_splits)) {
+      return MLA_ERR_WORKSPACE;
+    }
+  }
   *a = mla::DecodeArgs{q, batch, num_heads, cache, num_slots, record_bytes, page_table,
                        page_table_stride, page_size, seq_lens, topk_indices, sparse ? topk : 0,
-                       softmax_scale, global_scale, out, lse, workspace, num_splits, error_word};
+                       softmax_scale, global_scale, out, lse, workspace, workspace_bytes,
+                       planned ? 0 : num_splits, planned, error_word};
   *sms_out = sms;
   return MLA_OK;
 }

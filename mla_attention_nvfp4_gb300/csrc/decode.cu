@@ -113,9 +113,13 @@ struct Params {
   int topk_n;
   float softmax_scale;
   const float* gs;
-  float* part_o;    // [batch, splits, heads, 512]
-  float* part_lse;  // [batch, splits, heads]
-  int splits;
+  float* part_o;    // [rows, heads, 512]: split partials
+  float* part_lse;  // [rows, heads]
+  int splits;       // uniform mode: key splits per sequence
+  // planned mode (plan_items != null): CTA pair i runs item i of the plan
+  const int32_t* plan_hdr;  // [0] items, [1] tiles per chunk
+  const int2* plan_items;   // (sequence, chunk index)
+  const int2* plan_seqs;    // (first partial row or -1, chunks) per sequence
   __nv_bfloat16* out;  // [batch, heads, 512]: written here directly when splits == 1
   float* lse;          // [batch, heads] or null (same)
   uint32_t* error_word;
@@ -240,12 +244,16 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&z);
 }
 
-// bf16x2 -> f16x2; exact inside the f16 range (8 <= 11 significant bits).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+// bf16x2 -> f16x2; exact inside the f16 range (8 <= 11 significant bits),
+// saturating to +-65504 outside it.  `amax` collects the magnitudes, so a
+// value that saturated can be flagged.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v, float& amax) {
   float lo, hi;
   bf16x2_to_f32(v, lo, hi);
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
+  amax = max3(amax, fabsf(lo), fabsf(hi));
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -329,7 +337,7 @@ struct DeqCtx {
 // Convert part Q of key k of tile j (raw bytes in r, or zeros for a padding
 // key) into the tile's operand buffers.  False if a wait gave up.
 template <int Q, int kRecord>
-__device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPart<Q, kRecord>& r) {
+__device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPart<Q, kRecord>& r, float& rope_max) {
   uint32_t* err = c.p.error_word;
   Barriers& bars = *c.bars;
   const int k = c.k;
@@ -378,7 +386,8 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
         for (int u = 0; u < 8; ++u) {
           const uint4 x = r.v[5 + u];
           sts128(rope_row + ((u ^ (k & 7)) << 4),
-                 make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w)));
+                 make_uint4(bf16x2_to_f16x2_sat(x.x, rope_max), bf16x2_to_f16x2_sat(x.y, rope_max),
+                            bf16x2_to_f16x2_sat(x.z, rope_max), bf16x2_to_f16x2_sat(x.w, rope_max)));
         }
       }
     }
@@ -389,11 +398,12 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
 }
 
 // The dequantisation loop of one thread.  Returns whether an out-of-range
-// page or slot id was met.
+// page or slot id was met; flags a RoPE value beyond the f16 range.
 template <int Q, int kRecord>
 __device__ bool dequant_role(const DeqCtx& c) {
   const Params& p = c.p;
   bool bad = false;
+  float rope_max = 0.f;
   auto slot_of = [&](int j, int32_t idx) { return key_slot(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad); };
   auto index_of = [&](int j) { return load_index(p, c.b, (c.tile0 + j) * kTok + c.k); };
 
@@ -419,10 +429,11 @@ __device__ bool dequant_role(const DeqCtx& c) {
   for (int j = 0; j < nt; ++j) {
     const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
     i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
-    if (!convert_part<Q, kRecord>(c, j, ra)) break;
+    if (!convert_part<Q, kRecord>(c, j, ra, rope_max)) break;
     if (j + 1 < nt) load_or_zero(ra, s_nxt);
     s_nxt = s_2;
   }
+  if (rope_max > 65504.f) flag_error(p.error_word, MLA_DEVERR_RANGE);
   return bad;
 }
 
@@ -435,11 +446,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = blockIdx.x & 1;
-  const int split = blockIdx.x >> 1, b = blockIdx.y, hg = blockIdx.z;
+  const int hg = blockIdx.z;
+  // work item: (sequence b, key tiles [tile0, tile0 + nt)), where its
+  // partial output goes (first row of its heads), and whether it is the
+  // sequence's only item (then it writes out and lse itself)
+  int b, tile0, per;
+  int64_t row0;
+  bool direct;
+  if (p.plan_items != nullptr) {
+    const int item = blockIdx.x >> 1;
+    if (item >= p.plan_hdr[0]) return;  // the plan has fewer items than the grid: the whole CTA leaves
+    const int2 it = p.plan_items[item];
+    const int2 sq = p.plan_seqs[it.x];
+    b = it.x;
+    per = p.plan_hdr[1];
+    tile0 = it.y * per;
+    direct = sq.x < 0;
+    row0 = direct ? 0 : static_cast<int64_t>(sq.x + it.y) * p.num_heads;
+  } else {
+    const int split = blockIdx.x >> 1;
+    b = blockIdx.y;
+    const int n_keys_u = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
+    per = ((n_keys_u + kTok - 1) / kTok + p.splits - 1) / p.splits;
+    tile0 = split * per;
+    direct = p.splits == 1;
+    row0 = (static_cast<int64_t>(b) * p.splits + split) * p.num_heads;
+  }
   const int n_keys = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
-  const int n_tiles_all = (n_keys + kTok - 1) / kTok;
-  const int per = (n_tiles_all + p.splits - 1) / p.splits;
-  const int tile0 = split * per;
+  const int n_tiles_all = n_keys / kTok + (n_keys % kTok != 0);
   const int nt = max(0, min(n_tiles_all, tile0 + per) - tile0);
   uint32_t* err = p.error_word;
 
@@ -753,10 +787,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
     const bool live = __all_sync(0xffffffffu, ok) && nt > 0;
     const bool have = live && l_run > 0.f;
     const float f = have ? gs / l_run : 0.f;
-    const int64_t row = (static_cast<int64_t>(b) * p.splits + split) * p.num_heads + head;
-    // With one split the merge is the identity (weight exp(0) = 1, sum 1):
-    // the final bf16 output and the LSE are written here and no merge runs.
-    const bool direct = p.splits == 1;
+    const int64_t row = row0 + head;
+    // For a sequence's only item the merge is the identity (weight
+    // exp(0) = 1, sum 1): the final bf16 output and the LSE are written here
+    // and no merge touches the sequence.
     float4* dst = reinterpret_cast<float4*>(p.part_o + row * 512 + 256 * rank);
     uint4* dst_bf = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + head) * 512 + 256 * rank);
     if (live) tc_fence_after();
@@ -802,27 +836,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// Merge the per-split partials of one (batch, head): LSE = ln sum exp(lse_i),
-// out = sum exp(lse_i - LSE) o_i.
-__global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restrict__ part_o,
-                                                           const float* __restrict__ part_lse,
-                                                           int splits, int num_heads,
-                                                           __nv_bfloat16* __restrict__ out,
-                                                           float* __restrict__ lse) {
-  const int b = blockIdx.x / num_heads, h = blockIdx.x % num_heads;
+// Merge n partials of one (sequence, head), rows row0, row0 + stride, ...:
+// LSE = ln sum exp(lse_i), out = sum exp(lse_i - LSE) o_i.  Thread t (of
+// 128) handles features [4t, 4t + 4).
+__device__ __forceinline__ void merge_rows(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                                           int64_t row0, int64_t stride, int n, __nv_bfloat16* __restrict__ o,
+                                           float* __restrict__ lse_out, int t) {
   float m = -INFINITY;
-  for (int s = 0; s < splits; ++s)
-    m = fmaxf(m, part_lse[(static_cast<int64_t>(b) * splits + s) * num_heads + h]);
+  for (int s = 0; s < n; ++s) m = fmaxf(m, part_lse[row0 + s * stride]);
   float tot = 0.f;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   if (m != -INFINITY) {
-    for (int s = 0; s < splits; ++s) {
-      const int64_t row = (static_cast<int64_t>(b) * splits + s) * num_heads + h;
+    for (int s = 0; s < n; ++s) {
+      const int64_t row = row0 + s * stride;
       const float l = part_lse[row];
       if (l == -INFINITY) continue;
       const float w = expf(l - m);
       tot += w;
-      const float4 v = reinterpret_cast<const float4*>(part_o + row * 512)[threadIdx.x];
+      const float4 v = reinterpret_cast<const float4*>(part_o + row * 512)[t];
       acc[0] = fmaf(w, v.x, acc[0]);
       acc[1] = fmaf(w, v.y, acc[1]);
       acc[2] = fmaf(w, v.z, acc[2]);
@@ -830,12 +861,240 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restri
     }
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  __nv_bfloat16* o = out + (static_cast<int64_t>(b) * num_heads + h) * 512 + 4 * threadIdx.x;
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-  *reinterpret_cast<uint2*>(o) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-  if (lse != nullptr && threadIdx.x == 0)
-    lse[static_cast<int64_t>(b) * num_heads + h] = (tot > 0.f) ? m + logf(tot) : -INFINITY;
+  *reinterpret_cast<uint2*>(o + 4 * t) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  if (lse_out != nullptr && t == 0) *lse_out = (tot > 0.f) ? m + logf(tot) : -INFINITY;
+}
+
+// Uniform splits: one block per (batch, head), partial rows (b, split, h).
+__global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restrict__ part_o,
+                                                           const float* __restrict__ part_lse,
+                                                           int splits, int num_heads,
+                                                           __nv_bfloat16* __restrict__ out,
+                                                           float* __restrict__ lse) {
+  const int b = blockIdx.x / num_heads, h = blockIdx.x % num_heads;
+  const int64_t bh = static_cast<int64_t>(b) * num_heads + h;
+  merge_rows(part_o, part_lse, static_cast<int64_t>(b) * splits * num_heads + h, num_heads, splits,
+             out + bh * 512, lse != nullptr ? lse + bh : nullptr, threadIdx.x);
+}
+
+// Planned chunks: block (sequence b, group of kMergeHeads heads); a sequence
+// with one chunk was written by the decode kernel and is skipped.
+constexpr int kMergeHeads = 8;
+__global__ void __launch_bounds__(256) decode_plan_merge_kernel(const float* __restrict__ part_o,
+                                                                const float* __restrict__ part_lse,
+                                                                const int2* __restrict__ seqs, int num_heads,
+                                                                __nv_bfloat16* __restrict__ out,
+                                                                float* __restrict__ lse) {
+  const int b = blockIdx.x;
+  const int2 sq = seqs[b];
+  if (sq.x < 0) return;
+  for (int hh = threadIdx.x >> 7; hh < kMergeHeads; hh += 2) {
+    const int h = blockIdx.y * kMergeHeads + hh;
+    if (h >= num_heads) break;
+    const int64_t bh = static_cast<int64_t>(b) * num_heads + h;
+    merge_rows(part_o, part_lse, static_cast<int64_t>(sq.x) * num_heads + h, num_heads, sq.y, out + bh * 512,
+               lse != nullptr ? lse + bh : nullptr, threadIdx.x & 127);
+  }
+}
+
+// ------------------------------------------------------------------ plan
+// Length-aware work list (num_splits <= 0).  Every sequence is cut into
+// chunks of C key tiles (its last chunk shorter; an empty sequence is one
+// empty chunk) and CTA pair i runs item i.  The list holds all full chunks
+// first, then the shorter last chunks from longest to shortest (64 size
+// buckets), so that the hardware, which starts CTAs in index order as SMs
+// free up, schedules longest-first.  C is chosen among ceil(tmax / k),
+// k = 1..32, by an estimate of the makespan over the resident CTA pairs P,
+// with every item costing kItemOverhead tiles on top of its own:
+//   max( ceil(full / P) * (C + o),  (tiles + o * items) / P + (mean last chunk + o) / 2 )
+// (the full chunks' waves, or the average load plus half a typical last
+// chunk), subject to the items and partial rows fitting the workspace.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 64;
+constexpr float kItemOverhead = 2.f;
+
+struct PlanArgs {
+  const int32_t* seq_lens;  // paged mode; null in top-k mode
+  int topk_n;
+  int batch, pairs, max_items, max_rows;
+  int32_t* hdr;  // [0] items, [1] tiles per chunk
+  int2* items;   // [max_items] (sequence, chunk)
+  int2* seqs;    // [batch] (first partial row or -1, chunks)
+};
+
+__device__ __forceinline__ int plan_tiles(const PlanArgs& a, int b) {
+  const int n = a.seq_lens != nullptr ? max(0, a.seq_lens[b]) : a.topk_n;
+  return n / kTok + (n % kTok != 0);
+}
+
+// Bucket of a last chunk of r tiles (0 <= r < C): longer chunks first.
+__device__ __forceinline__ int plan_bucket(int r, int C) {
+  return kPlanBuckets - 1 - static_cast<int>(static_cast<long long>(r) * kPlanBuckets / C);
+}
+
+// Exclusive prefix sum over the 1024 threads of the block; *total gets the
+// block's sum.  `sm` holds 32 ints.  Every thread must call it.
+__device__ __forceinline__ int block_scan(int v, int* sm, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = sm[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sm[lane] = w;
+  }
+  __syncthreads();
+  *total = sm[31];
+  return x - v + (warp > 0 ? sm[warp - 1] : 0);
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) decode_plan_kernel(PlanArgs a) {
+  __shared__ long long s_tot[32];
+  __shared__ int s_max[32], s_scan[32];
+  __shared__ float s_est[32];
+  __shared__ int s_hist[kPlanBuckets], s_fill[kPlanBuckets];
+  __shared__ int s_chunk;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int B = a.batch;
+
+  // total tiles and the longest sequence
+  long long tot = 0;
+  int tmax = 0;
+  for (int b = threadIdx.x; b < B; b += kPlanThreads) {
+    const int t = plan_tiles(a, b);
+    tot += t;
+    tmax = max(tmax, t);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  }
+  if (lane == 0) {
+    s_tot[warp] = tot;
+    s_max[warp] = tmax;
+  }
+  if (threadIdx.x < kPlanBuckets) {
+    s_hist[threadIdx.x] = 0;
+    s_fill[threadIdx.x] = 0;
+  }
+  __syncthreads();
+  tot = 0;
+  tmax = 0;
+  for (int w = 0; w < 32; ++w) {
+    tot += s_tot[w];
+    tmax = max(tmax, s_max[w]);
+  }
+
+  // candidate C = ceil(tmax / (warp + 1)), evaluated by one warp each
+  {
+    const int C = max(1, (tmax + warp) / (warp + 1));
+    long long n = 0, full = 0, rows = 0, last = 0;
+    for (int b = lane; b < B; b += 32) {
+      const int t = plan_tiles(a, b);
+      const int nb = max(1, t / C + (t % C != 0));
+      const int f = t / C;
+      n += nb;
+      full += f;
+      rows += nb > 1 ? nb : 0;
+      last += (t == 0 || t % C != 0) ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n += __shfl_xor_sync(0xffffffffu, n, o);
+      full += __shfl_xor_sync(0xffffffffu, full, o);
+      rows += __shfl_xor_sync(0xffffffffu, rows, o);
+      last += __shfl_xor_sync(0xffffffffu, last, o);
+    }
+    if (lane == 0) {
+      const float P = static_cast<float>(max(1, a.pairs)), o = kItemOverhead;
+      const float waves = ceilf(static_cast<float>(full) / P) * (static_cast<float>(C) + o);
+      const float rem = static_cast<float>(tot - full * static_cast<long long>(C));
+      const float avg = (static_cast<float>(tot) + o * static_cast<float>(n)) / P +
+                        (last > 0 ? 0.5f * (rem / static_cast<float>(last) + o) : 0.f);
+      const bool fits = n <= a.max_items && rows <= a.max_rows;
+      s_est[warp] = fits ? fmaxf(waves, avg) : INFINITY;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // the first minimum (largest C); candidate 0 (one chunk per sequence)
+    // always fits, since max_items >= batch and it needs no partial rows
+    int best = 0;
+    for (int w = 1; w < 32; ++w)
+      if (s_est[w] < s_est[best]) best = w;
+    s_chunk = max(1, (tmax + best) / (best + 1));
+  }
+  __syncthreads();
+  const int C = s_chunk;
+
+  // pass 1: per-sequence chunks and partial rows, full chunks in sequence
+  // order, last-chunk size histogram
+  int full_base = 0, row_base = 0;
+  for (int b0 = 0; b0 < B; b0 += kPlanThreads) {
+    const int b = b0 + threadIdx.x;
+    int t = 0, nb = 0, f = 0;
+    if (b < B) {
+      t = plan_tiles(a, b);
+      nb = max(1, t / C + (t % C != 0));
+      f = t / C;
+    }
+    const int rows_b = nb > 1 ? nb : 0;
+    int f_tot, r_tot;
+    const int f_off = block_scan(f, s_scan, &f_tot);
+    const int r_off = block_scan(rows_b, s_scan, &r_tot);
+    if (b < B) {
+      a.seqs[b] = make_int2(rows_b > 0 ? row_base + r_off : -1, nb);
+      for (int c = 0; c < f; ++c) a.items[full_base + f_off + c] = make_int2(b, c);
+      const int r = t - f * C;
+      if (t == 0 || r > 0) atomicAdd(&s_hist[plan_bucket(r, C)], 1);
+    }
+    full_base += f_tot;
+    row_base += r_tot;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the histogram (longest bucket first)
+    int h0 = s_hist[lane], h1 = s_hist[32 + lane];
+    int x0 = h0, x1 = h1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+      if (lane >= o) {
+        x0 += y0;
+        x1 += y1;
+      }
+    }
+    const int sum0 = __shfl_sync(0xffffffffu, x0, 31);
+    s_hist[lane] = x0 - h0;
+    s_hist[32 + lane] = sum0 + x1 - h1;
+    if (lane == 31) {
+      a.hdr[0] = full_base + sum0 + x1;
+      a.hdr[1] = C;
+    }
+  }
+  __syncthreads();
+  // pass 2: the last chunks, bucket by bucket after the full chunks
+  for (int b = threadIdx.x; b < B; b += kPlanThreads) {
+    const int t = plan_tiles(a, b);
+    const int f = t / C, r = t - f * C;
+    if (t == 0 || r > 0) {
+      const int k = plan_bucket(r, C);
+      a.items[full_base + s_hist[k] + atomicAdd(&s_fill[k], 1)] = make_int2(b, f);
+    }
+  }
 }
 
 }  // namespace
@@ -847,6 +1106,25 @@ size_t decode_workspace_bytes(int batch, int num_heads, int num_splits) {
   return o_bytes + l_bytes;
 }
 
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+DecodePlanLayout decode_plan_layout(int batch, int num_heads, int num_sms, size_t bytes) {
+  DecodePlanLayout l;
+  l.pairs = num_sms / 2;
+  l.max_items = batch + 2 * l.pairs;
+  l.items = 256;
+  l.seqs = align256(l.items + static_cast<size_t>(l.max_items) * sizeof(int2));
+  l.rows = align256(l.seqs + static_cast<size_t>(batch) * sizeof(int2));
+  const size_t per_row = static_cast<size_t>(num_heads) * (512 + 1) * sizeof(float);  // o and lse per chunk
+  const size_t slack = 512;                                                          // two 256-byte alignments
+  size_t max_rows = static_cast<size_t>(l.max_items);
+  if (bytes != 0) max_rows = bytes >= l.rows + slack ? (bytes - l.rows - slack) / per_row : 0;
+  l.max_rows = static_cast<int>(max_rows < static_cast<size_t>(l.max_items) ? max_rows : l.max_items);
+  l.lse = align256(l.rows + static_cast<size_t>(l.max_rows) * num_heads * 512 * sizeof(float));
+  l.total = align256(l.lse + static_cast<size_t>(l.max_rows) * num_heads * sizeof(float));
+  return l;
+}
+
 int decode_default_splits(int batch, int num_heads, int num_sms) {
   const int groups = (num_heads + kHeads - 1) / kHeads;
   const int pairs = num_sms / 2;
@@ -855,7 +1133,7 @@ int decode_default_splits(int batch, int num_heads, int num_sms) {
   return s < 1 ? 1 : (s > 64 ? 64 : s);
 }
 
-int launch_decode(const DecodeArgs& a, cudaStream_t stream, int /*num_sms*/) {
+int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.batch = a.batch;
@@ -875,12 +1153,34 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int /*num_sms*/) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.error_word = a.error_word;
-  const size_t rows = static_cast<size_t>(a.batch) * a.num_splits * a.num_heads;
-  p.part_o = static_cast<float*>(a.workspace);
-  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + rows * 512 * sizeof(float));
-
-  dim3 grid(2 * a.num_splits, a.batch, (a.num_heads + kHeads - 1) / kHeads);
-  if (grid.y > 65535u || grid.z > 65535u) return MLA_ERR_INVALID_ARG;
+  p.plan_hdr = nullptr;
+  p.plan_items = nullptr;
+  p.plan_seqs = nullptr;
+  char* ws = static_cast<char*>(a.workspace);
+  const unsigned groups = static_cast<unsigned>((a.num_heads + kHeads - 1) / kHeads);
+  dim3 grid;
+  DecodePlanLayout l{};
+  if (a.planned) {
+    l = decode_plan_layout(a.batch, a.num_heads, num_sms, a.workspace_bytes);
+    p.plan_hdr = reinterpret_cast<int32_t*>(ws);
+    p.plan_items = reinterpret_cast<int2*>(ws + l.items);
+    p.plan_seqs = reinterpret_cast<int2*>(ws + l.seqs);
+    p.part_o = reinterpret_cast<float*>(ws + l.rows);
+    p.part_lse = reinterpret_cast<float*>(ws + l.lse);
+    grid = dim3(2u * static_cast<unsigned>(l.max_items), 1u, groups);
+    PlanArgs pa{a.seq_lens, a.topk, a.batch, l.pairs, l.max_items, l.max_rows,
+                reinterpret_cast<int32_t*>(ws), reinterpret_cast<int2*>(ws + l.items),
+                reinterpret_cast<int2*>(ws + l.seqs)};
+    decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pa);
+    if (const int st = launch_status()) return st;
+  } else {
+    const size_t rows = static_cast<size_t>(a.batch) * a.num_splits * a.num_heads;
+    p.part_o = static_cast<float*>(a.workspace);
+    p.part_lse = reinterpret_cast<float*>(ws + rows * 512 * sizeof(float));
+    grid = dim3(2u * static_cast<unsigned>(a.num_splits), static_cast<unsigned>(a.batch), groups);
+    if (grid.y > 65535u) return MLA_ERR_INVALID_ARG;
+  }
+  if (grid.z > 65535u) return MLA_ERR_INVALID_ARG;
   if (a.record_bytes == 432) {
     if (const int st = smem_limit_once(reinterpret_cast<const void*>(decode_tc_kernel<432>), static_cast<int>(kSmAlloc), 1))
       return st;
@@ -891,6 +1191,12 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int /*num_sms*/) {
     decode_tc_kernel<368><<<grid, kThreads, kSmAlloc, stream>>>(p);
   }
   if (const int st = launch_status()) return st;
+  if (a.planned) {
+    decode_plan_merge_kernel<<<dim3(static_cast<unsigned>(a.batch), (a.num_heads + kMergeHeads - 1) / kMergeHeads),
+                               256, 0, stream>>>(p.part_o, p.part_lse, p.plan_seqs, a.num_heads,
+                                                 static_cast<__nv_bfloat16*>(a.out), a.lse);
+    return launch_status();
+  }
   if (a.num_splits == 1) return MLA_OK;  // the decode kernel wrote out and lse
   decode_merge_kernel<<<a.batch * a.num_heads, 128, 0, stream>>>(
       p.part_o, p.part_lse, a.num_splits, a.num_heads, static_cast<__nv_bfloat16*>(a.out), a.lse);

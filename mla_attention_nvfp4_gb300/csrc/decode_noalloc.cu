@@ -27,7 +27,7 @@ __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::atomic<void*> g_scratch[kMaxDevices];
 std::mutex g_setup;
-thread_local char t_message[256];
+thread_local char t_message[512];
 
 // Device address of the current device's scratch, looked up on the first
 // call for that device and kept afterwards.
@@ -62,19 +62,33 @@ extern "C" int mla_nvfp4_decode_noalloc(const void* q, int batch, int num_heads,
   if (batch >= 1 && num_heads >= 1) {
     const int sms = mla::current_device_sms();
     if (sms < 0) return -sms;
-    const int splits = num_splits > 0 ? num_splits : mla::decode_default_splits(batch, num_heads, sms);
-    const long long rows = static_cast<long long>(batch) * splits * num_heads;
-    if (rows > MLA_DECODE_STATIC_ROWS) {
-      std::snprintf(t_message, sizeof t_message,
-                    "mla_nvfp4_decode_noalloc: batch %d x splits %d x heads %d = %lld partial rows "
-                    "exceed the built-in scratch of %d rows (%u bytes); pass fewer splits or use "
-                    "mla_nvfp4_decode with a caller workspace",
-                    batch, splits, num_heads, rows, MLA_DECODE_STATIC_ROWS,
-                    MLA_DECODE_STATIC_WORKSPACE_BYTES);
-      mla::set_last_error(t_message);
-      return MLA_ERR_WORKSPACE;
+    if (num_splits > 1) {
+      // uniform splits: batch x splits x heads partial rows must fit
+      const long long rows = static_cast<long long>(batch) * num_splits * num_heads;
+      if (rows > MLA_DECODE_STATIC_ROWS) {
+        std::snprintf(t_message, sizeof t_message,
+                      "mla_nvfp4_decode_noalloc: batch %d x splits %d x heads %d = %lld partial rows "
+                      "exceed the built-in scratch of %d rows (%u bytes); pass fewer splits, 0 for the "
+                      "length-aware plan, or use mla_nvfp4_decode with a caller workspace",
+                      batch, num_splits, num_heads, rows, MLA_DECODE_STATIC_ROWS,
+                      MLA_DECODE_STATIC_WORKSPACE_BYTES);
+        mla::set_last_error(t_message);
+        return MLA_ERR_WORKSPACE;
+      }
+    } else if (num_splits <= 0) {
+      // the plan sizes its chunks to the scratch; its tables must fit
+      const mla::DecodePlanLayout l = mla::decode_plan_layout(batch, num_heads, sms, kScratchBytes);
+      if (l.total > kScratchBytes) {
+        std::snprintf(t_message, sizeof t_message,
+                      "mla_nvfp4_decode_noalloc: the work list of batch %d needs %zu bytes, more than the "
+                      "built-in scratch of %u bytes; pass num_splits = 1 or use mla_nvfp4_decode",
+                      batch, l.total, MLA_DECODE_STATIC_WORKSPACE_BYTES);
+        mla::set_last_error(t_message);
+        return MLA_ERR_WORKSPACE;
+      }
     }
-    if (const int st = scratch_address(&scratch)) return st;
+    if (num_splits != 1)
+      if (const int st = scratch_address(&scratch)) return st;
   }
   return mla_nvfp4_decode(q, batch, num_heads, cache, num_slots, record_bytes, page_table,
                           page_table_stride, page_size, seq_lens, topk_indices, topk,

@@ -56,13 +56,25 @@ struct DecodeArgs {
   void* out;
   float* lse;
   void* workspace;
-  int num_splits;
+  size_t workspace_bytes;
+  int num_splits;  // uniform mode: key splits per sequence
+  bool planned;    // length-aware plan computed on the device (num_splits ignored)
   uint32_t* error_word;
 };
 
-// Decode workspace layout for (batch, heads, splits).
+// Decode workspace for uniform splits: partial rows (b, split, head).
 size_t decode_workspace_bytes(int batch, int num_heads, int num_splits);
 int decode_default_splits(int batch, int num_heads, int num_sms);
+
+// Workspace of the planned decode: a 256-byte header, the item list, the
+// per-sequence chunk table, then max_rows chunk rows of partial O (heads x
+// 512 fp32 each) and their LSE.  `bytes` == 0 gives the full size (one row
+// per possible item); otherwise max_rows is what fits in `bytes`.
+struct DecodePlanLayout {
+  int pairs, max_items, max_rows;
+  size_t items, seqs, rows, lse, total;
+};
+DecodePlanLayout decode_plan_layout(int batch, int num_heads, int num_sms, size_t bytes);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms);
 
 struct PrefillArgs {

@@ -7,17 +7,25 @@
 // "Contract notes" (block 1x16 along the contraction axis, E4M3 block scale,
 // global amax/(6*448)).
 //
-// Float32 operation order of one block (every op IEEE round-to-nearest, no
-// contraction; reciprocals instead of divisions, as NVFP4 quantisers
-// usually do):
-//     k     = 1 / (6 * gs)                       once per tensor
-//     s_raw = amax16 * k
-//     sb    = e4m3 RNE-satfinite(s_raw)
-//     S     = e4m3(sb) * gs
-//     code  = e2m1 RNE-satfinite(x * (1 / S)), all codes 0 when S is 0
+// Two evaluations of the block scale and codes:
+//  * correctly rounded (block_scale_rn, encode8_rn; the cache write): the
+//    definition in IEEE float32 arithmetic, divisions included,
+//        s_raw = (amax16 / 6) / gs,   sb = e4m3 RNE-satfinite(s_raw),
+//        S     = e4m3(sb) * gs,       code = e2m1 RNE-satfinite(x / S)
+//    (all codes 0 when S is 0).  Each division a / b is computed from the
+//    correctly rounded reciprocal y = 1/b: q0 = a * y, r = a - q0 * b
+//    (exact, one fma), q = q0 + r * y (one fma), which is the correctly
+//    rounded quotient (Markstein's theorem for round-to-nearest division
+//    from a correctly rounded reciprocal): bit-identical to float32
+//    division, at two fmas per element;
+//  * reciprocal form (block_scale, encode8; the prefill epilogue and the
+//    quantise-rows hook): s_raw = amax16 * (1 / (6 gs)), q = x * (1 / S),
+//    each quotient within 1.5 ulp of the correctly rounded one, so a code or
+//    scale byte differs from it only when that quotient lies within 1.5 ulp
+//    of a rounding midpoint.  The epilogue's quantisation sits on the
+//    prefill's critical path (it holds the output accumulator), where the
+//    two fmas per element measured 7 % of the prefill.
 // A global scale outside [2^-100, 2^100] is invalid (codes and scales 0).
-// The conversions use the sm_100-family cvt instructions, which round to
-// nearest even and clamp to the largest finite value (448, 6).
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -75,13 +83,50 @@ __device__ __forceinline__ bool scale_ok(float gs) {
   return gs >= 7.888609052210118e-31f && gs <= 1.2676506002282294e30f;  // [2^-100, 2^100]
 }
 
-// k = 1 / (6 * gs): the per-tensor factor of the raw block scale.
+// a / b rounded to nearest even, given y = 1 / b rounded to nearest even
+// and a quotient that cannot overflow.
+__device__ __forceinline__ float div_rn(float a, float b, float y) {
+  const float q0 = __fmul_rn(a, y);
+  return __fmaf_rn(__fmaf_rn(-q0, b, a), y, q0);
+}
+
+// Per-tensor factors of the raw block scale: 1 / gs (correctly rounded
+// form) and 1 / (6 gs) (reciprocal form), each rounded to nearest.
+__device__ __forceinline__ float inv_scale(float gs) { return __frcp_rn(gs); }
 __device__ __forceinline__ float scale_factor(float gs) { return __frcp_rn(__fmul_rn(6.0f, gs)); }
 
-// Block scale from the block's amax (amax is exact in any reduction order)
-// and k = scale_factor(gs).  Returns the scale byte sb and sets R = 1 / S
-// with S = e4m3(sb) * gs, or R = 0 when S is 0 (the block then encodes as
-// all-zero codes).
+// Correctly rounded block scale from the block's amax (exact in any
+// reduction order) and inv_gs = inv_scale(gs).  Returns the scale byte sb
+// and sets S = e4m3(sb) * gs and R = 1 / S (rounded to nearest), or R = 0
+// when S is 0 (the block then encodes as all-zero codes).  `bounded` tells
+// whether every |x| / S of the block is at most ~6.4 (the scale did not
+// saturate), so that the codes' quotients cannot overflow.
+__device__ __forceinline__ uint32_t block_scale_rn(float amax, float inv_gs, float gs, float& R, float& S,
+                                                   bool& bounded) {
+  const float sixth = 0.16666667163372040f;  // 1/6 rounded to nearest float32
+  const float q6 = div_rn(amax, 6.0f, sixth);
+  const float s0 = __fmul_rn(q6, inv_gs);
+  const float s_raw = isfinite(s0) ? div_rn(q6, gs, inv_gs) : s0;
+  const uint32_t sb = cvt_e4m3(s_raw);
+  bounded = s_raw <= 448.0f;
+  S = __fmul_rn(e4m3_to_f32(sb), gs);
+  R = (S > 0.f) ? __frcp_rn(S) : 0.f;
+  return sb;
+}
+
+// Eight correctly rounded codes of x / S (element i in nibble i); all zero
+// when R == 0.  An unbounded block (saturated scale) keeps the reciprocal
+// products, which the conversion saturates the same way.
+__device__ __forceinline__ uint32_t encode8_rn(const float* x, float R, float S, bool bounded) {
+  if (R == 0.f) return 0u;
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = bounded ? div_rn(x[i], S, R) : __fmul_rn(x[i], R);
+  return cvt_e2m1x8(q);
+}
+
+// Reciprocal-form block scale from the block's amax and k = scale_factor(gs):
+// returns sb and sets R = 1 / S, or R = 0 when S is 0.
 __device__ __forceinline__ uint32_t block_scale(float amax, float k, float gs, float& R) {
   const uint32_t sb = cvt_e4m3(__fmul_rn(amax, k));
   const float S = __fmul_rn(e4m3_to_f32(sb), gs);
@@ -89,7 +134,8 @@ __device__ __forceinline__ uint32_t block_scale(float amax, float k, float gs, f
   return sb;
 }
 
-// Eight codes of x * R (element i in nibble i); all zero when R == 0.
+// Eight reciprocal-form codes of x * R (element i in nibble i); all zero
+// when R == 0.
 __device__ __forceinline__ uint32_t encode8(const float* x, float R) {
   if (R == 0.f) return 0u;
   float q[8];

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const float gs = *gs_ptr;
   const bool gs_valid = scale_ok(gs);
-  const float k = scale_factor(gs);
+  const float inv_gs = inv_scale(gs);
   if (!gs_valid && warp == 0 && lane == 0) flag_error(error_word, MLA_DEVERR_SCALE);
 
   // Quantise one token's record from its loaded row, latent and rope parts.
@@ -66,11 +66,12 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     am_b = fmaxf(am_b, __shfl_xor_sync(0xffffffffu, am_b, 1));
     uint32_t code_a = 0, code_b = 0, sb_a = 0, sb_b = 0;
     if (gs_valid) {
-      float Ra, Rb;
-      sb_a = block_scale(am_a, k, gs, Ra);
-      sb_b = block_scale(am_b, k, gs, Rb);
-      code_a = encode8(xa, Ra);
-      code_b = encode8(xb, Rb);
+      float Ra, Rb, Sa, Sb;
+      bool ba, bb;
+      sb_a = block_scale_rn(am_a, inv_gs, gs, Ra, Sa, ba);
+      sb_b = block_scale_rn(am_b, inv_gs, gs, Rb, Sb, bb);
+      code_a = encode8_rn(xa, Ra, Sa, ba);
+      code_b = encode8_rn(xb, Rb, Sb, bb);
     }
     uint8_t* rec = cache + slot * kRecord;
     reinterpret_cast<uint32_t*>(rec)[lane] = code_a;        // bytes [4l, 4l+4)

@@ -23,11 +23,9 @@ three pages it restates:
   ``kernel.py``); the per-layer fp32 outer scale restored on read (PR
   description).
 
-Floating point is float64.  The NVFP4 quantisation decisions (scale byte,
-codes) are taken exactly, by comparing each input with grid midpoints times
-the scale, so they are the exact rounding of the definition's quotients; a
-kernel that evaluates the quotients in float32 may differ from them only
-where the exact quotient lies within its float32 error of a midpoint.
+Floating point is float64, except the NVFP4 quantisation (scale byte and
+codes), which evaluates its definition in IEEE float32 (divisions included)
+and rounds the float32 quotients exactly onto the e4m3 / e2m1 grids.
 
 Modules:
   nvfp4      e2m1 / e4m3 codecs, block quantisation, global scale.

@@ -6,20 +6,19 @@ block scale per 16 elements along the contraction axis, with the global
 scale amax/(6*448).  Codes are e2m1 with magnitudes {0, .5, 1, 1.5, 2, 3, 4,
 6}; the block scale is e4m3(amax16 / 6 / global).
 
-The definition is evaluated exactly: for a block with maximum magnitude
-amax16 and a float32 global scale gs,
+The definition is evaluated in IEEE float32 arithmetic, every operation
+(divisions included) rounded to nearest even: for a block with maximum
+magnitude amax16 and a float32 global scale gs,
 
-    sb    = the e4m3 code nearest to amax16 / 6 / gs   (ties to the even code,
-            values above 448 saturate to 448)
-    S     = e4m3(sb) * gs
-    code  = the e2m1 code nearest to x / S             (ties to the even code,
-            magnitudes above 6 saturate to 6; all codes 0 when S == 0)
+    s_raw = f32( f32(amax16 / 6) / gs )
+    sb    = e4m3 RNE-satfinite(s_raw)         (448 for anything above)
+    S     = f32( e4m3(sb) * gs )
+    code  = e2m1 RNE-satfinite( f32(x / S) )  (all codes 0 when S == 0)
 
-Every decision compares a float32 input with a product of a midpoint of the
-target grid and the scale, (m * 6 * gs for the scale, m * S for a code).
-Those products have at most 31 significant bits, so they and the comparisons
-are exact in float64: the result is the exact rounding of the real quotient,
-with no division performed and no evaluation order to choose.
+Reading: the pages give the formula and float32 inputs but no precision or
+evaluation order; float32, left to right, with true divisions is the plain
+one.  The roundings onto the 8-bit and 4-bit grids are exact RNE of the
+float32 quotient (computed here in float64, where they are exact).
 
 A global scale outside [2^-100, 2^100] (or not finite) is invalid: codes
 and scale bytes are then 0.
@@ -122,46 +121,26 @@ def scale_valid(gs) -> bool:
     return GS_MIN <= g <= GS_MAX
 
 
-E4M3_GRID = None  # magnitudes of codes 0x00..0x7E, filled below
-E2M1_MIDPOINTS = (E2M1_MAGNITUDES[:-1] + E2M1_MAGNITUDES[1:]) * 0.5
-
-
-def _round_by_midpoints(a, scaled_mids):
-    """Index of the grid value nearest to a / t, given the midpoints of the
-    grid already multiplied by t (exact float64 products), ties to the even
-    index.  a >= 0.  Above the last midpoint the last index is returned
-    (saturation)."""
-    below = np.searchsorted(scaled_mids, a, side="left")  # midpoints strictly below a
-    on = (below < len(scaled_mids)) & (scaled_mids[np.minimum(below, len(scaled_mids) - 1)] == a)
-    return below + (on & (below % 2 == 1))  # a tie after an odd index moves up to the even one
-
-
 def choose_scale(amax, gs) -> np.ndarray:
-    """Scale byte sb = e4m3 nearest to amax / 6 / gs (RNE, saturating at 448).
-
-    amax: float32 block maxima (>= 0).  gs: valid float32 global scale.
-    Exact: amax is compared with midpoint * 6 * gs (exact in float64)."""
-    a = np.asarray(amax, dtype=np.float32).astype(np.float64)
-    mids = (E4M3_GRID[:-1] + E4M3_GRID[1:]) * 0.5
-    scaled = mids * 6.0 * np.float64(np.float32(gs))
-    return _round_by_midpoints(a, scaled).astype(np.uint8)
+    """Scale byte sb = e4m3 RNE-satfinite of f32(f32(amax / 6) / gs)."""
+    a = np.asarray(amax, dtype=np.float32)
+    with np.errstate(over="ignore"):
+        s_raw = (a / np.float32(6.0)).astype(np.float32) / np.float32(gs)  # IEEE float32 divisions
+    s_raw = np.minimum(s_raw.astype(np.float64), 1e4)  # anything above 464 saturates to 448
+    return e4m3_encode(s_raw)
 
 
 def encode_with_scale(x, sb, gs) -> np.ndarray:
     """Codes of float32 blocks x [..., nb, 16] given their scale bytes sb
-    [..., nb]: code = e2m1 nearest to x / S with S = e4m3(sb) * gs (RNE,
-    saturating at 6, sign of x kept); all 16 codes 0 when S == 0."""
-    x = np.asarray(x, dtype=np.float32).astype(np.float64)
-    S = e4m3_decode(sb) * np.float64(np.float32(gs))  # exact: <= 4 + 24 significant bits
-    a = np.abs(x)
-    code = np.zeros(x.shape, dtype=np.int64)
-    for k, m in enumerate(E2M1_MIDPOINTS):
-        t = m * S[..., None]  # exact: <= 3 + 28 significant bits
-        code += (a > t)
-        if k % 2 == 1:
-            code += (a == t)
-    code = np.where((S > 0)[..., None], code | (np.signbit(x).astype(np.int64) << 3), 0)
-    return code.astype(np.uint8)
+    [..., nb]: code = e2m1 RNE-satfinite of f32(x / S), S = f32(e4m3(sb) *
+    gs), sign of x kept; all 16 codes 0 when S == 0."""
+    x = np.asarray(x, dtype=np.float32)
+    S = (e4m3_decode(sb).astype(np.float32) * np.float32(gs)).astype(np.float32)
+    ok = S > 0
+    with np.errstate(over="ignore"):
+        q = (x / np.where(ok, S, np.float32(1.0))[..., None]).astype(np.float32)  # IEEE float32 division
+    codes = e2m1_encode(q.astype(np.float64))
+    return np.where(ok[..., None], codes, np.uint8(0)).astype(np.uint8)
 
 
 def quantize_blocks(x, gs):
@@ -208,5 +187,3 @@ def unpack_e2m1(packed) -> np.ndarray:
     out[..., 1::2] = p >> 4
     return out
 
-
-E4M3_GRID = e4m3_decode(np.arange(0x7F))  # 0, 2^-9, ..., 448 ascending

@@ -25,7 +25,7 @@ def test_library_exports_every_declared_symbol():
     for name in declared:
         assert hasattr(lib, name), name
     assert sorted(mla.abi_symbols()) == declared
-    assert lib.mla_nvfp4_abi_version() == 1
+    assert lib.mla_nvfp4_abi_version() == 2
 
 
 def test_status_strings():
@@ -73,18 +73,27 @@ def test_bad_sizes_rejected():
                                            p, p, None, None, None) == 1
 
 
-def test_decode_default_splits_and_launch_count():
-    # an explicit split count is returned as given; invalid sizes give 0; the
-    # default is at least 1; one split means one launch (no merge kernel)
+def test_decode_split_modes_launch_count_and_workspace():
+    # an explicit split count is returned as given, num_splits <= 0 reports
+    # 0 (planned on the device from the lengths), invalid sizes give -1
     assert mla.mla_nvfp4_decode_default_splits(4, 128, 5) == 5
-    assert mla.mla_nvfp4_decode_default_splits(0, 128, 0) == 0
-    assert mla.mla_nvfp4_decode_default_splits(4, 0, 0) == 0
-    d = mla.mla_nvfp4_decode_default_splits(64, 128, 0)
-    assert d >= 1
+    assert mla.mla_nvfp4_decode_default_splits(64, 128, 0) == 0
+    assert mla.mla_nvfp4_decode_default_splits(64, 128, -3) == 0
+    assert mla.mla_nvfp4_decode_default_splits(0, 128, 0) == -1
+    assert mla.mla_nvfp4_decode_default_splits(4, 0, 0) == -1
+    # launches: one split = the decode alone; uniform splits add the merge;
+    # the plan adds its planning kernel in front
     assert mla.decode_launches(64, 128, 1) == 1
     assert mla.decode_launches(64, 128, 3) == 2
-    # the workspace the default needs is the one its split count needs
-    assert mla.mla_nvfp4_decode_workspace_size(64, 128, 0) == mla.mla_nvfp4_decode_workspace_size(64, 128, d)
+    assert mla.decode_launches(64, 128, 0) == 3
+    # workspace: none for one split, rows for uniform splits, the plan's
+    # tables plus one chunk row per possible item (batch + 2 per SM pair)
+    lib = mla.load_library()
+    assert lib.mla_nvfp4_decode_workspace_size(64, 128, 1) == 0
+    assert lib.mla_nvfp4_decode_workspace_size(64, 128, 3) >= 64 * 3 * 128 * 2052
+    planned = lib.mla_nvfp4_decode_workspace_size(64, 128, 0)
+    items = 64 + 152  # 152 SMs assumed when no device is visible
+    assert items * 128 * 2052 <= planned <= items * 128 * 2052 + items * 8 + 64 * 8 + 2048
 
 
 def test_decode_host_pairs_checked_before_any_copy():

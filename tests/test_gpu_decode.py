@@ -138,3 +138,167 @@ def test_decode_host_buffers_match_device_call(mode, rb, with_lse):
     assert torch.equal(out_host, out_d.cpu())
     if with_lse:
         assert torch.equal(lse_host, lse_d.cpu())
+
+
+def _decode(w, gs, cache, err, **kw):
+    pk = dict(page_table=w.page_table.to(DEV), seq_lens=w.seq_lens.to(DEV)) if w.paged else \
+        dict(topk_indices=w.topk_indices.to(DEV))
+    return mla.mla_nvfp4_decode(w.q.to(DEV), cache, torch.tensor([gs], device=DEV), w.softmax_scale,
+                                error_word=err, return_lse=True, **pk, **kw)
+
+
+def _written_cache(w, gs):
+    cache = torch.zeros((w.num_slots, w.record_bytes), dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.mla_nvfp4_cache_write(w.kv_c.to(DEV), w.k_pe.to(DEV), w.slot_mapping.to(DEV), cache,
+                              torch.tensor([gs], device=DEV), err)
+    return cache, err
+
+
+@pytest.mark.parametrize("rb", [432, 368])
+def test_decode_planned_mixed_lengths(rb):
+    # the length-aware plan (num_splits = 0 with a workspace): empty
+    # sequences, one-key sequences, tile edges and long sequences in one
+    # batch, so that the plan cuts some sequences into several chunks (merged)
+    # and leaves others whole (written directly)
+    lens = (0, 1, 64, 65, 4000, 130, 0, 2500, 3, 1999, 64 * 37, 700)
+    w = workloads.decode_paged("planned", len(lens), 128, lens, rb, perm_pages=True, outlier_frac=0.01,
+                               outlier_mult=20.0, seed=31)
+    gs = oracle_gs(w.kv_c)
+    cache, err = _written_cache(w, gs)
+    out, lse = _decode(w, gs, cache, err, num_splits=0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    out, lse = f32(out), f32(lse)
+    assert np.all(out[[0, 6]] == 0) and np.all(np.isneginf(lse[[0, 6]]))
+    assert_attention_close(out, o_ref, f"decode planned rb={rb}", o_abs)
+    assert_lse_close(lse, l_ref, "decode planned lse")
+
+
+def test_decode_planned_workspace_room():
+    # a planned call given only room for its work list (no partial rows) cuts
+    # no sequence: one chunk each, written directly, the same bytes as one
+    # uniform split; given the full workspace it may split and still agrees
+    lens = (3000, 10, 5000, 64)
+    w = workloads.decode_paged("room", len(lens), 64, lens, 432, perm_pages=True, seed=32)
+    gs = oracle_gs(w.kv_c)
+    cache, err = _written_cache(w, gs)
+    # 64 KB: the header, the item list (batch + 2 per SM pair) and the chunk
+    # table fit, one chunk row (64 heads x 2052 bytes) does not
+    tables_only = torch.empty(65536, dtype=torch.uint8, device=DEV)
+    o_small, l_small = _decode(w, gs, cache, err, num_splits=0, workspace=tables_only)
+    o_one, l_one = _decode(w, gs, cache, err, num_splits=1)  # no workspace at all
+    o_full, l_full = _decode(w, gs, cache, err, num_splits=0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(o_small, o_one) and torch.equal(l_small, l_one)
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(f32(o_full), o_ref, "decode planned, full workspace", o_abs)
+    assert_lse_close(f32(l_full), l_ref, "decode planned lse, full workspace")
+
+
+def test_decode_uniform_splits_need_their_workspace():
+    w = workloads.decode_paged("ws", 2, 16, (300, 77), 432, perm_pages=True, seed=33)
+    gs = oracle_gs(w.kv_c)
+    cache, err = _written_cache(w, gs)
+    short = torch.empty(mla.mla_nvfp4_decode_workspace_size(2, 16, 3) - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(mla.MLAError) as ei:
+        _decode(w, gs, cache, err, num_splits=3, workspace=short)
+    assert ei.value.status == 5  # MLA_ERR_WORKSPACE
+
+
+def test_decode_one_split_many_rows_without_workspace():
+    # one split, batch x heads above the no-allocation scratch's row count:
+    # no workspace is needed or checked
+    lens = (5,) * 130
+    w = workloads.decode_paged("rows", len(lens), 128, lens, 432, perm_pages=True, seed=34)
+    gs = oracle_gs(w.kv_c)
+    cache, err = _written_cache(w, gs)
+    out, lse = _decode(w, gs, cache, err, num_splits=1)
+    torch.cuda.synchronize()
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(f32(out), o_ref, "decode 130 x 128 heads, one split", o_abs)
+    assert_lse_close(f32(lse), l_ref, "decode 130 x 128 heads lse")
+
+
+@pytest.mark.parametrize("peak,flagged", [(6.0e4, False), (7.0e4, True)])
+def test_decode_rope_range(peak, flagged):
+    # bf16 k_pe enters the tensor cores as f16: inside the f16 range it is
+    # exact (the result matches the oracle); beyond it saturates and the
+    # call flags MLA_DEVERR_RANGE
+    w = workloads.decode_paged("rope", 2, 32, (100, 70), 432, perm_pages=True, seed=35)
+    w.k_pe[7, 3] = peak
+    w.k_pe[120, 0] = -peak
+    w.q[:, :, 512:] *= 1e-4  # keeps the scores of those keys moderate
+    gs = oracle_gs(w.kv_c)
+    cache, err = _written_cache(w, gs)
+    out, lse = _decode(w, gs, cache, err, num_splits=1)
+    torch.cuda.synchronize()
+    assert bool(int(err.item()) & mla.DEVERR_RANGE) == flagged
+    if not flagged:
+        o_ref, l_ref, o_abs = run_oracle(w, gs)
+        assert_attention_close(f32(out), o_ref, "decode rope near the f16 limit", o_abs)
+        assert_lse_close(f32(lse), l_ref, "decode rope near the f16 limit lse")
+    else:
+        assert torch.isfinite(out.float()).all()
+
+
+def _plan_choice(tiles, pairs, max_items, max_rows, overhead=2.0):
+    """The chunk size the plan documents: among C = ceil(tmax / k), k = 1..32,
+    the first minimum of max(ceil(full / P) * (C + o), (tiles + o * items) /
+    P + (mean last chunk + o) / 2) over the candidates whose items and
+    partial rows fit."""
+    tmax, tot = max(tiles), sum(tiles)
+    best, best_est = None, math.inf
+    for k in range(1, 33):
+        C = max(1, -(-tmax // k))
+        nb = [max(1, -(-t // C)) for t in tiles]
+        n, full = sum(nb), sum(t // C for t in tiles)
+        rows = sum(x for x in nb if x > 1)
+        last = sum(1 for t in tiles if t == 0 or t % C)
+        waves = math.ceil(full / pairs) * (C + overhead)
+        avg = (tot + overhead * n) / pairs + (0.5 * ((tot - full * C) / last + overhead) if last else 0.0)
+        est = max(waves, avg) if (n <= max_items and rows <= max_rows) else math.inf
+        if est < best_est * (1 - 1e-6):  # float32 on the device: a near tie keeps the larger C
+            best, best_est = C, est
+    return best
+
+
+@pytest.mark.parametrize("lens", [(4096,) * 64, (0, 1, 64, 65, 4000, 130, 0, 2500, 3, 1999, 2368, 700),
+                                  (32768, 1024, 1500, 20000, 5000, 8000, 1100)])
+def test_decode_plan_covers_every_chunk_once(lens):
+    w = workloads.decode_paged("plan", len(lens), 16, lens, 432, perm_pages=True, seed=36)
+    gs = oracle_gs(w.kv_c)
+    cache, err = _written_cache(w, gs)
+    B = len(lens)
+    ws = torch.zeros(mla.mla_nvfp4_decode_workspace_size(B, 16, 0), dtype=torch.uint8, device=DEV)
+    _decode(w, gs, cache, err, num_splits=0, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    raw = ws.cpu().numpy()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs, max_items = sms // 2, B + 2 * (sms // 2)
+    n_items, C = (int(x) for x in raw[:8].view(np.int32))
+    items = raw[256:256 + 8 * n_items].view(np.int32).reshape(-1, 2)
+    seq_off = (256 + 8 * max_items + 255) // 256 * 256
+    seqs = raw[seq_off:seq_off + 8 * B].view(np.int32).reshape(-1, 2)
+    tiles = [-(-L // 64) for L in lens]
+    assert C == _plan_choice(tiles, pairs, max_items, max_items)
+    nb = [max(1, -(-t // C)) for t in tiles]
+    # every (sequence, chunk) exactly once
+    assert sorted(map(tuple, items.tolist())) == sorted((b, c) for b in range(B) for c in range(nb[b]))
+    # the chunk table: one-chunk sequences are direct, the others own
+    # consecutive, disjoint partial rows
+    assert seqs[:, 1].tolist() == nb
+    rows = [(int(seqs[b, 0]), nb[b]) for b in range(B) if nb[b] > 1]
+    assert all(seqs[b, 0] == -1 for b in range(B) if nb[b] == 1)
+    used = sorted(r for base, n in rows for r in range(base, base + n))
+    assert used == list(range(len(used)))
+    # longest first: full chunks, then the last chunks by non-increasing
+    # size bucket (64 buckets over [0, C))
+    size = [min(C, tiles[b] - c * C) for b, c in items.tolist()]
+    n_full = sum(t // C for t in tiles)
+    assert all(s_ == C for s_ in size[:n_full])
+    buckets = [63 - s_ * 64 // C for s_ in size[n_full:]]
+    assert buckets == sorted(buckets)

@@ -11,12 +11,21 @@ import torch
 
 import mla_attention_nvfp4_gb300 as mla
 from mla_attention_nvfp4_gb300 import workloads
-from oracle import attention, swizzle
+from oracle import attention, nvfp4, swizzle
 from tests.helpers import assert_lse_close, check_fused_blocks, check_fused_output, f32, oracle_gs
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
 DEV = "cuda:0"
+# Codes and scale bytes of the fused output that differ from the oracle's
+# quantisation of the exact attention output, as a fraction of the codes (a
+# scale byte counts 17).  Each one is checked to lie at a rounding boundary
+# within the kernel's attention error (the bf16 rounding of P moves every
+# output by up to 2^-9 of softmax @ |v|), so their rate follows from that
+# error, not from the quantiser: the quantiser itself, given identical fp32
+# inputs, is held to 1e-4 (test_gpu_quant: quantize_rows).  Measured: 1.2e-2
+# on 1..200-token sequences, where P is large and its rounding error with it.
+FUSED_FLIP_RATE = 2e-2
 
 
 def _run(w, gs):
@@ -41,7 +50,8 @@ def test_prefill_small(lens, heads):
                                              w.softmax_scale, with_abs=True)
     T = w.total_tokens
     o2 = o_ref.reshape(T, heads * 128)
-    n_sf, n_codes = check_fused_output(codes, sf, o2, o_abs.reshape(T, heads * 128), gs)
+    counts = check_fused_output(codes, sf, o2, o_abs.reshape(T, heads * 128), gs, f"prefill {lens} H{heads}")
+    assert counts["rate"] <= FUSED_FLIP_RATE, counts
     deq = swizzle.dequantize_rows(codes, sf, T, heads * 128, gs)
     ref_deq = swizzle.dequantize_rows(*swizzle.quantize_rows(o2.astype(np.float32), gs), T, heads * 128, gs)
     # codes agree up to boundary flips (checked above), so the dequantised
@@ -76,7 +86,7 @@ def test_prefill_full_size_sampled():
     """8 sequences x 4096 tokens x 128 heads (the benchmark's prefill): sampled
     rows of three heads against the oracle, one row at a time."""
     w = workloads.prefill_8x4096(device=DEV)
-    gs = oracle_gs(w.v[:4096, :8].cpu())
+    gs = nvfp4.global_scale(float(w.v.abs().max()))  # the whole tensor's amax, as the benchmark uses
     gst = torch.tensor([gs], device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     codes, sf, lse = mla.mla_nvfp4_prefill_fused_out(w.q, w.k, w.v, w.cu_seqlens, w.max_seqlen, w.softmax_scale,
@@ -102,7 +112,8 @@ def test_prefill_full_size_sampled():
         c_rows = codes[rows][:, h * 64:(h + 1) * 64].cpu().numpy()
         m, kk = np.meshgrid(np.array(rows), np.arange(h * 8, h * 8 + 8), indexing="ij")
         sf_rows = sf_np[swizzle.sf_offset(m, kk, H * 8)]
-        check_fused_blocks(c_rows, sf_rows, o_ref, o_abs, gs)
+        counts = check_fused_blocks(c_rows, sf_rows, o_ref, o_abs, gs, f"prefill 8x4096 head {h} sampled rows")
+        assert counts["rate"] <= FUSED_FLIP_RATE, counts
         assert_lse_close(f32(lse[h, rows]), l_ref, f"prefill lse head {h}")
 
 
@@ -153,5 +164,7 @@ def test_prefill_random_mixes(seed):
     o_ref, l_ref, o_abs = attention.prefill(f32(w.q), f32(w.k), f32(w.v), w.cu_seqlens.numpy(),
                                              w.softmax_scale, with_abs=True)
     T = w.total_tokens
-    check_fused_output(codes, sf, o_ref.reshape(T, heads * 128), o_abs.reshape(T, heads * 128), gs)
+    counts = check_fused_output(codes, sf, o_ref.reshape(T, heads * 128), o_abs.reshape(T, heads * 128), gs,
+                                f"prefill mix {lens} H{heads}")
+    assert counts["rate"] <= FUSED_FLIP_RATE, counts
     assert_lse_close(lse, l_ref, f"prefill lse mix {lens} H{heads}")

@@ -1,15 +1,19 @@
 """GPU parity of the elementwise NVFP4 kernels against the oracle: the
 quantise-rows hook (the prefill epilogue's quantiser), the cache write and
-the global scale.  Bit-exact: both sides take every rounding decision in
-float32 in the same order."""
+the global scale.  The oracle takes the exact NVFP4 decisions; the kernels
+evaluate the quotients in float32, so a code or scale byte may differ only
+where the exact quotient lies within that float32 error of a rounding
+midpoint, and such flips are counted against a budget of 1e-4 of the codes
+(tests.helpers.quant_flips).  Everything else (RoPE bytes, padding, skipped
+slots, the global scale) is bit-exact."""
 import numpy as np
 import pytest
 import torch
 
 import mla_attention_nvfp4_gb300 as mla
 from mla_attention_nvfp4_gb300 import workloads
-from oracle import cache as ocache, nvfp4, swizzle
-from tests.helpers import f32, oracle_cache, oracle_gs
+from oracle import nvfp4, swizzle
+from tests.helpers import f32, oracle_gs, quant_flips, record_flips
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
@@ -32,16 +36,22 @@ def _edge_matrix(M, N, seed):
 
 
 @pytest.mark.parametrize("M,N,gs", [(1, 16, 1.0), (130, 48, 1.0), (256, 1024, 0.37), (300, 8192, 0.002)])
-def test_quantize_rows_bit_exact(M, N, gs):
+def test_quantize_rows_matches_definition(M, N, gs):
     x = _edge_matrix(M, N, seed=M + N)
     g = np.float32(gs)
-    codes_ref, sf_ref = swizzle.quantize_rows(x, g)
     xt = torch.from_numpy(x).to(DEV)
     gst = torch.tensor([g], dtype=torch.float32, device=DEV)
     codes, sf = mla.mla_nvfp4_quantize_rows(xt, gst)
     torch.cuda.synchronize()
-    assert np.array_equal(codes.cpu().numpy(), codes_ref)
-    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+    codes, sf = codes.cpu().numpy(), sf.cpu().numpy()
+    assert sf.size == swizzle.sf_buffer_bytes(M, N // 16)
+    quant_flips(x, g, nvfp4.unpack_e2m1(codes), swizzle.unswizzle_scales(sf, M, N // 16),
+                f"quantize_rows {M}x{N} gs={gs}")
+    # padding rows and columns of the swizzled buffer are zero
+    pad = np.ones(sf.size, dtype=bool)
+    m, k = np.meshgrid(np.arange(M), np.arange(N // 16), indexing="ij")
+    pad[swizzle.sf_offset(m, k, N // 16)] = False
+    assert np.all(sf[pad] == 0)
 
 
 def test_quantize_rows_scale_guard():
@@ -54,17 +64,21 @@ def test_quantize_rows_scale_guard():
 
 
 @pytest.mark.parametrize("rb", [432, 368])
-def test_cache_write_tiny_bit_exact(rb):
+def test_cache_write_tiny(rb):
     w = workloads.decode_tiny(record_bytes=rb)
     gs = oracle_gs(w.kv_c)
-    ref = oracle_cache(w, gs)
     cache = torch.zeros((w.num_slots, rb), dtype=torch.uint8, device=DEV)
     gst = torch.tensor([gs], device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     mla.mla_nvfp4_cache_write(w.kv_c.to(DEV), w.k_pe.to(DEV), w.slot_mapping.to(DEV), cache, gst, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert np.array_equal(cache.cpu().numpy(), ref)
+    c = cache.cpu().numpy()
+    slots = w.slot_mapping.numpy()
+    record_flips(c[slots], f32(w.kv_c), f32(w.k_pe), gs, rb, f"cache write tiny {rb}")
+    untouched = np.ones(w.num_slots, dtype=bool)
+    untouched[slots] = False
+    assert np.all(c[untouched] == 0)
 
 
 @pytest.mark.parametrize("rb", [432, 368])
@@ -81,17 +95,20 @@ def test_cache_write_ragged_skip_and_bounds(rb):
     slots[3] = -1
     slots[5] = S + 10  # out of range: skipped and flagged
     gs = oracle_gs(kv)
-    ref = np.full((S, rb), 0xEE, dtype=np.uint8)
-    keep = slots.numpy().copy()
-    keep[5] = -1
-    ocache.write_cache(ref, f32(kv), f32(pe), keep, gs, rb)
     cache = torch.full((S, rb), 0xEE, dtype=torch.uint8, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     mla.mla_nvfp4_cache_write(kv.to(DEV), pe.to(DEV), slots.to(DEV), cache,
                               torch.tensor([gs], device=DEV), err)
     torch.cuda.synchronize()
     assert int(err.item()) == mla.DEVERR_BOUNDS
-    assert np.array_equal(cache.cpu().numpy(), ref)
+    c = cache.cpu().numpy()
+    keep = slots.numpy().copy()
+    keep[5] = -1
+    written = keep >= 0
+    record_flips(c[keep[written]], f32(kv)[written], f32(pe)[written], gs, rb, f"cache write ragged {rb}")
+    untouched = np.ones(S, dtype=bool)
+    untouched[keep[written]] = False
+    assert np.all(c[untouched] == 0xEE)  # skipped and out-of-range tokens wrote nothing
 
 
 def test_global_scale_exact():
@@ -105,7 +122,7 @@ def test_global_scale_exact():
 
 
 @pytest.mark.parametrize("rb", [432, 368])
-def test_cache_write_many_tokens_per_warp_bit_exact(rb):
+def test_cache_write_many_tokens_per_warp(rb):
     # 50,003 tokens: the grid is one wave of resident blocks, so every warp
     # loops over about ten tokens (two per iteration, ragged last iteration);
     # records land in a permuted slot order
@@ -115,11 +132,10 @@ def test_cache_write_many_tokens_per_warp_bit_exact(rb):
     pe = torch.from_numpy(rng.standard_normal((T, 64)).astype(np.float32)).to(torch.bfloat16)
     slots = torch.from_numpy(rng.permutation(T).astype(np.int64))
     gs = oracle_gs(kv)
-    ref = np.zeros((T, rb), dtype=np.uint8)
-    ocache.write_cache(ref, f32(kv), f32(pe), slots.numpy(), gs, rb)
     cache = torch.zeros((T, rb), dtype=torch.uint8, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     mla.mla_nvfp4_cache_write(kv.to(DEV), pe.to(DEV), slots.to(DEV), cache, torch.tensor([gs], device=DEV), err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert np.array_equal(cache.cpu().numpy(), ref)
+    c = cache.cpu().numpy()
+    record_flips(c[slots.numpy()], f32(kv), f32(pe), gs, rb, f"cache write 50003 tokens {rb}")

@@ -151,28 +151,32 @@ def _nearest_even_argmin(d):
 
 
 def _brute_force_quantize(x, gs):
-    """Nearest e4m3 scale to amax/6/gs, then nearest e2m1 magnitude to
-    |x|/S, both by exhaustive search over the grid (ties to the even code).
-    Distances are taken as |amax - 6*gs*g| and ||x| - g*S|: the products are
-    exact in float64 and so are the differences for the two grid points
-    around the value, which are the only ones a tie can involve."""
-    gs = np.float64(np.float32(gs))
-    blocks = np.asarray(x, dtype=np.float32).astype(np.float64).reshape(-1, 16)
-    amax = np.abs(blocks).max(axis=1)
+    """The float32 quotients from torch's float32 division, then the nearest
+    e4m3 scale and the nearest e2m1 magnitude by exhaustive search over the
+    grid (ties to the even code).  Distances are exact in float64: a float32
+    quotient and a grid value (at most 4 significant bits) differ by a value
+    float64 holds."""
+    g32 = torch.tensor(np.float32(gs))
+    blocks = torch.from_numpy(np.asarray(x, dtype=np.float32).reshape(-1, 16))
+    amax = blocks.abs().amax(dim=1)
+    s32 = ((amax / 6.0) / g32).double().clamp(max=1e4).numpy()
     grid = nvfp4.e4m3_decode(np.arange(0x7F))
-    sb = _nearest_even_argmin(np.abs(amax[:, None] - 6.0 * gs * grid[None, :]))
-    S = grid[sb] * gs
+    sb = _nearest_even_argmin(np.abs(s32[:, None] - grid[None, :]))
+    S32 = (torch.from_numpy(grid[sb]).float() * g32).float()
+    ok = (S32 > 0).numpy()
+    q32 = (blocks / torch.where(S32 > 0, S32, torch.ones_like(S32))[:, None]).double().abs().numpy()
     mags = nvfp4.E2M1_MAGNITUDES
-    d = np.abs(np.abs(blocks)[..., None] - mags[None, None, :] * S[:, None, None])
-    mag = _nearest_even_argmin(d)
-    codes = np.where(S[:, None] > 0, mag | (np.signbit(blocks).astype(np.int64) << 3), 0)
+    mag = _nearest_even_argmin(np.abs(q32[..., None] - mags[None, None, :]))
+    codes = np.where(ok[:, None], mag | (np.signbit(blocks.numpy()).astype(np.int64) << 3), 0)
     return codes.astype(np.uint8).reshape(np.shape(x)), sb.astype(np.uint8)
 
 
 def _tie_blocks(rng, n, gs):
-    """Blocks whose scale or codes sit exactly on a rounding midpoint.  gs has
-    at most 16 significant bits, so 6*gs*midpoint (scale ties) and
-    e2m1-midpoint*e4m3*gs (code ties) are float32 values."""
+    """Blocks whose float32 quotients sit exactly on a rounding midpoint.  gs
+    has at most 16 significant bits, so 6*gs*midpoint (scale ties, whose
+    quotient (amax/6)/gs is then the midpoint exactly) and
+    e2m1-midpoint*e4m3*gs (code ties, with S = e4m3*gs exact) are float32
+    values."""
     grid = nvfp4.e4m3_decode(np.arange(0x7F))
     mids = (grid[:-1] + grid[1:]) / 2
     out = np.zeros((2 * n, 16), dtype=np.float32)
@@ -278,3 +282,64 @@ def test_tie_flip_rule_accepts_float32_kernels_and_rejects_errors():
     bad[row, col] = (bad[row, col] & 8) | (m + 1 if m < 7 else 6)
     with pytest.raises(AssertionError):
         quant_flips(x, g, bad, sb.reshape(x.shape[0], 4), "planted error", budget=1.0)
+
+
+def _fma32(a, b, c):
+    """float32 fma: a * b + c exactly, rounded once to float32.  The product
+    is exact in float64; the sum is carried as float64 plus its exact error
+    (two-sum), which decides a float32 rounding that float64 left halfway."""
+    a, b, c = (np.asarray(v, dtype=np.float32).astype(np.float64) for v in (a, b, c))
+    p = a * b
+    s_ = p + c
+    bb = s_ - p
+    err = (p - (s_ - bb)) + (c - bb)
+    r = s_.astype(np.float32)
+    lo = np.nextafter(r, np.float32(-np.inf))
+    hi = np.nextafter(r, np.float32(np.inf))
+    down = (s_ == (r.astype(np.float64) + lo.astype(np.float64)) / 2) & (err < 0)
+    up = (s_ == (r.astype(np.float64) + hi.astype(np.float64)) / 2) & (err > 0)
+    return np.where(down, lo, np.where(up, hi, r)).astype(np.float32)
+
+
+def _div_rn_model(a, b, y):
+    """The kernels' correctly rounded division: q0 = a * y, then
+    q0 + (a - q0 * b) * y, both corrections as float32 fmas."""
+    a = np.asarray(a, dtype=np.float32)
+    q0 = (a * y).astype(np.float32)
+    return _fma32(_fma32(-q0, b, a), y, q0)
+
+
+def _cache_write_model(x, gs):
+    """A float32 model of the cache write's quantiser: every division from a
+    correctly rounded reciprocal plus two fmas."""
+    x = np.asarray(x, dtype=np.float32).reshape(-1, 16)
+    g = np.float32(gs)
+    amax = np.abs(x).max(1)
+    q6 = _div_rn_model(amax, np.float32(6), np.float32(1) / np.float32(6))
+    s_raw = _div_rn_model(q6, g, np.float32(1) / g)
+    sb = nvfp4.e4m3_encode(np.minimum(s_raw.astype(np.float64), 1e4))
+    S = (nvfp4.e4m3_decode(sb).astype(np.float32) * g).astype(np.float32)
+    R = (np.float32(1) / np.where(S > 0, S, np.float32(1))).astype(np.float32)
+    q = _div_rn_model(x, S[:, None], R[:, None])
+    codes = np.where((S > 0)[:, None], nvfp4.e2m1_encode(q.astype(np.float64)), 0)
+    return codes.astype(np.uint8), sb.astype(np.uint8)
+
+
+@pytest.mark.parametrize("gs", [0.37, 1.0, 4.5e-3])
+def test_correctly_rounded_division_reproduces_the_definition(gs):
+    # bf16 latents with the global scale of their own amax (whose thresholds
+    # sit within 2^-24 of bf16 values at a rate of ~1e-3), exact tie blocks
+    # and random floats: the fma-corrected reciprocal gives the definition's
+    # float32 quotients exactly, the plain reciprocal does not
+    rng = np.random.default_rng(40)
+    bf = torch.from_numpy(rng.standard_normal(400_000).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    g_bf = nvfp4.global_scale(np.abs(bf).max())
+    g_tie = _f32_16bit(gs)
+    cases = [(bf.reshape(-1, 16), g_bf), (_tie_blocks(rng, 5000, g_tie), g_tie),
+             ((rng.standard_normal((50_000, 16)) * np.exp2(rng.uniform(-10, 10, (50_000, 1)))).astype(np.float32),
+              np.float32(gs))]
+    for x, g in cases:
+        codes, sb = nvfp4.quantize_blocks(x, g)
+        mc, msb = _cache_write_model(x, g)
+        assert np.array_equal(msb, sb.reshape(-1))
+        assert np.array_equal(mc, codes.reshape(-1, 16))
