@@ -398,7 +398,7 @@ def run_ours(args, rank, world):
                                 dtype=mla.operand_dtype("decode"), kernel=None),
         })
         launches += mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(wm.batch, wm.heads, 0) + \
-            mla.decode_launches(wt.batch, wt.heads, 0)
+            mla.decode_launches(wt.batch, wt.heads, 0, paged=False)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     barrier = (lambda: torch.distributed.barrier()) if world > 1 else None
     with ClockSampler(dev.index) as clk:

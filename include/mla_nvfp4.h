@@ -109,9 +109,10 @@ int mla_nvfp4_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_p
 /*
  * Bytes of decode workspace mla_nvfp4_decode needs for (batch, num_heads,
  * num_splits) on the current device:
- *   num_splits <= 0 : the length-aware plan (see mla_nvfp4_decode): a small
- *                     header and work list plus room for the split partials
- *                     of batch + SMs items, each num_heads x 2052 bytes;
+ *   num_splits <= 0 : paged mode's length-aware plan (see mla_nvfp4_decode):
+ *                     a small header and work list plus room for the split
+ *                     partials of batch + SMs/2 items, each num_heads x 2052
+ *                     bytes (enough for top-k mode's default splits too);
  *   num_splits == 1 : 0 (one split per sequence needs no workspace);
  *   num_splits > 1  : batch * num_splits * num_heads * 2048 bytes of partial
  *                     outputs plus their LSE (256-byte rounded).
@@ -120,11 +121,12 @@ int mla_nvfp4_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_p
 size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits);
 
 /*
- * How mla_nvfp4_decode splits the keys for a given num_splits: the value
- * itself when > 0 (every sequence cut into that many equal ranges of key
- * tiles), 0 when the split is planned on the device per call from the
- * sequence lengths (num_splits <= 0), -1 for invalid sizes.  Launches per
- * call: one with one split, two (decode, merge) with uniform splits > 1,
+ * The number of equal key splits mla_nvfp4_decode uses for (batch,
+ * num_heads) on the current device: num_splits itself when > 0, else the
+ * default that fills the SMs, which top-k calls and paged calls without a
+ * workspace use (paged calls with a workspace and num_splits <= 0 are
+ * planned from the lengths instead).  Returns 0 for invalid sizes.
+ * Launches per call: one with one split, two (decode, merge) with more,
  * three (plan, decode, merge) when planned.
  */
 int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits);
@@ -153,13 +155,15 @@ int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits);
  *                  lse = -inf.
  *   num_splits   : > 0: every sequence's key tiles (64 keys each) are cut
  *                  into num_splits equal ranges, one CTA pair each, merged
- *                  by LSE.  <= 0 with a workspace: length-aware plan, made
- *                  on the device from the lengths: every sequence is cut
- *                  into chunks of C tiles (C chosen per call from the tile
+ *                  by LSE.  <= 0 in top-k mode: as many equal splits as
+ *                  fill the SMs (all rows have topk entries).  <= 0 in paged
+ *                  mode with a workspace: length-aware plan, made on the
+ *                  device from the lengths: every sequence is cut into
+ *                  chunks of C tiles (C chosen per call from the tile
  *                  counts, the SM count and the workspace room), the CTA
  *                  pairs take the chunks longest first, and sequences with
- *                  one chunk are written directly.  <= 0 without a
- *                  workspace (NULL): one split per sequence.
+ *                  one chunk are written directly.  <= 0 in paged mode
+ *                  without a workspace (NULL): one split per sequence.
  *   workspace    : >= mla_nvfp4_decode_workspace_size(batch, num_heads,
  *                  num_splits) bytes, 256-byte aligned, contents ignored;
  *                  may be NULL for one split.  A planned call given less

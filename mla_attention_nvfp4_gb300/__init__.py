@@ -187,18 +187,20 @@ def mla_nvfp4_decode_workspace_size(batch: int, num_heads: int, num_splits: int 
 
 
 def mla_nvfp4_decode_default_splits(batch: int, num_heads: int, num_splits: int = 0) -> int:
-    """Uniform key splits a decode of (batch, num_heads) uses: num_splits
-    when > 0, 0 when the split is planned on the device from the lengths,
-    -1 for invalid sizes."""
+    """Equal key splits a decode of (batch, num_heads) uses: num_splits when
+    > 0, else the library default on the current device (top-k calls, and
+    paged calls without a workspace; paged calls with one are planned)."""
     return int(load_library().mla_nvfp4_decode_default_splits(batch, num_heads, num_splits))
 
 
-def decode_launches(batch: int, num_heads: int, num_splits: int = 0) -> int:
-    """Kernels one mla_nvfp4_decode call (with a workspace) launches: the
-    decode alone with one split, plus the merge with uniform splits, plus
-    the planning kernel when planned."""
-    s = mla_nvfp4_decode_default_splits(batch, num_heads, num_splits)
-    return 3 if s == 0 else (1 if s == 1 else 2)
+def decode_launches(batch: int, num_heads: int, num_splits: int = 0, *, paged: bool = True,
+                    workspace: bool = True) -> int:
+    """Kernels one mla_nvfp4_decode call launches: plan, decode and merge
+    when planned (paged, num_splits <= 0, a workspace); otherwise the decode,
+    plus the merge with more than one split."""
+    if paged and num_splits <= 0 and workspace:
+        return 3
+    return 1 if mla_nvfp4_decode_default_splits(batch, num_heads, num_splits) == 1 else 2
 
 
 def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, seq_lens=None,

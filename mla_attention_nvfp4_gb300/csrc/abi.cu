@@ -119,8 +119,10 @@ size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits)
 }
 
 int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits) {
-  if (batch < 1 || num_heads < 1) return -1;
-  return num_splits > 0 ? num_splits : 0;
+  if (batch < 1 || num_heads < 1) return 0;
+  if (num_splits > 0) return num_splits;
+  const int sms = device_sms();
+  return mla::decode_default_splits(batch, num_heads, sms > 0 ? sms : 152);
 }
 
 }  // extern "C"
@@ -156,8 +158,12 @@ int decode_prepare(const void* q, int batch, int num_heads, const uint8_t* cache
   const int sms = device_sms();
   if (sms < 0) return -sms;
   if (num_splits > 4096) return MLA_ERR_INVALID_ARG;
-  // num_splits <= 0 with a workspace: the length-aware plan; without one,
-  // one split per sequence.  One split needs no workspace.
+  // num_splits <= 0: in top-k mode every row has the same number of index
+  // entries, so the split count follows from the sizes alone (enough splits
+  // to fill the SMs); in paged mode, with a workspace, the length-aware
+  // plan, and without one, one split per sequence.  One split needs no
+  // workspace.
+  if (num_splits <= 0 && sparse) num_splits = mla::decode_default_splits(batch, num_heads, sms);
   const bool planned = num_splits <= 0 && workspace != nullptr;
   if (num_splits <= 0 && !planned) num_splits = 1;
   if (planned || num_splits > 1) {

@@ -1111,7 +1111,12 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 DecodePlanLayout decode_plan_layout(int batch, int num_heads, int num_sms, size_t bytes) {
   DecodePlanLayout l;
   l.pairs = num_sms / 2;
-  l.max_items = batch + 2 * l.pairs;
+  // Items beyond one per sequence: one per resident CTA pair.  On the
+  // log-uniform 1k..32k-token batch this balances as well as two per pair
+  // (simulated makespan 239 against 240 tiles, lower bound 217), while each
+  // slot the plan leaves unused is a CTA pair that still has to be launched
+  // (~0.07 us each on GB300, measured).
+  l.max_items = batch + l.pairs;
   l.items = 256;
   l.seqs = align256(l.items + static_cast<size_t>(l.max_items) * sizeof(int2));
   l.rows = align256(l.seqs + static_cast<size_t>(batch) * sizeof(int2));

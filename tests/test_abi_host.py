@@ -74,25 +74,27 @@ def test_bad_sizes_rejected():
 
 
 def test_decode_split_modes_launch_count_and_workspace():
-    # an explicit split count is returned as given, num_splits <= 0 reports
-    # 0 (planned on the device from the lengths), invalid sizes give -1
+    # an explicit split count is returned as given, num_splits <= 0 gives
+    # the default that fills the SMs (at least 1), invalid sizes give 0
     assert mla.mla_nvfp4_decode_default_splits(4, 128, 5) == 5
-    assert mla.mla_nvfp4_decode_default_splits(64, 128, 0) == 0
-    assert mla.mla_nvfp4_decode_default_splits(64, 128, -3) == 0
-    assert mla.mla_nvfp4_decode_default_splits(0, 128, 0) == -1
-    assert mla.mla_nvfp4_decode_default_splits(4, 0, 0) == -1
+    assert mla.mla_nvfp4_decode_default_splits(64, 128, 0) >= 1
+    assert mla.mla_nvfp4_decode_default_splits(2, 128, 0) > 1
+    assert mla.mla_nvfp4_decode_default_splits(0, 128, 0) == 0
+    assert mla.mla_nvfp4_decode_default_splits(4, 0, 0) == 0
     # launches: one split = the decode alone; uniform splits add the merge;
-    # the plan adds its planning kernel in front
+    # a planned call (paged, num_splits <= 0, a workspace) adds the plan
     assert mla.decode_launches(64, 128, 1) == 1
     assert mla.decode_launches(64, 128, 3) == 2
     assert mla.decode_launches(64, 128, 0) == 3
+    assert mla.decode_launches(2, 128, 0, paged=False) == 2
+    assert mla.decode_launches(2, 128, 0, workspace=False) == 2
     # workspace: none for one split, rows for uniform splits, the plan's
-    # tables plus one chunk row per possible item (batch + 2 per SM pair)
+    # tables plus one chunk row per possible item (batch + one per SM pair)
     lib = mla.load_library()
     assert lib.mla_nvfp4_decode_workspace_size(64, 128, 1) == 0
     assert lib.mla_nvfp4_decode_workspace_size(64, 128, 3) >= 64 * 3 * 128 * 2052
     planned = lib.mla_nvfp4_decode_workspace_size(64, 128, 0)
-    items = 64 + 152  # 152 SMs assumed when no device is visible
+    items = 64 + 76  # batch + one per SM pair (152 SMs assumed when no device is visible)
     assert items * 128 * 2052 <= planned <= items * 128 * 2052 + items * 8 + 64 * 8 + 2048
 
 
