@@ -14,7 +14,10 @@ every workload the path is specified on:
   5. decode of the mixed-length batch (128 sequences, lengths log-uniform
      1k..32k, 128 heads, 368-byte records);
   6. sparse top-k decode (32 queries x 128 heads, 2048 of 65,536 context
-     tokens each, a few -1 entries).
+     tokens each, a few -1 entries);
+  7. the NVFP4 output projection on the prefill's fused output as written
+     (32,768 tokens x 16,384 = 128 heads x 128, against a 7168-row NVFP4
+     weight), on block-scaled fp4 tensor cores.
 Legs are timed with CUDA events on the launching stream; L2 is flushed (a
 256 MB write) before every leg.  `value` is the DeepSeek-V3-shaped decode
 leg's algorithmic HBM throughput (the metric's first part); every leg's
@@ -46,10 +49,14 @@ UNIT = "GB/s"
 WORKLOAD = ("decode_dsv3: B64 H128 L4096 paged 432B NVFP4 cache (cache write of its 262144 tokens + "
             "planned split-K decode) + prefill_8x4096: causal varlen H128 qk192 v128 fused NVFP4 out + "
             "decode_mixed: B128 H128 L~logU(1k,32k) 368B fp8-RoPE records (cache write + decode) + "
-            "decode_topk: B32 H128 2048 of 65536 tokens, 432B")
+            "decode_topk: B32 H128 2048 of 65536 tokens, 432B + gemm_oproj: NVFP4 [32768 x 16384] x [7168 x 16384]^T "
+            "on the prefill output")
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SM_COUNT, SM_MAX_MHZ, FP32_LANES = 152, 2070.0, 128
+# Dense tensor-core rate of fp4 (block-scaled e2m1) over bf16: 13.5 / 2.25
+# PFLOP/s nominal; the fp4 roofline is the measured bf16 peak times this.
+FP4_OVER_BF16 = 6.0
 CLOCK_SAMPLE_MS = 50
 
 
@@ -303,9 +310,13 @@ def summarize(leg_ms, meta, world, peaks, peak_src, headline="decode_dsv3"):
                 leg["dram_gbs"] = traffic / (ms * 1e-3) / 1e9
                 leg["dram_frac"] = leg["dram_gbs"] / hbm
         else:
-            roof = {"bound": "tensor", "achieved": tflops / world, "peak": bf16, "unit": "TFLOP/s"}
+            x = m.get("peak_x", 1.0)
+            roof = {"bound": "tensor", "achieved": tflops / world, "peak": bf16 * x, "unit": "TFLOP/s"}
+            if x != 1.0:
+                leg["tensor_frac"] = tflops / world / (bf16 * x)
         roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["peak_source"] = peak_src
+        roof["peak_source"] = peak_src if m.get("peak_x", 1.0) == 1.0 else \
+            f"{peak_src} bf16 x {m['peak_x']:g} (nominal fp4 / bf16 dense ratio)"
         roof["traffic"] = traffic
         leg["roofline"] = roof
         legs[name] = leg
@@ -374,6 +385,22 @@ def run_ours(args, rank, world):
                                         out_codes=codes, out_scales=scales, error_word=err)
 
     legs = [("cache_write_432", cache_write(ds)), ("decode_dsv3", decode(ds)), ("prefill", leg_prefill)]
+    # output projection weight: random NVFP4 [7168, H*128] (codes and
+    # scales in a moderate range), and the GEMM's bf16 output
+    n_out, k_in = 7168, p.heads * 128
+    gw = torch.Generator(device=dev)
+    gw.manual_seed(7)
+    w_codes = torch.randint(0, 256, (n_out, k_in // 2), dtype=torch.uint8, device=dev, generator=gw)
+    w_sf = torch.randint(0x28, 0x48, (n_out * k_in // 16,), dtype=torch.uint8, device=dev, generator=gw)
+    gs_w = torch.tensor([1.0 / 4096], device=dev)
+    o_proj = torch.empty((p.total_tokens, n_out), dtype=torch.bfloat16, device=dev)
+
+    def leg_gemm():
+        mla.mla_nvfp4_gemm(codes, scales, w_codes, w_sf, gsp, gs_w, out=o_proj)
+
+    with_gemm = args.case != "decode-steady"
+    if with_gemm:
+        legs.append(("gemm_oproj", leg_gemm))
     meta = {
         "cache_write_432": dict(bytes=cache_write_bytes(w), flops=0, bound="hbm", dtype="fp32->nvfp4",
                                 kernel="cache_write"),
@@ -381,9 +408,13 @@ def run_ours(args, rank, world):
                             dtype=mla.operand_dtype("decode"), kernel="decode"),
         "prefill": dict(bytes=prefill_bytes(p), flops=prefill_flops(p), bound=mla.kernel_kind("prefill"),
                         dtype=mla.operand_dtype("prefill"), kernel="prefill"),
+        "gemm_oproj": dict(bytes=p.total_tokens * k_in // 2 + n_out * k_in // 2 + (p.total_tokens + n_out) * k_in // 16
+                           + p.total_tokens * n_out * 2, flops=2.0 * p.total_tokens * n_out * k_in,
+                           bound=mla.kernel_kind("gemm"), dtype=mla.operand_dtype("gemm"), kernel=None,
+                           peak_x=FP4_OVER_BF16),
     }
     launches = mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(w.batch, w.heads, decode_splits) + \
-        mla.LAUNCHES_PER_CALL["prefill"]
+        mla.LAUNCHES_PER_CALL["prefill"] + (mla.LAUNCHES_PER_CALL["gemm"] if with_gemm else 0)
     if full:
         dm, dt = decode_setup(wm, 0), decode_setup(wt, 0)
         cache_write(dt)()  # the top-k cache is written once, outside the timed legs

@@ -317,6 +317,27 @@ int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
                                 void* stream);
 
 /*
+ * NVFP4 x NVFP4 GEMM on block-scaled tensor cores, reading the fused
+ * prefill output as written (the attention output projection, o_proj):
+ *     out[m, n] = gs_a * gs_w * sum_k a_hat[m, k] * w_hat[n, k]   (bf16)
+ * with a_hat = e2m1(code) * e4m3(scale) per block of 16 along k.
+ * Source: "feat: MLA prefill NVFP4 fused output - #8" (PR description: the
+ * packed e2m1 output and its 128x4-swizzled e4m3 scales are what the NVFP4
+ * GEMMs consume, with no standalone quantisation in between).
+ *   a_codes      : uint8 [M, K/2] (e.g. out_codes of the prefill, K = heads*128).
+ *   a_scales     : the 128x4-swizzled scale buffer of A's [M, K/16] scales
+ *                  (layout as for out_scales of the prefill), padding readable.
+ *   w_codes      : uint8 [N, K/2], the weight; w_scales likewise for [N, K/16].
+ *   gs_a, gs_w   : device fp32 global scales of A and W.
+ *   out          : bf16 [M, N] with row stride ldc >= N elements.
+ * N must be a multiple of 128 and K of 256; all pointers and ldc*2
+ * 16-byte aligned.  M == 0 or N == 0 is a no-op.
+ */
+int mla_nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int64_t M, const uint8_t* w_codes,
+                   const uint8_t* w_scales, int64_t N, int64_t K, const float* gs_a, const float* gs_w,
+                   void* out, int64_t ldc, uint32_t* error_word, void* stream);
+
+/*
  * Self-test of the bounded waits (test hook; no counterpart on the pages).
  * Every wait of the library's pipelined kernels (decode, prefill) gives up
  * after a time limit, ORs MLA_DEVERR_TIMEOUT into the error word and raises

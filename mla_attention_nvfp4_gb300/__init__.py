@@ -21,7 +21,7 @@ __all__ = [
     "load_library", "MLAError", "mla_nvfp4_global_scale", "mla_nvfp4_cache_write",
     "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode_default_splits", "decode_launches",
     "mla_nvfp4_decode", "mla_nvfp4_prefill_fused_out",
-    "mla_nvfp4_quantize_rows", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
+    "mla_nvfp4_quantize_rows", "mla_nvfp4_gemm", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
     "LAUNCHES_PER_CALL",
 ]
 
@@ -33,14 +33,14 @@ DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE, DEVERR_RANGE = 0x1, 0x2, 0x4, 0x8
 # decode launches one kernel with one key split, two (plus the merge) with
 # uniform splits and three (plan, decode, merge) when planned, see
 # decode_launches().
-LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 3, "prefill": 1, "global_scale": 2}
+LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 3, "prefill": 1, "global_scale": 2, "gemm": 1}
 # What bounds each hot kernel as built: "hbm", "tensor" (tcgen05 MMA) or
 # "alu" (CUDA-core arithmetic).
-KERNEL_BOUND = {"cache_write": "hbm", "decode": "tensor", "prefill": "tensor"}
+KERNEL_BOUND = {"cache_write": "hbm", "decode": "tensor", "prefill": "tensor", "gemm": "tensor"}
 # Operand type of each kernel's tensor-core products (fp32 accumulation):
 # the decode multiplies f16 operands (the dequantised latent c*s is exact in
 # f16), the prefill bf16 inputs as given.
-OPERAND_DTYPE = {"decode": "f16", "prefill": "bf16"}
+OPERAND_DTYPE = {"decode": "f16", "prefill": "bf16", "gemm": "nvfp4"}
 
 
 def kernel_kind(name: str) -> str:
@@ -76,6 +76,8 @@ _SIGS = {
                                              _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_int, _c_int,
                                              _c_f, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_nvfp4_quantize_rows": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_nvfp4_gemm": (_c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64,
+                                _c_vp, _c_vp]),
     "mla_nvfp4_selftest_wait": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp]),
 }
 
@@ -409,3 +411,29 @@ def mla_nvfp4_quantize_rows(x, global_scale, *, codes=None, scales=None, error_w
             _ptr(x), M, N, _ptr(global_scale), _ptr(codes), _ptr(scales), _ptr(error_word),
             _stream(x)))
     return codes, scales
+
+
+def mla_nvfp4_gemm(a_codes, a_scales, w_codes, w_scales, gs_a, gs_w, *, out=None):
+    """NVFP4 x NVFP4 -> bf16: a_codes [M, K/2] / w_codes [N, K/2] (uint8)
+    with their 128x4-swizzled scale buffers and device fp32 global scales;
+    returns out [M, N] bf16."""
+    dev = a_codes.device
+    for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"), (w_scales, "w_scales")):
+        _need(t, n, torch.uint8, dev)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _need(gs_a, "gs_a", torch.float32, dev)
+    _need(gs_w, "gs_w", torch.float32, dev)
+    if a_codes.dim() != 2 or w_codes.dim() != 2 or a_codes.shape[1] != w_codes.shape[1]:
+        raise ValueError("a_codes [M, K/2] and w_codes [N, K/2] must share K")
+    M, N, K = a_codes.shape[0], w_codes.shape[0], 2 * a_codes.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    if out.dim() != 2 or out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with a contiguous last dimension")
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_gemm", load_library().mla_nvfp4_gemm(
+            _ptr(a_codes), _ptr(a_scales), M, _ptr(w_codes), _ptr(w_scales), N, K, _ptr(gs_a), _ptr(gs_w),
+            _ptr(out), out.stride(0), None, _stream(a_codes)))
+    return out

@@ -291,6 +291,24 @@ int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
   return mla::launch_prefill(a, static_cast<cudaStream_t>(stream), sms);
 }
 
+int mla_nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int64_t M, const uint8_t* w_codes,
+                   const uint8_t* w_scales, int64_t N, int64_t K, const float* gs_a, const float* gs_w,
+                   void* out, int64_t ldc, uint32_t* error_word, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || (N > 0 && N % 128 != 0) || (K > 0 && K % 256 != 0)) return MLA_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MLA_OK;
+  if (K == 0) return MLA_ERR_INVALID_ARG;
+  if (a_codes == nullptr || a_scales == nullptr || w_codes == nullptr || w_scales == nullptr || gs_a == nullptr ||
+      gs_w == nullptr || out == nullptr || ldc < N || M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) || !aligned16(w_scales) ||
+      !aligned16(out) || (ldc * 2) % 16 != 0)
+    return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  mla::GemmArgs a{a_codes, a_scales, M, w_codes, w_scales, N, K, gs_a, gs_w, out, ldc, error_word};
+  return mla::launch_gemm(a, static_cast<cudaStream_t>(stream), sms);
+}
+
 int mla_nvfp4_quantize_rows(const float* x, int64_t M, int64_t N, const float* global_scale,
                             uint8_t* codes, uint8_t* scales, uint32_t* error_word, void* stream) {
   if (M < 0 || N < 0 || N % 16 != 0) return MLA_ERR_INVALID_ARG;

@@ -97,4 +97,20 @@ struct PrefillArgs {
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms);
 
+struct GemmArgs {
+  const uint8_t* a_codes;
+  const uint8_t* a_scales;
+  int64_t M;
+  const uint8_t* w_codes;
+  const uint8_t* w_scales;
+  int64_t N, K;
+  const float* gs_a;
+  const float* gs_w;
+  void* out;
+  int64_t ldc;
+  uint32_t* error_word;
+};
+
+int launch_gemm(const GemmArgs& a, cudaStream_t stream, int num_sms);
+
 }  // namespace mla
