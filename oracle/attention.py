@@ -21,7 +21,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import cache as cache_mod
+from . import cache as cache_mod, nvfp4
 
 D_QK_DECODE = 576
 D_V_DECODE = 512
@@ -100,6 +100,31 @@ def decode(q, cache, record_bytes, gs, softmax_scale, slots_per_seq, with_abs=Fa
         if with_abs:
             out_abs[b], _ = attend(q[b], k, np.abs(lat), softmax_scale)
     return (out, lse, out_abs) if with_abs else (out, lse)
+
+
+def quantize_query(q, gs_q):
+    """The absorbed query quantised to NVFP4 and read back (the caller-side
+    query quantisation of the absorbed decode): blocks of 16 along the 576
+    features of each head (the contraction axis of Q K^T), e4m3 block scales,
+    the float32 global scale gs_q of the whole query tensor.
+
+    Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for MLA (vLLM
+    TRITON_MLA) - #2244", first commit message (forward_mqa runs the
+    absorbed-Q quantise-dequantise before the decode kernel) and PR
+    description, "Contract notes" (NVFP4 is 1x16 along the contraction axis,
+    E4M3 block scale, amax/(6*448)).  Reading: the RoPE features are part of
+    the contraction and quantised with the rest (36 blocks per head); gs_q is
+    amax|q| / 2688 over the tensor.
+    Returns q_hat [B, H, 576] in float64."""
+    q = np.asarray(q, dtype=np.float32)
+    B, H, D = q.shape
+    codes, sb = nvfp4.quantize_blocks(q.reshape(B * H, D), gs_q)
+    return nvfp4.dequantize_blocks(codes, sb, gs_q).reshape(B, H, D)
+
+
+def decode_q4(q, cache, record_bytes, gs, softmax_scale, slots_per_seq, gs_q, with_abs=False):
+    """decode() of the NVFP4-quantised query quantize_query(q, gs_q)."""
+    return decode(quantize_query(q, gs_q), cache, record_bytes, gs, softmax_scale, slots_per_seq, with_abs)
 
 
 def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None, with_abs=False):

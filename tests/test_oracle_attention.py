@@ -236,3 +236,32 @@ def test_decode_with_abs_bounds_output():
     oa, _ = attention.attend(q, k, np.abs(v), 0.5)
     assert np.all(oa >= np.abs(o) - 1e-15)
     assert np.any(oa > np.abs(o) + 1e-3)  # mixed signs: strictly larger somewhere
+
+
+def test_query_quantisation_is_the_block_quantiser_and_lossless_on_grid():
+    # a query already on the NVFP4 grid (gs_q a power of two, a magnitude-6
+    # code in every block) is unchanged, so decode_q4 equals decode; and a
+    # generic query moves by at most half an e2m1 step of its block scale
+    from oracle import attention, cache as ocache, nvfp4
+    rng = np.random.default_rng(60)
+    B, H = 2, 4
+    gs_q = np.float32(2.0 ** -5)
+    sb = rng.integers(0x20, 0x58, (B * H, 36))
+    codes = rng.integers(0, 16, (B * H, 36, 16))
+    codes[..., 3] = 7
+    q_grid = (nvfp4.e2m1_decode(codes) * nvfp4.e4m3_decode(sb)[..., None] * float(gs_q)).reshape(B, H, 576)
+    assert np.array_equal(attention.quantize_query(q_grid.astype(np.float32), gs_q), q_grid)
+    kv = rng.standard_normal((100, 512)).astype(np.float32)
+    pe = rng.standard_normal((100, 64)).astype(np.float32)
+    gs = nvfp4.global_scale(np.abs(kv).max())
+    cache = ocache.encode_records(kv, pe.astype(np.float32), gs, 368)
+    slots = [np.arange(0, 60), np.arange(60, 100)]
+    o1, l1 = attention.decode_q4(q_grid.astype(np.float32), cache, 368, gs, 0.07, slots, gs_q)
+    o2, l2 = attention.decode(q_grid, cache, 368, gs, 0.07, slots)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    q = rng.standard_normal((B, H, 576)).astype(np.float32)
+    g = nvfp4.global_scale(np.abs(q).max())
+    qh = attention.quantize_query(q, g)
+    blocks = q.reshape(-1, 36, 16)
+    S = (np.abs(blocks).max(-1) / 6.0)[..., None]
+    assert np.all(np.abs(qh.reshape(-1, 36, 16) - blocks) <= S * (1.0 + 2.0 ** -3) + 1e-12)
