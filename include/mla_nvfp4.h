@@ -180,6 +180,30 @@ int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cac
                      const float* global_scale, void* out, float* lse, void* workspace,
                      size_t workspace_bytes, int num_splits, uint32_t* error_word, void* stream);
 
+/*
+ * mla_nvfp4_decode with the absorbed query quantised to NVFP4: the query's
+ * 576 features per head in blocks of 16 (the contraction axis of Q K^T),
+ * e4m3 block scales, global scale *q_global_scale (device fp32, e.g.
+ * mla_nvfp4_global_scale of q), correctly rounded as the cache write does;
+ * the scores are those of that quantised query:
+ *   scores = softmax_scale * q_hat . [x_hat, k_pe],  out = softmax . x_hat.
+ * Source: "#2244", first commit message (forward_mqa quantises the absorbed
+ * query before the decode kernel) and PR description, "Contract notes"
+ * (NVFP4 1x16 along the contraction axis).  The latent part of the score
+ * product runs on block-scaled fp4 tensor cores straight from the cache's
+ * codes and scales; the RoPE part in f16, with k_pe / gs rounded once to f16
+ * (|k_pe / gs| above 65504 saturates and sets MLA_DEVERR_RANGE).  An invalid
+ * q_global_scale gives zero scores' query and MLA_DEVERR_SCALE.  Other
+ * arguments, the workspace, the splits and the result as mla_nvfp4_decode.
+ */
+int mla_nvfp4_decode_q4(const void* q, int batch, int num_heads, const uint8_t* cache,
+                        int64_t num_slots, int record_bytes, const int32_t* page_table,
+                        int64_t page_table_stride, int page_size, const int32_t* seq_lens,
+                        const int32_t* topk_indices, int topk, float softmax_scale,
+                        const float* global_scale, const float* q_global_scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, int num_splits, uint32_t* error_word,
+                        void* stream);
+
 /* Size of the library's built-in decode scratch: MLA_DECODE_STATIC_ROWS
  * partial rows (one head of one split each) and the bytes those rows take
  * (the value of mla_nvfp4_decode_workspace_size for that many rows). */

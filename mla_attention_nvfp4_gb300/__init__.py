@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = [
     "load_library", "MLAError", "mla_nvfp4_global_scale", "mla_nvfp4_cache_write",
     "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode_default_splits", "decode_launches",
-    "mla_nvfp4_decode", "mla_nvfp4_prefill_fused_out",
+    "mla_nvfp4_decode", "mla_nvfp4_decode_q4", "mla_nvfp4_prefill_fused_out",
     "mla_nvfp4_quantize_rows", "mla_nvfp4_gemm", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
     "LAUNCHES_PER_CALL",
 ]
@@ -65,6 +65,9 @@ _SIGS = {
     "mla_nvfp4_decode": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64, _c_int,
                                   _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp, _c_vp,
                                   ctypes.c_size_t, _c_int, _c_vp, _c_vp]),
+    "mla_nvfp4_decode_q4": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64, _c_int,
+                                     _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                     ctypes.c_size_t, _c_int, _c_vp, _c_vp]),
     "mla_nvfp4_decode_noalloc": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64,
                                           _c_int, _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp,
                                           _c_int, _c_vp, _c_vp]),
@@ -205,9 +208,15 @@ def decode_launches(batch: int, num_heads: int, num_splits: int = 0, *, paged: b
     return 1 if mla_nvfp4_decode_default_splits(batch, num_heads, num_splits) == 1 else 2
 
 
+def mla_nvfp4_decode_q4(q, cache, global_scale, softmax_scale, q_global_scale, **kw):
+    """mla_nvfp4_decode with the query quantised to NVFP4 (global scale
+    q_global_scale, a device fp32 [1]) and block-scaled fp4 scores."""
+    return mla_nvfp4_decode(q, cache, global_scale, softmax_scale, _q_global_scale=q_global_scale, **kw)
+
+
 def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, seq_lens=None,
                      page_size=64, topk_indices=None, out=None, lse=None, workspace=None,
-                     num_splits=0, error_word=None, return_lse=False):
+                     num_splits=0, error_word=None, return_lse=False, _q_global_scale=None):
     """Absorbed MLA decode.  q [B,H,576] bf16 -> out [B,H,512] bf16 (and lse [B,H] fp32)."""
     dev = q.device
     _need(q, "q", torch.bfloat16)
@@ -236,11 +245,15 @@ def mla_nvfp4_decode(q, cache, global_scale, softmax_scale, *, page_table=None, 
         topk = topk_indices.shape[1] if topk_indices is not None else 0
         if topk_indices is not None and topk_indices.stride(1) != 1:
             raise ValueError("topk_indices rows must be contiguous")
-        _check("mla_nvfp4_decode", lib.mla_nvfp4_decode(
-            _ptr(q), B, H, _ptr(cache), cache.shape[0], cache.shape[1], _ptr(page_table), pt_stride,
-            page_size, _ptr(seq_lens), _ptr(topk_indices), topk, float(softmax_scale),
-            _ptr(global_scale), _ptr(out), _ptr(lse), _ptr(workspace),
-            workspace.numel() if workspace is not None else 0, num_splits, _ptr(error_word), _stream(q)))
+        args = (_ptr(q), B, H, _ptr(cache), cache.shape[0], cache.shape[1], _ptr(page_table), pt_stride,
+                page_size, _ptr(seq_lens), _ptr(topk_indices), topk, float(softmax_scale), _ptr(global_scale))
+        tail = (_ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                num_splits, _ptr(error_word), _stream(q))
+        if _q_global_scale is None:
+            _check("mla_nvfp4_decode", lib.mla_nvfp4_decode(*args, *tail))
+        else:
+            _need(_q_global_scale, "q_global_scale", torch.float32, dev)
+            _check("mla_nvfp4_decode_q4", lib.mla_nvfp4_decode_q4(*args, _ptr(_q_global_scale), *tail))
     return (out, lse) if return_lse else out
 
 

@@ -136,7 +136,7 @@ int decode_prepare(const void* q, int batch, int num_heads, const uint8_t* cache
                    int page_size, const int32_t* seq_lens, const int32_t* topk_indices, int topk,
                    float softmax_scale, const float* global_scale, void* out, float* lse,
                    void* workspace, size_t workspace_bytes, int num_splits, uint32_t* error_word,
-                   mla::DecodeArgs* a, int* sms_out) {
+                   mla::DecodeArgs* a, int* sms_out, const float* q_global_scale = nullptr) {
   if (record_bytes != MLA_RECORD_BF16_ROPE && record_bytes != MLA_RECORD_FP8_ROPE)
     return MLA_ERR_RECORD_BYTES;
   if (batch < 0 || num_heads < 1 || num_slots < 0) return MLA_ERR_INVALID_ARG;
@@ -177,7 +177,7 @@ int decode_prepare(const void* q, int batch, int num_heads, const uint8_t* cache
   }
   *a = mla::DecodeArgs{q, batch, num_heads, cache, num_slots, record_bytes, page_table,
                        page_table_stride, page_size, seq_lens, topk_indices, sparse ? topk : 0,
-                       softmax_scale, global_scale, out, lse, workspace, workspace_bytes,
+                       softmax_scale, global_scale, q_global_scale, out, lse, workspace, workspace_bytes,
                        planned ? 0 : num_splits, planned, error_word};
   *sms_out = sms;
   return MLA_OK;
@@ -204,6 +204,25 @@ int mla_nvfp4_decode(const void* q, int batch, int num_heads, const uint8_t* cac
                                     page_table_stride, page_size, seq_lens, topk_indices, topk,
                                     softmax_scale, global_scale, out, lse, workspace,
                                     workspace_bytes, num_splits, error_word, &a, &sms))
+    return st;
+  if (batch == 0) return MLA_OK;
+  return mla::launch_decode(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+int mla_nvfp4_decode_q4(const void* q, int batch, int num_heads, const uint8_t* cache,
+                        int64_t num_slots, int record_bytes, const int32_t* page_table,
+                        int64_t page_table_stride, int page_size, const int32_t* seq_lens,
+                        const int32_t* topk_indices, int topk, float softmax_scale,
+                        const float* global_scale, const float* q_global_scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, int num_splits, uint32_t* error_word,
+                        void* stream) {
+  if (batch > 0 && q_global_scale == nullptr) return MLA_ERR_INVALID_ARG;
+  mla::DecodeArgs a;
+  int sms = 0;
+  if (const int st = decode_prepare(q, batch, num_heads, cache, num_slots, record_bytes, page_table,
+                                    page_table_stride, page_size, seq_lens, topk_indices, topk,
+                                    softmax_scale, global_scale, out, lse, workspace,
+                                    workspace_bytes, num_splits, error_word, &a, &sms, q_global_scale))
     return st;
   if (batch == 0) return MLA_OK;
   return mla::launch_decode(a, static_cast<cudaStream_t>(stream), sms);

@@ -113,6 +113,7 @@ struct Params {
   int topk_n;
   float softmax_scale;
   const float* gs;
+  const float* gs_q;  // NVFP4-query mode: the query's global scale (null otherwise)
   float* part_o;    // [rows, heads, 512]: split partials
   float* part_lse;  // [rows, heads]
   int splits;       // uniform mode: key splits per sequence
@@ -141,6 +142,7 @@ struct alignas(8) Barriers {
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_full;
+  uint64_t sfa_ready;  // NVFP4-query mode: the query scales are in TMEM
 };
 
 // Key addressing in two halves so that the index load can be issued a tile
@@ -437,6 +439,174 @@ __device__ bool dequant_role(const DeqCtx& c) {
   return bad;
 }
 
+// The online softmax over an item's tiles (thread = head row; warps 0..3
+// read their lane quarter of the scores): raw scores from TMEM, masking of
+// padding keys, lazy max raise with an O rescale, probabilities as f16 into
+// the scores' columns for P.V, running row sum.  Shared by both decode
+// kernels.
+__device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, volatile int& abort_s, uint32_t tmem,
+                                              uint32_t lane_off, int b, int tile0, int nt, int n_keys,
+                                              float score_scale, bool& ok, float& m_run, float& l_run) {
+  uint32_t* err = p.error_word;
+  const int lane = threadIdx.x & 31;
+  // per-tile validity: lane checks keys `lane` and `lane + 32`
+  int32_t ia = load_index(p, b, tile0 * kTok + lane), ib = load_index(p, b, tile0 * kTok + 32 + lane);
+  for (int j = 0; j < nt; ++j) {
+    const int pb = j & 1;
+    const int key = (tile0 + j) * kTok + lane;
+    bool badv = false;
+    const unsigned va = __ballot_sync(0xffffffffu, key_slot(p, ia, key, n_keys, badv) >= 0);
+    const unsigned vb = __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0);
+    if (j + 1 < nt) {
+      ia = load_index(p, b, key + kTok);
+      ib = load_index(p, b, key + kTok + 32);
+    }
+    if (!bar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // raw scores: four loads in flight, one wait
+    float x[kTok];
+    {
+      uint32_t v[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld16(tmem + lane_off + col_s(pb) + 16 * c, v[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < kTok; ++c) x[c] = __uint_as_float(v[c >> 4][c & 15]);
+    }
+    // max of the raw scores (score_scale > 0), padding keys at -inf; the
+    // scale is applied inside the exponent below
+    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if ((va & vb) != 0xffffffffu) {
+#pragma unroll
+      for (int c = 0; c < kTok; ++c) {
+        const unsigned m = c < 32 ? va : vb;
+        x[c] = ((m >> (c & 31)) & 1u) ? x[c] : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kTok; c += 2) mq[(c >> 1) & 3] = max3(mq[(c >> 1) & 3], x[c], x[c + 1]);
+    const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * score_scale;  // log2 units
+    float m_use = m_run, alpha = 1.f;
+    const bool raise = mx > m_run + kRescaleThreshold;
+    if (raise) {
+      m_use = mx;
+      alpha = ex2_approx(m_run - mx);
+    }
+    // an O rescale must follow every earlier P.V and precede PV(j).
+    // PV(j-1) and PV(j-2) come from different issuers; each issuer's
+    // earlier P.V products retire before its later ones.
+    if (__any_sync(0xffffffffu, raise && j > 0)) {
+      if (!bar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s) ||
+          (j >= 2 && !bar_wait(&bars.pv_done[j & 1], ((j - 2) >> 1) & 1, err, &abort_s))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 4
+      for (int c = 0; c < 256; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_off + kTO + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+        tmem_st16(tmem + lane_off + kTO + c, v);
+      }
+      tmem_st_wait();
+    }
+    m_run = m_use;
+    const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;  // no valid key so far
+    // exponent arguments and row sums two at a time
+    const uint64_t sc2 = pk2(score_scale, score_scale), nm2 = pk2(-m_ref, -m_ref);
+    uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial sums
+    uint32_t pv[kTok / 2];
+#pragma unroll
+    for (int i = 0; i < kTok / 2; ++i) {
+      float a0, a1;
+      unpk2(fma2(pk2(x[2 * i], x[2 * i + 1]), sc2, nm2), a0, a1);
+      const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+      ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
+      pv[i] = pack_f16(p0, p1);  // P <= 2^14 (lazy reference), f16 operand
+    }
+    float ls[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) unpk2(ls2[i], ls[2 * i], ls[2 * i + 1]);
+    l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+    // P(j) over S(j): the buffer's previous P was read by PV(j-2), which
+    // ran before QK(j) wrote S(j)
+    uint32_t v0[16], v1[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v0[i] = pv[i];
+      v1[i] = pv[16 + i];
+    }
+    tmem_st16(tmem + lane_off + col_s(pb), v0);
+    tmem_st16(tmem + lane_off + col_s(pb) + 16, v1);
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&bars.p_full[pb]);
+  }
+}
+
+// The partial output of an item (thread = head row): O half / l, scaled by
+// gs, and the LSE, as the final bf16 output when the item is its sequence's
+// only one, else as an fp32 partial row for the merge.  TMEM loads are
+// warp-collective, so every lane loads; only stores depend on the head.
+__device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, uint32_t lane_off, bool ok, int nt,
+                                              float m_run, float l_run, float gs, int64_t row0, int b, int head,
+                                              bool head_ok, bool direct, int rank) {
+  // partial output of this split: O half / l (scaled by gs), lse.  TMEM
+  // loads are warp-collective, so every lane loads; only stores depend on
+  // the head.
+  const bool live = __all_sync(0xffffffffu, ok) && nt > 0;
+  const bool have = live && l_run > 0.f;
+  const float f = have ? gs / l_run : 0.f;
+  const int64_t row = row0 + head;
+  // For a sequence's only item the merge is the identity (weight
+  // exp(0) = 1, sum 1): the final bf16 output and the LSE are written here
+  // and no merge touches the sequence.
+  float4* dst = reinterpret_cast<float4*>(p.part_o + row * 512 + 256 * rank);
+  uint4* dst_bf = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + head) * 512 + 256 * rank);
+  if (live) tc_fence_after();
+#pragma unroll 2
+  for (int c = 0; c < 256; c += 16) {
+    uint32_t v[16];
+    if (live) {
+      tmem_ld16(tmem + lane_off + kTO + c, v);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0u;
+    }
+    if (head_ok) {
+      if (direct) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
+          w[i] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        dst_bf[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst_bf[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[c / 4 + i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
+                                       __uint_as_float(v[4 * i + 2]) * f, __uint_as_float(v[4 * i + 3]) * f);
+      }
+    }
+  }
+  if (head_ok && rank == 0) {
+    const float l = have ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    if (!direct)
+      p.part_lse[row] = l;
+    else if (p.lse != nullptr)
+      p.lse[static_cast<int64_t>(b) * p.num_heads + head] = l;
+  }
+}
+
 template <int kRecord>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -680,155 +850,437 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
       tc_fence_before();
       mbar_arrive(&bars.q_ready);
 
-      // per-tile validity: lane checks keys `lane` and `lane + 32`
-      int32_t ia = load_index(p, b, tile0 * kTok + lane), ib = load_index(p, b, tile0 * kTok + 32 + lane);
-      for (int j = 0; j < nt; ++j) {
-        const int pb = j & 1;
-        const int key = (tile0 + j) * kTok + lane;
-        bool badv = false;
-        const unsigned va = __ballot_sync(0xffffffffu, key_slot(p, ia, key, n_keys, badv) >= 0);
-        const unsigned vb = __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0);
-        if (j + 1 < nt) {
-          ia = load_index(p, b, key + kTok);
-          ib = load_index(p, b, key + kTok + 32);
-        }
-        if (!bar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // raw scores: four loads in flight, one wait
-        float x[kTok];
-        {
-          uint32_t v[4][16];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld16(tmem + lane_off + col_s(pb) + 16 * c, v[c]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < kTok; ++c) x[c] = __uint_as_float(v[c >> 4][c & 15]);
-        }
-        // max of the raw scores (score_scale > 0), padding keys at -inf; the
-        // scale is applied inside the exponent below
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if ((va & vb) != 0xffffffffu) {
-#pragma unroll
-          for (int c = 0; c < kTok; ++c) {
-            const unsigned m = c < 32 ? va : vb;
-            x[c] = ((m >> (c & 31)) & 1u) ? x[c] : -INFINITY;
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < kTok; c += 2) mq[(c >> 1) & 3] = max3(mq[(c >> 1) & 3], x[c], x[c + 1]);
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * score_scale;  // log2 units
-        float m_use = m_run, alpha = 1.f;
-        const bool raise = mx > m_run + kRescaleThreshold;
-        if (raise) {
-          m_use = mx;
-          alpha = ex2_approx(m_run - mx);
-        }
-        // an O rescale must follow every earlier P.V and precede PV(j).
-        // PV(j-1) and PV(j-2) come from different issuers; each issuer's
-        // earlier P.V products retire before its later ones.
-        if (__any_sync(0xffffffffu, raise && j > 0)) {
-          if (!bar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s) ||
-              (j >= 2 && !bar_wait(&bars.pv_done[j & 1], ((j - 2) >> 1) & 1, err, &abort_s))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 4
-          for (int c = 0; c < 256; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_off + kTO + c, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st16(tmem + lane_off + kTO + c, v);
-          }
-          tmem_st_wait();
-        }
-        m_run = m_use;
-        const float m_ref = (m_use == -INFINITY) ? 0.f : m_use;  // no valid key so far
-        // exponent arguments and row sums two at a time
-        const uint64_t sc2 = pk2(score_scale, score_scale), nm2 = pk2(-m_ref, -m_ref);
-        uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial sums
-        uint32_t pv[kTok / 2];
-#pragma unroll
-        for (int i = 0; i < kTok / 2; ++i) {
-          float a0, a1;
-          unpk2(fma2(pk2(x[2 * i], x[2 * i + 1]), sc2, nm2), a0, a1);
-          const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-          ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
-          pv[i] = pack_f16(p0, p1);  // P <= 2^14 (lazy reference), f16 operand
-        }
-        float ls[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) unpk2(ls2[i], ls[2 * i], ls[2 * i + 1]);
-        l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
-        // P(j) over S(j): the buffer's previous P was read by PV(j-2), which
-        // ran before QK(j) wrote S(j)
-        uint32_t v0[16], v1[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          v0[i] = pv[i];
-          v1[i] = pv[16 + i];
-        }
-        tmem_st16(tmem + lane_off + col_s(pb), v0);
-        tmem_st16(tmem + lane_off + col_s(pb) + 16, v1);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars.p_full[pb]);
-      }
+      softmax_tiles(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run);
       if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
     }
-    // partial output of this split: O half / l (scaled by gs), lse.  TMEM
-    // loads are warp-collective, so every lane loads; only stores depend on
-    // the head.
-    const bool live = __all_sync(0xffffffffu, ok) && nt > 0;
-    const bool have = live && l_run > 0.f;
-    const float f = have ? gs / l_run : 0.f;
-    const int64_t row = row0 + head;
-    // For a sequence's only item the merge is the identity (weight
-    // exp(0) = 1, sum 1): the final bf16 output and the LSE are written here
-    // and no merge touches the sequence.
-    float4* dst = reinterpret_cast<float4*>(p.part_o + row * 512 + 256 * rank);
-    uint4* dst_bf = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + head) * 512 + 256 * rank);
-    if (live) tc_fence_after();
-#pragma unroll 2
-    for (int c = 0; c < 256; c += 16) {
-      uint32_t v[16];
-      if (live) {
-        tmem_ld16(tmem + lane_off + kTO + c, v);
-        tmem_ld_wait();
-      } else {
+    write_partial(p, tmem, lane_off, ok, nt, m_run, l_run, gs, row0, b, head, head_ok, direct, rank);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// ================================================== NVFP4-query decode mode
+// The absorbed query quantised to NVFP4 (16 features a block along the 576
+// of a head, e4m3 scales, the query's global scale gs_q) in the staging
+// pass, as the pages' caller-side query quantisation; the latent score
+// product then runs on block-scaled fp4 tensor cores straight from the
+// cache's codes and scales:
+//   s_j = softmax_scale * gs_q * gs * ( sum_lat (c_q s_q)(c_k s_k)
+//                                       + sum_rope (c_q s_q)(k_pe / gs) ),
+// the first sum by eight kind::mxf4nvf4 MMAs (M 128 heads, N 64 keys, K 64)
+// with the query scales and the keys' block scales in TMEM, the second by
+// four f16 MMAs into the same accumulator: c_q s_q is exact in f16, k_pe / gs
+// is rounded once to f16 (saturating, flagged MLA_DEVERR_RANGE).  P.V is the
+// f16 product of the exact path.  Per key only this CTA's 256 output
+// features are dequantised; the record's codes and scales go to shared
+// memory as they are.
+//
+// Shared memory (1024-aligned parts): query codes 2 x 16 KB (128 heads x 256
+// bytes, 128-byte swizzle), query scale tiles 4 KB; per tile parity: key
+// codes 2 x 8 KB, RoPE f16 8 KB, key scale tiles 4 KB, V part 4 x 8 KB.
+// TMEM: O [0,256), scores [256,384), query RoPE (f16) [384,416), query
+// scales [416,448), key scales per parity [448,480) [480,512).
+constexpr uint32_t kQ4Q = 0;
+constexpr uint32_t kQ4Sfa = 32768;
+constexpr uint32_t kQ4Buf0 = 36864;
+constexpr uint32_t kQ4BufBytes = 61440;
+constexpr uint32_t kQ4K = 0, kQ4Rope = 16384, kQ4Sfb = 24576, kQ4V = 28672;  // within a buffer
+constexpr uint32_t kQ4SmBytes = kQ4Buf0 + 2 * kQ4BufBytes;
+constexpr uint32_t kQ4SmAlloc = kQ4SmBytes + 1024;
+static_assert(kQ4SmAlloc + 512 <= 232448, "shared memory budget");
+constexpr uint32_t kQ4TRope = 384, kQ4TSfa = 416;
+__host__ __device__ constexpr uint32_t q4_col_sfb(int buf) { return 448u + 32u * buf; }
+constexpr uint32_t kIdescQ4 = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kTok >> 3) << 17) |
+                              (static_cast<uint32_t>(kHeads >> 4) << 24);  // mxf4nvf4, e2m1 x e2m1, ue4m3 scales
+
+// One 512-byte tile of 128 rows x 4 scale bytes, as tcgen05.cp 32x128b reads
+// it: 32 rows of 16 bytes (byte (r % 32) * 16 + (r / 32) * 4 + block),
+// four 8-row core matrices 128 bytes apart, no swizzle.
+__device__ __forceinline__ uint64_t q4_sf_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+__device__ __forceinline__ void q4_sf_copy(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+__device__ __forceinline__ void q4_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(kIdescQ4), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Raw record parts per key: 0 = all codes and scales (straight to the
+// shared tiles), 1 = this CTA's 256 latent features and their scales
+// (dequantised to the V part), 2 = the RoPE part (to f16, over gs).
+template <int Q, int kRecord>
+struct RawQ4 {
+  static constexpr int kN = (Q == 0) ? 18 : (Q == 1) ? 9 : ((kRecord == 368) ? 4 : 8);
+  uint4 v[kN];
+};
+
+template <int Q, int kRecord>
+__device__ __forceinline__ void q4_load(RawQ4<Q, kRecord>& r, const uint8_t* rec, int rank) {
+  if constexpr (Q == 0) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0u;
+    for (int i = 0; i < 18; ++i) r.v[i] = ldg16(rec + 16 * i);
+  } else if constexpr (Q == 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r.v[i] = ldg16(rec + 128 * rank + 16 * i);
+    r.v[8] = ldg16(rec + 256 + 16 * rank);
+  } else {
+#pragma unroll
+    for (int i = 0; i < RawQ4<Q, kRecord>::kN; ++i) r.v[i] = ldg16(rec + 288 + 16 * i);
+  }
+}
+
+struct Q4Ctx {
+  const Params& p;
+  Barriers* bars;
+  volatile int* abort_s;
+  uint32_t sbuf;  // shared address of tile buffer 0
+  int rank, b, tile0, nt, n_keys, k;
+  float inv_gs;
+};
+
+// Write part Q of key k of tile j into the tile's buffers.  False if a wait
+// gave up.
+template <int Q, int kRecord>
+__device__ __forceinline__ bool q4_convert(const Q4Ctx& c, int j, const RawQ4<Q, kRecord>& r, float& rope_max) {
+  uint32_t* err = c.p.error_word;
+  Barriers& bars = *c.bars;
+  const int k = c.k;
+  const uint32_t buf = c.sbuf + (j & 1) * kQ4BufBytes;
+  const uint32_t ph = ((j >> 1) & 1) ^ 1;
+  if constexpr (Q == 0) {
+    if (!bar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)  // codes: two 128-byte swizzled chunks
+      sts128(buf + kQ4K + (u >> 3) * 8192 + k * 128 + (((u & 7) ^ (k & 7)) << 4), r.v[u]);
+    const uint32_t w[8] = {r.v[16].x, r.v[16].y, r.v[16].z, r.v[16].w, r.v[17].x, r.v[17].y, r.v[17].z, r.v[17].w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t)  // scales of blocks 4t..4t+3 into scale tile t
+      sts32(buf + kQ4Sfb + 512 * t + (k & 31) * 16 + (k >> 5) * 4, w[t]);
+    fence_async_smem();
+    mbar_arrive(&bars.t_full[j & 1]);
+  } else if constexpr (Q == 1) {
+    if (!bar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dequant_segment(r.v[i], byte_of(r.v[8], 2 * i), byte_of(r.v[8], 2 * i + 1), buf + kQ4V, 4 * i, k);
+    fence_async_smem();
+    mbar_arrive(&bars.v_full[j & 1]);
+  } else {
+    if (!bar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
+    const uint32_t row = buf + kQ4Rope + k * 128;
+    auto put = [&](int u, const float (&f)[8]) {
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = f[2 * i] * c.inv_gs, bb = f[2 * i + 1] * c.inv_gs;
+        rope_max = max3(rope_max, fabsf(a), fabsf(bb));
+        asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h[i]) : "f"(bb), "f"(a));
       }
-      if (head_ok) {
-        if (direct) {
-          uint32_t w[8];
+      sts128(row + ((u ^ (k & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
+    };
+    if constexpr (kRecord == 368) {  // e4m3 -> f32 (exact) -> / gs -> f16
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
-            w[i] = *reinterpret_cast<uint32_t*>(&h2);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t ws[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t two = ws[2 * hh + e];
+            const uint32_t lo2 = e4m3x2_to_f16x2(two & 0xFFFFu), hi2 = e4m3x2_to_f16x2(two >> 16);
+            const __half2 a = *reinterpret_cast<const __half2*>(&lo2), bq = *reinterpret_cast<const __half2*>(&hi2);
+            f[4 * e] = __low2float(a);
+            f[4 * e + 1] = __high2float(a);
+            f[4 * e + 2] = __low2float(bq);
+            f[4 * e + 3] = __high2float(bq);
           }
-          dst_bf[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst_bf[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[c / 4 + i] = make_float4(__uint_as_float(v[4 * i]) * f, __uint_as_float(v[4 * i + 1]) * f,
-                                         __uint_as_float(v[4 * i + 2]) * f, __uint_as_float(v[4 * i + 3]) * f);
+          put(2 * i + hh, f);
         }
       }
+    } else {  // bf16 -> / gs -> f16
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t ws[4] = {r.v[u].x, r.v[u].y, r.v[u].z, r.v[u].w};
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bf16x2_to_f32(ws[i], f[2 * i], f[2 * i + 1]);
+        put(u, f);
+      }
     }
-    if (head_ok && rank == 0) {
-      const float l = have ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-      if (!direct)
-        p.part_lse[row] = l;
-      else if (p.lse != nullptr)
-        p.lse[static_cast<int64_t>(b) * p.num_heads + head] = l;
+    fence_async_smem();
+    mbar_arrive(&bars.t_full[j & 1]);
+  }
+  return true;
+}
+
+template <int Q, int kRecord>
+__device__ bool q4_role(const Q4Ctx& c) {
+  const Params& p = c.p;
+  bool bad = false;
+  float rope_max = 0.f;
+  auto slot_of = [&](int j, int32_t idx) { return key_slot(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad); };
+  auto index_of = [&](int j) { return load_index(p, c.b, (c.tile0 + j) * kTok + c.k); };
+  const int nt = c.nt;
+  const int64_t s_cur = nt > 0 ? slot_of(0, index_of(0)) : -1;
+  int64_t s_nxt = nt > 1 ? slot_of(1, index_of(1)) : -1;
+  int32_t i_2 = nt > 2 ? index_of(2) : -1;
+  RawQ4<Q, kRecord> ra;
+  auto load_or_zero = [&](int64_t slot) {
+    if (slot >= 0) {
+      q4_load(ra, p.cache + slot * kRecord, c.rank);
+    } else {
+#pragma unroll
+      for (int i = 0; i < RawQ4<Q, kRecord>::kN; ++i) ra.v[i] = make_uint4(0, 0, 0, 0);
     }
+  };
+  load_or_zero(s_cur);
+#pragma unroll 1
+  for (int j = 0; j < nt; ++j) {
+    const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
+    i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
+    if (!q4_convert<Q, kRecord>(c, j, ra, rope_max)) break;
+    if (j + 1 < nt) load_or_zero(s_nxt);
+    s_nxt = s_2;
+  }
+  if (rope_max > 65504.f) flag_error(p.error_word, MLA_DEVERR_RANGE);
+  return bad;
+}
+
+template <int kRecord>
+__global__ void __launch_bounds__(kThreads, 1) decode_q4_kernel(Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Barriers bars;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = blockIdx.x & 1;
+  const int hg = blockIdx.z;
+  int b, tile0, per;
+  int64_t row0;
+  bool direct;
+  if (p.plan_items != nullptr) {
+    const int item = blockIdx.x >> 1;
+    if (item >= p.plan_hdr[0]) return;  // the plan has fewer items than the grid: the whole CTA leaves
+    const int2 it = p.plan_items[item];
+    const int2 sq = p.plan_seqs[it.x];
+    b = it.x;
+    per = p.plan_hdr[1];
+    tile0 = it.y * per;
+    direct = sq.x < 0;
+    row0 = direct ? 0 : static_cast<int64_t>(sq.x + it.y) * p.num_heads;
+  } else {
+    const int split = blockIdx.x >> 1;
+    b = blockIdx.y;
+    const int n_keys_u = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
+    per = ((n_keys_u + kTok - 1) / kTok + p.splits - 1) / p.splits;
+    tile0 = split * per;
+    direct = p.splits == 1;
+    row0 = (static_cast<int64_t>(b) * p.splits + split) * p.num_heads;
+  }
+  const int n_keys = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
+  const int n_tiles_all = n_keys / kTok + (n_keys % kTok != 0);
+  const int nt = max(0, min(n_tiles_all, tile0 + per) - tile0);
+  uint32_t* err = p.error_word;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem + kQ4Q), sSfa = smem_u32(smem + kQ4Sfa), sBuf = smem_u32(smem + kQ4Buf0);
+
+  if (threadIdx.x == 0) {
+    abort_s = 0;
+    mbar_init(&bars.q_ready, 128);
+    mbar_init(&bars.sfa_ready, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.t_full[i], 128);  // codes and scales (64 threads), RoPE (64)
+      mbar_init(&bars.t_empty[i], 1);
+      mbar_init(&bars.v_full[i], 64);
+      mbar_init(&bars.v_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.p_full[i], 128);
+      mbar_init(&bars.pv_done[i], 1);
+    }
+    mbar_init(&bars.o_full, 2);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == kMmaWarp || warp == kMmaWarp2) {
+    // ----------------------------------------------------------------- MMA
+    // issuer p runs the tiles of parity p: QK (scales of the tile into TMEM,
+    // 8 block-scaled latent MMAs, 4 f16 RoPE MMAs), then P.V
+    const int par = (warp == kMmaWarp) ? 0 : 1;
+    if (lane == 0 && nt > 0) {
+      const uint64_t dq = smem_desc_sw128(sQ, 0, 1024);
+      const uint64_t dbuf = smem_desc_sw128(sBuf, 0, 1024);
+      const uint64_t dbuf_mn = smem_desc_sw128(sBuf, kChunk, 1024);  // V read MN-major: 64-feature chunks 8 KB apart
+      bool ok = bar_wait(&bars.q_ready, 0, err, &abort_s);
+      tc_fence_after();
+      if (ok && par == 0) {  // the query scales, for both issuers
+#pragma unroll 1
+        for (int t = 0; t < 8; ++t) q4_sf_copy(tmem + kQ4TSfa + 4 * t, q4_sf_desc(sSfa + 512 * t));
+        mma_commit(&bars.sfa_ready);
+      }
+      ok = ok && bar_wait(&bars.sfa_ready, 0, err, &abort_s);
+      tc_fence_after();
+      auto issue_qk = [&](int j) -> bool {
+        const int tb = j & 1;
+        if (!bar_wait(&bars.t_full[tb], (j >> 1) & 1, err, &abort_s)) return false;
+        tc_fence_after();
+        const uint32_t bsh = sBuf + tb * kQ4BufBytes;
+#pragma unroll 1
+        for (int t = 0; t < 8; ++t) q4_sf_copy(tmem + q4_col_sfb(tb) + 4 * t, q4_sf_desc(bsh + kQ4Sfb + 512 * t));
+        const uint32_t d = tmem + col_s(tb);
+        const uint64_t dk = dbuf + (tb * kQ4BufBytes + kQ4K) / 16;
+#pragma unroll 1
+        for (int t = 0; t < 8; ++t)  // K 64 a step: chunk t / 4, 32 bytes along the swizzled row
+          q4_mma(d, dq + (t >> 2) * (16384 / 16) + 2 * (t & 3), dk + (t >> 2) * (8192 / 16) + 2 * (t & 3),
+                 tmem + kQ4TSfa + 4 * t, tmem + q4_col_sfb(tb) + 4 * t, t > 0 ? 1u : 0u);
+        const uint64_t dr = dbuf + (tb * kQ4BufBytes + kQ4Rope) / 16;
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) mma_ts(d, tmem + kQ4TRope + 8 * kk, dr + 2 * kk, kIdescQK, 1u);
+        mma_commit(&bars.t_empty[tb]);
+        mma_commit(&bars.s_full[tb]);
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int pb = j & 1;
+        if (!bar_wait(&bars.v_full[pb], (j >> 1) & 1, err, &abort_s) ||
+            !bar_wait(&bars.p_full[pb], (j >> 1) & 1, err, &abort_s))
+          return false;
+        tc_fence_after();
+        const uint64_t vd = dbuf_mn + (pb * kQ4BufBytes + kQ4V) / 16;
+#pragma unroll 1
+        for (int kk = 0; kk < kTok / 16; ++kk)
+          mma_ts(tmem + kTO, tmem + col_s(pb) + 8 * kk, vd + (2048 * kk) / 16, kIdescPV, 1u);  // O starts at 0
+        mma_commit(&bars.v_empty[pb]);
+        mma_commit(&bars.pv_done[pb]);
+        return true;
+      };
+      for (int j = par; ok && j < nt; j += 2) ok = issue_qk(j) && issue_pv(j);
+      mma_commit(&bars.o_full);
+      bar_wait(&bars.o_full, 0, err, nullptr);  // both issuers' MMAs retired
+    }
+  } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
+    // ------------------------------------------------------- record parts
+    const int di = threadIdx.x - 32 * kDeqWarp0;
+    const int k = di & 63, q = di >> 6;
+    const float gs = *p.gs;
+    Q4Ctx c{p, &bars, &abort_s, sBuf, rank, b, tile0, nt, n_keys, k, scale_ok(gs) ? 1.f / gs : 0.f};
+    bool bad;
+    if (q == 0)
+      bad = q4_role<0, kRecord>(c);
+    else if (q == 1)
+      bad = q4_role<1, kRecord>(c);
+    else
+      bad = q4_role<2, kRecord>(c);
+    if (bad && rank == 0 && q == 0) flag_error(err, MLA_DEVERR_BOUNDS);
+  } else {
+    // ------------------------------ query quantisation, softmax, epilogue
+    const int hr = warp * 32 + lane;
+    const int head = hg * kHeads + hr;
+    const bool head_ok = head < p.num_heads;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float gs = *p.gs, gs_q = *p.gs_q;
+    const bool scales_ok = scale_ok(gs) && scale_ok(gs_q);
+    const float score_scale = p.softmax_scale * gs_q * gs * kLog2e;
+    bool ok = true;
+    float m_run = -INFINITY, l_run = 0.f;
+    if (nt > 0) {
+      // the query row to NVFP4 (correctly rounded, as the cache write):
+      // latent codes to shared memory, their scales to the scale tiles, the
+      // RoPE part's values c*s (exact in f16) to TMEM
+      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q + (static_cast<int64_t>(b) * p.num_heads + head) * 576);
+      const float inv_gs_q = inv_scale(gs_q);
+      uint32_t sf_word = 0, rope[16];
+#pragma unroll 1
+      for (int u = 0; u < 36; u += 2) {  // two blocks of 16 = one 16-byte unit of codes
+        uint2 codes[2];
+        uint32_t sbs[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int blk = u + h;
+          const uint4 w0 = head_ok ? ldg16(qrow + 32 * blk) : make_uint4(0, 0, 0, 0);
+          const uint4 w1 = head_ok ? ldg16(qrow + 32 * blk + 16) : make_uint4(0, 0, 0, 0);
+          float x[16];
+          const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) bf16x2_to_f32(ws[i], x[2 * i], x[2 * i + 1]);
+          float R = 0.f, S = 0.f;
+          bool bounded = true;
+          sbs[h] = scales_ok ? block_scale_rn(fmaxf(amax8(x), amax8(x + 8)), inv_gs_q, gs_q, R, S, bounded) : 0u;
+          codes[h] = scales_ok ? make_uint2(encode8_rn(x, R, S, bounded), encode8_rn(x + 8, R, S, bounded))
+                               : make_uint2(0u, 0u);
+        }
+        if (u < 32) {
+          const int cu = u >> 1;  // 16-byte unit of the 256-byte code row
+          sts128(sQ + (cu >> 3) * 16384 + hr * 128 + (((cu & 7) ^ (hr & 7)) << 4),
+                 make_uint4(codes[0].x, codes[0].y, codes[1].x, codes[1].y));
+          sf_word |= (sbs[0] | (sbs[1] << 8)) << (16 * ((u >> 1) & 1));
+          if ((u & 3) == 2) {  // blocks u-2 .. u+1 done: scale tile u / 4
+            sts32(sSfa + 512 * (u >> 2) + (hr & 31) * 16 + (hr >> 5) * 4, sf_word);
+            sf_word = 0;
+          }
+        } else {
+          // RoPE values c * s (exact in f16), 8 f16 pairs a block: blocks u
+          // and u + 1 fill 16 TMEM columns
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t f = e4m3x2_to_f16x2(sbs[h] | (sbs[h] << 8));
+            uint32_t hh[4];
+            e2m1x8_to_f16x8(codes[h].x, hh);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rope[8 * h + i] = hmul2_u32(hh[i], f);
+            e2m1x8_to_f16x8(codes[h].y, hh);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rope[8 * h + 4 + i] = hmul2_u32(hh[i], f);
+          }
+          tmem_st16(tmem + lane_off + kQ4TRope + 8 * (u - 32), rope);
+        }
+      }
+      {  // O starts at zero: every P.V accumulates, whichever issuer runs first
+        uint32_t z[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll 1
+        for (int cc = 0; cc < 256; cc += 16) tmem_st16(tmem + lane_off + kTO + cc, z);
+      }
+      fence_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.q_ready);
+      if (!scales_ok && hr == 0 && rank == 0) flag_error(err, MLA_DEVERR_SCALE);
+      softmax_tiles(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run);
+      if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
+    }
+    write_partial(p, tmem, lane_off, ok, nt, m_run, l_run, gs, row0, b, head, head_ok, direct, rank);
   }
   tc_fence_before();
   __syncthreads();
@@ -1154,6 +1606,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
   p.topk_n = a.topk;
   p.softmax_scale = a.softmax_scale;
   p.gs = a.gs;
+  p.gs_q = a.gs_q;
   p.splits = a.num_splits;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
@@ -1186,7 +1639,16 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
     if (grid.y > 65535u) return MLA_ERR_INVALID_ARG;
   }
   if (grid.z > 65535u) return MLA_ERR_INVALID_ARG;
-  if (a.record_bytes == 432) {
+  if (a.gs_q != nullptr) {
+    const bool r432 = a.record_bytes == 432;
+    const void* kern = r432 ? reinterpret_cast<const void*>(decode_q4_kernel<432>)
+                            : reinterpret_cast<const void*>(decode_q4_kernel<368>);
+    if (const int st = smem_limit_once(kern, static_cast<int>(kQ4SmAlloc), r432 ? 5 : 6)) return st;
+    if (r432)
+      decode_q4_kernel<432><<<grid, kThreads, kQ4SmAlloc, stream>>>(p);
+    else
+      decode_q4_kernel<368><<<grid, kThreads, kQ4SmAlloc, stream>>>(p);
+  } else if (a.record_bytes == 432) {
     if (const int st = smem_limit_once(reinterpret_cast<const void*>(decode_tc_kernel<432>), static_cast<int>(kSmAlloc), 1))
       return st;
     decode_tc_kernel<432><<<grid, kThreads, kSmAlloc, stream>>>(p);

@@ -53,6 +53,7 @@ struct DecodeArgs {
   int topk;
   float softmax_scale;
   const float* gs;
+  const float* gs_q;  // non-null: NVFP4-query mode with this query global scale
   void* out;
   float* lse;
   void* workspace;
