@@ -165,6 +165,66 @@ def prefill(q, k, v, cu_seqlens, softmax_scale, heads=None, with_abs=False):
     return (o, lse, o_abs) if with_abs else (o, lse)
 
 
+def prefill_with_context(q, k, v, cu_seqlens, k_ctx, v_ctx, cu_ctx, softmax_scale, with_abs=False):
+    """Prefill of new tokens after a cached context (chunked-context
+    prefill): query i of sequence s attends to every context key of s
+    (k_ctx / v_ctx rows cu_ctx[s]..cu_ctx[s+1]) and to the new keys 0..i of
+    s, in one softmax.
+
+    Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for MLA (vLLM
+    TRITON_MLA) - #2244", first commit message (the prefill's natural-log
+    LSE serves chunked-context merging; forward_mha keeps the chunked-context
+    path, whose context keys and values are projected from the latent
+    gathered out of the paged cache) and second commit message (cached
+    context chunks are gathered from the quantised paged cache).
+    q, k [T,H,192], v [T,H,128] (new tokens); k_ctx [Tc,H,192], v_ctx
+    [Tc,H,128].  Returns (o [T,H,128], lse [H,T]) in float64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    kc = np.asarray(k_ctx, dtype=np.float64)
+    vc = np.asarray(v_ctx, dtype=np.float64)
+    T, H, _ = q.shape
+    o = np.zeros((T, H, v.shape[2]))
+    o_abs = np.zeros((T, H, v.shape[2])) if with_abs else None
+    lse = np.full((H, T), -np.inf)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    cc = np.asarray(cu_ctx, dtype=np.int64)
+    for s_ in range(len(cu) - 1):
+        a, e = int(cu[s_]), int(cu[s_ + 1])
+        ca, ce = int(cc[s_]), int(cc[s_ + 1])
+        for i in range(a, e):
+            for h in range(H):
+                keys = np.concatenate([kc[ca:ce, h], k[a:i + 1, h]])
+                vals = np.concatenate([vc[ca:ce, h], v[a:i + 1, h]])
+                oi, li = attend(q[i:i + 1, h], keys, vals, softmax_scale)
+                o[i, h], lse[h, i] = oi[0], li[0]
+                if with_abs:
+                    o_abs[i, h] = attend(q[i:i + 1, h], keys, np.abs(vals), softmax_scale)[0][0]
+    return (o, lse, o_abs) if with_abs else (o, lse)
+
+
+def attend_all(q, k, v, cu_seqlens, k_ctx, v_ctx, cu_ctx, softmax_scale):
+    """Each query of sequence s over all keys of its context chunk only (no
+    mask): the partial result a context chunk contributes.  Returns (o
+    [T,H,Dv], lse [H,T]); a sequence with an empty chunk gives o = 0, lse =
+    -inf."""
+    q = np.asarray(q, dtype=np.float64)
+    T, H, _ = q.shape
+    o = np.zeros((T, H, np.asarray(v_ctx).shape[2]))
+    lse = np.full((H, T), -np.inf)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    cc = np.asarray(cu_ctx, dtype=np.int64)
+    for s_ in range(len(cu) - 1):
+        a, e = int(cu[s_]), int(cu[s_ + 1])
+        ca, ce = int(cc[s_]), int(cc[s_ + 1])
+        for h in range(H):
+            oo, ll = attend(q[a:e, h], np.asarray(k_ctx, np.float64)[ca:ce, h],
+                            np.asarray(v_ctx, np.float64)[ca:ce, h], softmax_scale)
+            o[a:e, h], lse[h, a:e] = oo, ll
+    return o, lse
+
+
 def prefill_rows(q, k, v, cu_seqlens, softmax_scale, rows, head, with_abs=False):
     """Causal prefill for selected global query rows of one head (sampling).
     With ``with_abs`` also softmax(s) @ |v| for those rows."""

@@ -99,3 +99,24 @@ def decode_records(rec, gs, record_bytes: int):
         hi = rec[:, ROPE_OFF + 1:ROPE_OFF + 2 * D_ROPE:2].astype(np.uint16)
         rope = bf16_from_bits(lo | (hi << 8)).astype(np.float64)
     return latent, rope
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value (8 significant bits,
+    ties to even), returned as float32 (bf16 values are float32 values).
+    Exact: the 8-bit mantissa is rounded from the float64 significand."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)  # x = m * 2^e, 0.5 <= |m| < 1
+    r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)  # numpy rint: half to even
+    return r.astype(np.float32)
+
+
+def gather_latent(cache, slots, gs, record_bytes: int):
+    """The latent of cached tokens read back for a context chunk: records at
+    `slots` dequantised (x_hat = e2m1 * e4m3 * gs, exactly) and rounded once
+    to bf16; k_pe as stored (bf16, or the e4m3 value, exact in bf16).
+    Source: "#2244", second commit message (cached-context prefill chunks
+    gather from the quantised paged cache).  Returns (kv_c [n,512], k_pe
+    [n,64]) as float32 holding bf16 values."""
+    lat, rope = decode_records(np.asarray(cache)[np.asarray(slots, dtype=np.int64)], gs, record_bytes)
+    return bf16_round(lat), bf16_round(rope)

@@ -265,3 +265,28 @@ def test_query_quantisation_is_the_block_quantiser_and_lossless_on_grid():
     blocks = q.reshape(-1, 36, 16)
     S = (np.abs(blocks).max(-1) / 6.0)[..., None]
     assert np.all(np.abs(qh.reshape(-1, 36, 16) - blocks) <= S * (1.0 + 2.0 ** -3) + 1e-12)
+
+
+def test_context_prefill_is_the_merge_of_its_parts():
+    # attention over [context chunk; causal new keys] in one softmax equals
+    # the LSE merge of the chunk's all-keys attention and the causal
+    # attention of the new keys, and reduces to the causal prefill when the
+    # chunk is empty
+    from oracle import attention
+    rng = np.random.default_rng(71)
+    H, lens, ctx = 2, (5, 1, 9), (7, 0, 3)
+    T, Tc = sum(lens), sum(ctx)
+    q, k = rng.standard_normal((T, H, 192)), rng.standard_normal((T, H, 192))
+    v = rng.standard_normal((T, H, 128))
+    kc, vc = rng.standard_normal((Tc, H, 192)), rng.standard_normal((Tc, H, 128))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    cc = np.concatenate([[0], np.cumsum(ctx)])
+    o, lse = attention.prefill_with_context(q, k, v, cu, kc, vc, cc, 0.07)
+    o1, l1 = attention.attend_all(q, k, v, cu, kc, vc, cc, 0.07)
+    o2, l2 = attention.prefill(q, k, v, cu, 0.07)
+    for h in range(H):
+        om, lm = attention.lse_merge(np.stack([o1[:, h], o2[:, h]]), np.stack([l1[h], l2[h]]))
+        assert np.allclose(om, o[:, h], atol=1e-12) and np.allclose(lm, lse[h], atol=1e-12)
+    z = np.zeros((0, H, 192))
+    o0, l0 = attention.prefill_with_context(q, k, v, cu, z, np.zeros((0, H, 128)), np.zeros(4, dtype=int), 0.07)
+    assert np.allclose(o0, o2, atol=1e-12) and np.allclose(l0, l2, atol=1e-12)

@@ -71,3 +71,24 @@ def test_write_cache_skips_negative_slots():
     cache.write_cache(c, kv2, pe2, np.array([2, -1]), np.float32(1.0), 432)
     assert np.all(c[[0, 1, 3]] == 0xAB)
     assert c[2, 0] == 0x17
+
+
+def test_bf16_round_is_nearest_even():
+    # against a search over the two bf16 neighbours of each value, with
+    # exact ties (the midpoint of two bf16 values) going to the even one
+    import torch
+    from oracle import cache as oc
+    rng = np.random.default_rng(70)
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))
+    lo = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    cand = []
+    b = lo.view(torch.int16).numpy().astype(np.int32)
+    for d in (-1, 0, 1):
+        cand.append(torch.from_numpy((b + d).astype(np.int16)).view(torch.bfloat16).double().numpy())
+    cand = np.stack(cand, 1)
+    dist = np.abs(cand - x[:, None])
+    best = cand[np.arange(len(x)), dist.argmin(1)]
+    got = oc.bf16_round(x).astype(np.float64)
+    assert np.array_equal(got, best)
+    mids = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(2.0 + 2.0 ** -7)])
+    assert oc.bf16_round(mids).tolist() == [1.0, 1.0 + 4 * 2.0 ** -8, -2.0]
