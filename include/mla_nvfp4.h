@@ -341,6 +341,64 @@ int mla_nvfp4_prefill_fused_out(const void* q, const void* k, const void* v,
                                 void* stream);
 
 /*
+ * Chunked-context prefill over the quantised cache, in three calls.
+ * Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for MLA (vLLM
+ * TRITON_MLA) - #2244", first commit message (the prefill's natural-log LSE
+ * serves chunked-context merging; the chunked-context path projects context
+ * keys and values from the latent) and second commit message (cached
+ * context chunks are gathered from the quantised paged cache).  A prefill
+ * of new tokens after a cached context: gather each context chunk's latent
+ * (mla_nvfp4_gather_latent), project it to per-head keys and values (the
+ * model's kv_b_proj; the caller's GEMM), attend the new queries to each
+ * chunk and, causally, to the new tokens (mla_nvfp4_prefill_partial), then
+ * merge the partial results and write the NVFP4 output
+ * (mla_nvfp4_merge_fused_out).
+ *
+ * mla_nvfp4_gather_latent: cache records at slots[0..n) (int64; -1 gives
+ * zeros, a slot >= num_slots zeros and MLA_DEVERR_BOUNDS) read back as
+ *   kv_c : bf16 [n, 512], x_hat = e2m1 * e4m3 * gs rounded once to bf16
+ *          (nearest, ties to even, from the exact product);
+ *   k_pe : bf16 [n, 64], as stored (432-byte records) or the e4m3 value.
+ */
+int mla_nvfp4_gather_latent(const uint8_t* cache, int64_t num_slots, int record_bytes, const float* global_scale,
+                            const int64_t* slots, int64_t n, void* kv_c, void* k_pe, uint32_t* error_word,
+                            void* stream);
+
+/*
+ * mla_nvfp4_prefill_partial: the prefill's attention with an unquantised
+ * result, for merging.  q bf16 [total_tokens, H, 192]; k bf16 [.., H, 192]
+ * and v bf16 [.., H, 128] (strides as in mla_nvfp4_prefill_fused_out).
+ *   cu_seqlens_k NULL : query i of sequence s attends causally to keys
+ *                       0..i of its own tokens (k, v rows as q's).
+ *   cu_seqlens_k set  : int32 [num_seqs + 1] over total_k rows of k and v;
+ *                       the queries of sequence s attend to every key of
+ *                       rows [cu_seqlens_k[s], cu_seqlens_k[s+1]) (a
+ *                       context chunk); an empty chunk gives O = 0, LSE =
+ *                       -inf.
+ *   out  : fp32 [total_tokens, H, 128], the normalised output;
+ *   lse  : fp32 [H, total_tokens], natural log (required).
+ */
+int mla_nvfp4_prefill_partial(const void* q, const void* k, const void* v, int64_t q_stride_t,
+                              int64_t q_stride_h, int64_t k_stride_t, int64_t k_stride_h, int64_t v_stride_t,
+                              int64_t v_stride_h, const int32_t* cu_seqlens, const int32_t* cu_seqlens_k,
+                              int num_seqs, int64_t total_tokens, int64_t total_k, int max_seqlen,
+                              int num_heads, float softmax_scale, float* out, float* lse,
+                              uint32_t* error_word, void* stream);
+
+/*
+ * mla_nvfp4_merge_fused_out: num_parts partial results over the same
+ * queries, o_parts fp32 [num_parts, T, H, 128] (each normalised) and
+ * lse_parts fp32 [num_parts, H, T], merged by LSE (O = sum_i exp(lse_i -
+ * LSE) O_i, LSE = ln sum_i exp(lse_i); all -inf gives O = 0) and written
+ * as mla_nvfp4_prefill_fused_out writes its output: out_codes uint8
+ * [T, H*64], out_scales 128x4-swizzled (padding zeroed), lse fp32 [H, T] or
+ * NULL; the epilogue's quantiser with *global_scale.
+ */
+int mla_nvfp4_merge_fused_out(const float* o_parts, const float* lse_parts, int num_parts, int64_t total_tokens,
+                              int num_heads, const float* global_scale, uint8_t* out_codes, uint8_t* out_scales,
+                              float* lse, uint32_t* error_word, void* stream);
+
+/*
  * NVFP4 x NVFP4 GEMM on block-scaled tensor cores, reading the fused
  * prefill output as written (the attention output projection, o_proj):
  *     out[m, n] = gs_a * gs_w * sum_k a_hat[m, k] * w_hat[n, k]   (bf16)

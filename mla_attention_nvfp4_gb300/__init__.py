@@ -21,7 +21,8 @@ __all__ = [
     "load_library", "MLAError", "mla_nvfp4_global_scale", "mla_nvfp4_cache_write",
     "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode_default_splits", "decode_launches",
     "mla_nvfp4_decode", "mla_nvfp4_decode_q4", "mla_nvfp4_prefill_fused_out",
-    "mla_nvfp4_quantize_rows", "mla_nvfp4_gemm", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
+    "mla_nvfp4_quantize_rows", "mla_nvfp4_gemm", "mla_nvfp4_gather_latent", "mla_nvfp4_prefill_partial",
+    "mla_nvfp4_merge_fused_out", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
     "LAUNCHES_PER_CALL",
 ]
 
@@ -33,7 +34,8 @@ DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE, DEVERR_RANGE = 0x1, 0x2, 0x4, 0x8
 # decode launches one kernel with one key split, two (plus the merge) with
 # uniform splits and three (plan, decode, merge) when planned, see
 # decode_launches().
-LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 3, "prefill": 1, "global_scale": 2, "gemm": 1}
+LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 3, "prefill": 1, "global_scale": 2, "gemm": 1,
+                     "gather_latent": 1, "prefill_partial": 1, "merge_fused_out": 1}
 # What bounds each hot kernel as built: "hbm", "tensor" (tcgen05 MMA) or
 # "alu" (CUDA-core arithmetic).
 KERNEL_BOUND = {"cache_write": "hbm", "decode": "tensor", "prefill": "tensor", "gemm": "tensor"}
@@ -79,6 +81,12 @@ _SIGS = {
                                              _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_int, _c_int,
                                              _c_f, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_nvfp4_quantize_rows": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_nvfp4_gather_latent": (_c_int, [_c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_nvfp4_prefill_partial": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64,
+                                           _c_vp, _c_vp, _c_int, _c_i64, _c_i64, _c_int, _c_int, _c_f, _c_vp,
+                                           _c_vp, _c_vp, _c_vp]),
+    "mla_nvfp4_merge_fused_out": (_c_int, [_c_vp, _c_vp, _c_int, _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp,
+                                           _c_vp, _c_vp]),
     "mla_nvfp4_gemm": (_c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64,
                                 _c_vp, _c_vp]),
     "mla_nvfp4_selftest_wait": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp]),
@@ -450,3 +458,87 @@ def mla_nvfp4_gemm(a_codes, a_scales, w_codes, w_scales, gs_a, gs_w, *, out=None
             _ptr(a_codes), _ptr(a_scales), M, _ptr(w_codes), _ptr(w_scales), N, K, _ptr(gs_a), _ptr(gs_w),
             _ptr(out), out.stride(0), None, _stream(a_codes)))
     return out
+
+
+def mla_nvfp4_gather_latent(cache, global_scale, slots, *, kv_c=None, k_pe=None, error_word=None):
+    """Records of ``slots`` (int64 [n]) read back: kv_c bf16 [n, 512] (the
+    dequantised latent rounded to bf16) and k_pe bf16 [n, 64]."""
+    dev = cache.device
+    _need(cache, "cache", torch.uint8, dev)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    _need(slots, "slots", torch.int64, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    if cache.dim() != 2 or not cache.is_contiguous() or not slots.is_contiguous():
+        raise ValueError("cache [num_slots, record_bytes] and slots must be contiguous")
+    n = slots.numel()
+    if kv_c is None:
+        kv_c = torch.empty((n, 512), dtype=torch.bfloat16, device=dev)
+    if k_pe is None:
+        k_pe = torch.empty((n, 64), dtype=torch.bfloat16, device=dev)
+    for t, name, d in ((kv_c, "kv_c", 512), (k_pe, "k_pe", 64)):
+        _need(t, name, torch.bfloat16, dev)
+        if t.shape != (n, d) or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [n, {d}]")
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_gather_latent", load_library().mla_nvfp4_gather_latent(
+            _ptr(cache), cache.shape[0], cache.shape[1], _ptr(global_scale), _ptr(slots), n, _ptr(kv_c), _ptr(k_pe),
+            _ptr(error_word), _stream(cache)))
+    return kv_c, k_pe
+
+
+def mla_nvfp4_prefill_partial(q, k, v, cu_seqlens, max_seqlen, softmax_scale, *, cu_seqlens_k=None, out=None,
+                              lse=None, error_word=None):
+    """Prefill attention with an unquantised result: causal over the
+    sequence's own tokens (cu_seqlens_k None) or over all keys of its chunk
+    of k / v (cu_seqlens_k given).  Returns (out fp32 [T, H, 128], lse fp32
+    [H, T])."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, dev)
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError(f"{n} must be [T, H, D] with a contiguous last dimension")
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    T, H, dq = q.shape
+    if dq != 192 or k.shape[1:] != (H, 192) or v.shape[1:] != (H, 128) or k.shape[0] != v.shape[0]:
+        raise ValueError("expected q [T,H,192], k [Tk,H,192], v [Tk,H,128]")
+    if cu_seqlens_k is None and k.shape[0] != T:
+        raise ValueError("without cu_seqlens_k, k and v hold the queries' own tokens")
+    if out is None:
+        out = torch.empty((T, H, 128), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_prefill_partial", load_library().mla_nvfp4_prefill_partial(
+            _ptr(q), _ptr(k), _ptr(v), q.stride(0), q.stride(1), k.stride(0), k.stride(1), v.stride(0), v.stride(1),
+            _ptr(cu_seqlens), _ptr(cu_seqlens_k), cu_seqlens.numel() - 1, T, k.shape[0], int(max_seqlen), H,
+            float(softmax_scale), _ptr(out), _ptr(lse), _ptr(error_word), _stream(q)))
+    return out, lse
+
+
+def mla_nvfp4_merge_fused_out(o_parts, lse_parts, global_scale, *, out_codes=None, out_scales=None, lse=None,
+                              error_word=None):
+    """Merge partials o_parts fp32 [P, T, H, 128] / lse_parts fp32 [P, H, T]
+    by LSE into the fused NVFP4 output: (codes [T, H*64], swizzled scales)."""
+    dev = o_parts.device
+    _need(o_parts, "o_parts", torch.float32, dev)
+    _need(lse_parts, "lse_parts", torch.float32, dev)
+    _need(global_scale, "global_scale", torch.float32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    if o_parts.dim() != 4 or o_parts.shape[3] != 128 or not o_parts.is_contiguous() or not lse_parts.is_contiguous():
+        raise ValueError("o_parts must be contiguous [P, T, H, 128]")
+    P, T, H, _ = o_parts.shape
+    if lse_parts.shape != (P, H, T):
+        raise ValueError("lse_parts must be [P, H, T]")
+    if out_codes is None:
+        out_codes = torch.empty((T, H * 64), dtype=torch.uint8, device=dev)
+    if out_scales is None:
+        out_scales = torch.empty(prefill_scale_bytes(T, H), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_merge_fused_out", load_library().mla_nvfp4_merge_fused_out(
+            _ptr(o_parts), _ptr(lse_parts), P, T, H, _ptr(global_scale), _ptr(out_codes), _ptr(out_scales),
+            _ptr(lse), _ptr(error_word), _stream(o_parts)))
+    return out_codes, out_scales

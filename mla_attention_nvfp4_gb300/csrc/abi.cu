@@ -328,6 +328,82 @@ int mla_nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, int64_t M, c
   return mla::launch_gemm(a, static_cast<cudaStream_t>(stream), sms);
 }
 
+int mla_nvfp4_prefill_partial(const void* q, const void* k, const void* v, int64_t q_stride_t,
+                              int64_t q_stride_h, int64_t k_stride_t, int64_t k_stride_h, int64_t v_stride_t,
+                              int64_t v_stride_h, const int32_t* cu_seqlens, const int32_t* cu_seqlens_k,
+                              int num_seqs, int64_t total_tokens, int64_t total_k, int max_seqlen,
+                              int num_heads, float softmax_scale, float* out, float* lse,
+                              uint32_t* error_word, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || num_heads < 1 || total_k < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (total_tokens == 0 || num_seqs == 0) return total_tokens != 0 ? MLA_ERR_INVALID_ARG : MLA_OK;
+  if (max_seqlen < 1 || total_tokens > (int64_t(1) << 31) - 1 || total_k > (int64_t(1) << 31) - 1)
+    return MLA_ERR_INVALID_ARG;
+  if (q == nullptr || cu_seqlens == nullptr || out == nullptr || lse == nullptr) return MLA_ERR_INVALID_ARG;
+  const int64_t tk = cu_seqlens_k != nullptr ? total_k : total_tokens;
+  if (tk > 0 && (k == nullptr || v == nullptr)) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !(softmax_scale < 3.0e38f)) return MLA_ERR_INVALID_ARG;
+  if (q_stride_h < MLA_D_QK_PREFILL || k_stride_h < MLA_D_QK_PREFILL || v_stride_h < MLA_D_V_PREFILL ||
+      q_stride_t < q_stride_h * (num_heads - 1) + MLA_D_QK_PREFILL ||
+      k_stride_t < k_stride_h * (num_heads - 1) + MLA_D_QK_PREFILL ||
+      v_stride_t < v_stride_h * (num_heads - 1) + MLA_D_V_PREFILL)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (q_stride_t * 2) % 16 ||
+      (q_stride_h * 2) % 16 || (k_stride_t * 2) % 16 || (k_stride_h * 2) % 16 || (v_stride_t * 2) % 16 ||
+      (v_stride_h * 2) % 16)
+    return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  mla::PrefillArgs a{q, k, v, q_stride_t, q_stride_h, k_stride_t, k_stride_h, v_stride_t,
+                     v_stride_h, cu_seqlens, num_seqs, total_tokens, max_seqlen, num_heads,
+                     softmax_scale, nullptr, nullptr, nullptr, lse, error_word};
+  a.o_out = out;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.total_k = total_k;
+  if (cu_seqlens_k != nullptr && total_k == 0) {
+    // every chunk empty (the kernel writes O = 0, LSE = -inf): the key maps
+    // still need a valid base, and no key block is read
+    a.k = q;
+    a.v = q;
+    a.k_st = q_stride_t;
+    a.k_sh = q_stride_h;
+    a.v_st = q_stride_t;
+    a.v_sh = q_stride_h;
+    a.total_k = 1;
+  }
+  return mla::launch_prefill(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+int mla_nvfp4_merge_fused_out(const float* o_parts, const float* lse_parts, int num_parts, int64_t total_tokens,
+                              int num_heads, const float* global_scale, uint8_t* out_codes, uint8_t* out_scales,
+                              float* lse, uint32_t* error_word, void* stream) {
+  if (num_parts < 1 || total_tokens < 0 || num_heads < 1) return MLA_ERR_INVALID_ARG;
+  if (total_tokens == 0) return MLA_OK;
+  if (o_parts == nullptr || lse_parts == nullptr || global_scale == nullptr || out_codes == nullptr ||
+      out_scales == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || (reinterpret_cast<uintptr_t>(out_codes) & 7u) != 0) return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  return mla::launch_merge_fused_out(o_parts, lse_parts, num_parts, total_tokens, num_heads, global_scale,
+                                     out_codes, out_scales, lse, error_word, static_cast<cudaStream_t>(stream));
+}
+
+int mla_nvfp4_gather_latent(const uint8_t* cache, int64_t num_slots, int record_bytes, const float* global_scale,
+                            const int64_t* slots, int64_t n, void* kv_c, void* k_pe, uint32_t* error_word,
+                            void* stream) {
+  if (record_bytes != MLA_RECORD_BF16_ROPE && record_bytes != MLA_RECORD_FP8_ROPE) return MLA_ERR_RECORD_BYTES;
+  if (n < 0 || num_slots < 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (cache == nullptr || global_scale == nullptr || slots == nullptr || kv_c == nullptr || k_pe == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(cache) || !aligned16(kv_c) || !aligned16(k_pe)) return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  return mla::launch_gather_latent(cache, num_slots, record_bytes, global_scale, slots, n, kv_c, k_pe, error_word,
+                                   static_cast<cudaStream_t>(stream), sms);
+}
+
 int mla_nvfp4_quantize_rows(const float* x, int64_t M, int64_t N, const float* global_scale,
                             uint8_t* codes, uint8_t* scales, uint32_t* error_word, void* stream) {
   if (M < 0 || N < 0 || N % 16 != 0) return MLA_ERR_INVALID_ARG;

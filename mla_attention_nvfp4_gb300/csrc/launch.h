@@ -38,6 +38,13 @@ int launch_quantize_rows(const float* x, int64_t M, int64_t N, const float* gs, 
 
 int launch_global_scale(const void* x, int64_t n, float* gs, cudaStream_t stream, int num_sms);
 
+int launch_gather_latent(const uint8_t* cache, int64_t num_slots, int record_bytes, const float* gs,
+                         const int64_t* slots, int64_t n, void* kv_c, void* k_pe, uint32_t* error_word,
+                         cudaStream_t stream, int num_sms);
+int launch_merge_fused_out(const float* o_parts, const float* lse_parts, int parts, int64_t T, int H,
+                           const float* gs, uint8_t* codes, uint8_t* scales, float* lse, uint32_t* error_word,
+                           cudaStream_t stream);
+
 struct DecodeArgs {
   const void* q;
   int batch;
@@ -94,6 +101,12 @@ struct PrefillArgs {
   uint8_t* out_scales;
   float* lse;
   uint32_t* error_word;
+  // partial mode (o_out set): fp32 normalised output, no codes; a key table
+  // (cu_seqlens_k over total_k key rows) makes every key of a sequence's
+  // chunk visible instead of the causal prefix of its own tokens
+  float* o_out = nullptr;
+  const int32_t* cu_seqlens_k = nullptr;
+  int64_t total_k = 0;
 };
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms);

@@ -79,6 +79,14 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
+// Two e4m3 bytes (lo in bits 0..7) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_pair(uint32_t two_bytes) {
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(two_bytes & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return h2;
+}
+
 __device__ __forceinline__ bool scale_ok(float gs) {
   return gs >= 7.888609052210118e-31f && gs <= 1.2676506002282294e30f;  // [2^-100, 2^100]
 }

@@ -106,6 +106,14 @@ struct Params {
   uint8_t* scales;
   float* lse;
   uint32_t* error_word;
+  // partial mode (kPartial): the normalised fp32 output [total, H, 128]
+  // (lse required), and, when cu_k is set, the key sequences of the key
+  // tensors (total_k rows): queries of sequence s see every key of
+  // [cu_k[s], cu_k[s+1]) (a context chunk), else the causal prefix of their
+  // own sequence
+  float* o_out;
+  const int32_t* cu_k;
+  int64_t total_k;
 };
 
 constexpr int kRing = 4;  // item indices in flight from the producer to the other roles
@@ -129,6 +137,7 @@ static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsEpi <= 4 * 128, "register split
 
 struct Item {
   int h, seq_begin, n, row0, n_kv;
+  int k_begin, n_k;  // key rows of the item's sequence (its own tokens unless a key table is given)
   bool valid;
 };
 
@@ -146,8 +155,22 @@ __device__ __forceinline__ Item item_at(const Params& p, uint32_t idx, bool& bad
     bad = true;
     it.n = 0;
   }
-  it.valid = it.row0 < it.n;
-  it.n_kv = it.valid ? (min(it.n, it.row0 + kBM) - 1) / kBN + 1 : 0;  // causal: keys < row0 + 128
+  if (p.cu_k != nullptr) {
+    it.k_begin = p.cu_k[seq];
+    const int k_end = p.cu_k[seq + 1];
+    it.n_k = k_end - it.k_begin;
+    if (it.k_begin < 0 || k_end > p.total_k || it.n_k < 0) {
+      bad = true;
+      it.n_k = 0;
+    }
+    it.n_kv = (it.n_k + kBN - 1) / kBN;  // every key of the chunk
+    it.valid = it.row0 < it.n && it.n_kv > 0;
+  } else {
+    it.k_begin = it.seq_begin;
+    it.n_k = it.n;
+    it.valid = it.row0 < it.n;
+    it.n_kv = it.valid ? (min(it.n, it.row0 + kBM) - 1) / kBN + 1 : 0;  // causal: keys < row0 + 128
+  }
   return it;
 }
 
@@ -161,7 +184,8 @@ __device__ int grab_item(const Params& p, bool& bad) {
     const Item w = item_at(p, idx, bad);
     if (w.valid) return static_cast<int>(idx);
     const uint32_t group = idx / static_cast<uint32_t>(p.q_tiles);
-    const uint32_t tiles = static_cast<uint32_t>((w.n + kBM - 1) / kBM);
+    // a sequence with an empty key chunk has no item at all
+    const uint32_t tiles = w.n_k > 0 || p.cu_k == nullptr ? static_cast<uint32_t>((w.n + kBM - 1) / kBM) : 0u;
     atomicMax(p.sched, group * static_cast<uint32_t>(p.q_tiles) + static_cast<uint32_t>(p.q_tiles) - tiles);
   }
 }
@@ -213,6 +237,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, abort));
 }
 
+template <bool kPartial>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, Params p) {
@@ -227,15 +252,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t k_tiles_sf = (static_cast<int64_t>(p.num_heads) * 8 + 3) / 4;
 
-  // rows [total, roundup(total,128)) of the scale columns are zero
-  {
+  if constexpr (!kPartial) {
+    // rows [total, roundup(total,128)) of the scale columns are zero
     const int64_t Mp = (p.total + 127) / 128 * 128;
     const int64_t pad = (Mp - p.total) * 8;
     for (int h = blockIdx.x; h < p.num_heads; h += gridDim.x)
       for (int64_t i = threadIdx.x; i < pad; i += kThreads)
         p.scales[sf_offset(p.total + i / 8, static_cast<int64_t>(h) * 8 + i % 8, k_tiles_sf)] = 0;
+  } else if (p.cu_k != nullptr) {
+    // queries whose key chunk is empty attend to nothing: O = 0, LSE = -inf
+    for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x) {
+      const int a = p.cu[s], e = p.cu[s + 1];
+      if (p.cu_k[s + 1] - p.cu_k[s] != 0 || a < 0 || e > p.total || a > e) continue;
+      for (int64_t i = threadIdx.x; i < static_cast<int64_t>(e - a) * p.num_heads * kDv; i += kThreads)
+        p.o_out[static_cast<int64_t>(a) * p.num_heads * kDv + i] = 0.f;
+      for (int64_t i = threadIdx.x; i < static_cast<int64_t>(e - a) * p.num_heads; i += kThreads)
+        p.lse[(i / (e - a)) * p.total + a + i % (e - a)] = -INFINITY;
+    }
   }
-  const float gs = *p.gs;
+  const float gs = kPartial ? 0.f : *p.gs;  // the partial result is not quantised
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + kSmemQ;
@@ -307,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ph = (nk >> 1) & 1;
           if (!(ok = mbar_wait(&bars.k_empty[s], ph ^ 1, err, &abort_s))) break;
           mbar_expect_tx(&bars.k_full[s], kKBytes);
-          tma_load_4d(sK + s * kKBytes, &tm_k, 0, w.h, w.seq_begin + j * kBN, 0, &bars.k_full[s]);
+          tma_load_4d(sK + s * kKBytes, &tm_k, 0, w.h, w.k_begin + j * kBN, 0, &bars.k_full[s]);
           ++nk;
           if (j == 0) {  // Q of this item, once the previous item's last score product has read it
             if (!(ok = mbar_wait(&bars.q_empty, (nq & 1) ^ 1, err, &abort_s))) break;
@@ -317,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!(ok = mbar_wait(&bars.v_empty[s], ph ^ 1, err, &abort_s))) break;
           mbar_expect_tx(&bars.v_full[s], kVBytes);
-          tma_load_4d(sV + s * kVBytes, &tm_v, 0, w.h, w.seq_begin + j * kBN, 0, &bars.v_full[s]);
+          tma_load_4d(sV + s * kVBytes, &tm_v, 0, w.h, w.k_begin + j * kBN, 0, &bars.v_full[s]);
           ++nv;
         }
         if (!ok) break;
@@ -466,9 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mq[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mq[i] = -INFINITY;
-        if (key0 + kBN - 1 > qi) {  // diagonal block: mask keys after the query
+        // the last visible key: the query itself (causal), or the chunk's last
+        const int lim = (kPartial && p.cu_k != nullptr) ? w.n_k - 1 : qi;
+        if (key0 + kBN - 1 > lim) {  // diagonal (or last) block: mask the keys beyond
 #pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = (key0 + c <= qi) ? x[c] : -INFINITY;
+          for (int c = 0; c < 128; ++c) x[c] = (key0 + c <= lim) ? x[c] : -INFINITY;
         }
 #pragma unroll
         for (int c = 0; c < 128; c += 2) mq[(c >> 1) & 7] = max3(mq[(c >> 1) & 7], x[c], x[c + 1]);
@@ -568,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c0 = a0 * inv_l, c1 = a1 * inv_l;
       const int qi = w.row0 + r;
       const int64_t m = w.seq_begin + qi;
-      uint8_t* code_row = p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + w.h * 64;
+      uint8_t* code_row = kPartial ? nullptr : p.codes + m * (static_cast<int64_t>(p.num_heads) * 64) + w.h * 64;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t sbits = 0;
@@ -595,7 +632,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ov[i] = c1 > 0.f ? fmaf(c1, __uint_as_float(u0[i]), y0) : y0;
             ov[16 + i] = c1 > 0.f ? fmaf(c1, __uint_as_float(u1[i]), y1) : y1;
           }
-          if (qi < w.n) {
+          if constexpr (kPartial) {
+            if (qi < w.n) {  // the normalised fp32 row, 32 features
+              float4* dst = reinterpret_cast<float4*>(p.o_out + (m * p.num_heads + w.h) * kDv + col);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+            }
+          } else if (qi < w.n) {
             uint32_t wd[4];
             uint32_t sb[2];
 #pragma unroll
@@ -609,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sbits |= (sb[0] | (sb[1] << 8)) << (16 * qq);
           }
         }
-        if (qi < w.n) {
+        if (!kPartial && qi < w.n) {
           const int64_t kc = static_cast<int64_t>(w.h) * 8 + 4 * half;
           *reinterpret_cast<uint32_t*>(p.scales + sf_offset(m, kc, k_tiles_sf)) = sbits;
         }
@@ -617,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qi < w.n) {
         if (p.lse != nullptr)
           p.lse[static_cast<int64_t>(w.h) * p.total + m] = l_tot > 0.f ? (m_row + log2f(l_tot)) * kLn2 : -INFINITY;
-        if (!gs_ok && qi == 0) flag_error(err, MLA_DEVERR_SCALE);
+        if (!kPartial && !gs_ok && qi == 0) flag_error(err, MLA_DEVERR_SCALE);
       }
     }
   }
@@ -706,10 +749,12 @@ int sched_counter(uint32_t** out) {
 }  // namespace
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms) {
+  const bool partial = a.o_out != nullptr;
+  const int64_t total_k = a.cu_seqlens_k != nullptr ? a.total_k : a.total_tokens;
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, a.q, kDqk, a.num_heads, a.total_tokens, a.q_st, a.q_sh) ||
-      !make_map(&tk, a.k, kDqk, a.num_heads, a.total_tokens, a.k_st, a.k_sh) ||
-      !make_map(&tv, a.v, kDv, a.num_heads, a.total_tokens, a.v_st, a.v_sh))
+      !make_map(&tk, a.k, kDqk, a.num_heads, total_k, a.k_st, a.k_sh) ||
+      !make_map(&tv, a.v, kDv, a.num_heads, total_k, a.v_st, a.v_sh))
     return MLA_ERR_LAUNCH;
   Params p;
   p.cu = a.cu_seqlens;
@@ -727,12 +772,19 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms) {
   p.scales = a.out_scales;
   p.lse = a.lse;
   p.error_word = a.error_word;
-  if (const int st = smem_limit_once(reinterpret_cast<const void*>(prefill_tc_kernel), static_cast<int>(kSmemAlloc), 0))
-    return st;
+  p.o_out = a.o_out;
+  p.cu_k = a.cu_seqlens_k;
+  p.total_k = total_k;
+  const void* kern = partial ? reinterpret_cast<const void*>(prefill_tc_kernel<true>)
+                             : reinterpret_cast<const void*>(prefill_tc_kernel<false>);
+  if (const int st = smem_limit_once(kern, static_cast<int>(kSmemAlloc), partial ? 3 : 0)) return st;
   if (p.num_items == 0) return MLA_OK;
   // persistent: one CTA per SM
   const int grid = p.num_items < static_cast<uint32_t>(num_sms) ? static_cast<int>(p.num_items) : num_sms;
-  prefill_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
+  if (partial)
+    prefill_tc_kernel<true><<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
+  else
+    prefill_tc_kernel<false><<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
   return launch_status();
 }
 

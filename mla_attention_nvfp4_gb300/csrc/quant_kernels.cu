@@ -151,6 +151,183 @@ int launch_cache_write(const void* kv_c, int64_t kv_stride, const void* k_pe, in
 }
 
 // ---------------------------------------------------------------------------
+// Gather of a cached context chunk: the records of the given slots read back
+// as bf16 latent (x_hat = e2m1 * e4m3 * gs, rounded once to bf16) and k_pe.
+// One warp per token; lane l dequantises latent block l (16 features, its 8
+// code bytes and scale byte) and writes 32 bytes, the warp a 1 KB row.
+// Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for MLA ..." -
+// #2244, second commit message (cached-context prefill chunks gather from
+// the quantised paged cache).
+// ---------------------------------------------------------------------------
+
+// bf16 nearest (ties to even) to the exact product a * b (a with at most 8
+// significant bits, b any float32): hi = a * b rounded to float32, lo its
+// exact error (one fma); only when hi sits exactly halfway between two bf16
+// values does lo decide the direction.
+__device__ __forceinline__ uint32_t bf16_of_product(float a, float b) {
+  const float hi = __fmul_rn(a, b);
+  const float lo = __fmaf_rn(a, b, -hi);
+  const uint32_t u = __float_as_uint(hi);
+  if ((u & 0xFFFFu) == 0x8000u && lo != 0.f) return ((lo > 0.f) == (hi > 0.f)) ? (u >> 16) + 1u : (u >> 16);
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+template <bool kFp8Rope>
+__global__ void __launch_bounds__(256) gather_latent_kernel(const uint8_t* __restrict__ cache, int64_t num_slots,
+                                                            const float* __restrict__ gs_ptr,
+                                                            const int64_t* __restrict__ slots, int64_t n,
+                                                            __nv_bfloat16* __restrict__ kv_c,
+                                                            __nv_bfloat16* __restrict__ k_pe, uint32_t* error_word) {
+  constexpr int kRecord = kFp8Rope ? 368 : 432;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const float gs = *gs_ptr;
+  if (!scale_ok(gs) && warp == 0 && lane == 0) flag_error(error_word, MLA_DEVERR_SCALE);
+  for (int64_t t = warp; t < n; t += n_warps) {
+    const int64_t slot = slots[t];
+    const bool ok = slot >= 0 && slot < num_slots;
+    if (slot >= num_slots && lane == 0) flag_error(error_word, MLA_DEVERR_BOUNDS);
+    uint4 out0 = make_uint4(0, 0, 0, 0), out1 = out0, rope = out0;
+    if (ok) {
+      const uint8_t* rec = cache + slot * kRecord;
+      const uint2 codes = *reinterpret_cast<const uint2*>(rec + 8 * lane);
+      const float s = e4m3_to_f32(rec[256 + lane]);
+      uint32_t w[8];
+      const uint32_t cw[2] = {codes.x, codes.y};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // features 2i, 2i+1 of the block: one code byte
+        const uint32_t byte = (cw[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+        uint32_t h2;
+        asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
+        const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+        const float c0 = __low2float(hv) * s, c1 = __high2float(hv) * s;  // exact: <= 7 significant bits
+        w[i] = bf16_of_product(c0, gs) | (bf16_of_product(c1, gs) << 16);
+      }
+      out0 = make_uint4(w[0], w[1], w[2], w[3]);
+      out1 = make_uint4(w[4], w[5], w[6], w[7]);
+      if (lane < 8) {
+        if constexpr (kFp8Rope) {  // 8 e4m3 values -> bf16 (exact)
+          const uint2 e = *reinterpret_cast<const uint2*>(rec + 288 + 8 * lane);
+          const uint32_t ew[2] = {e.x, e.y};
+          uint32_t r[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t two = (ew[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+            const uint32_t hf = e4m3x2_to_f16x2_pair(two);
+            const __half2 hv = *reinterpret_cast<const __half2*>(&hf);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__low2float(hv), __high2float(hv));
+            r[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          rope = make_uint4(r[0], r[1], r[2], r[3]);
+        } else {
+          rope = *reinterpret_cast<const uint4*>(rec + 288 + 16 * lane);
+        }
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(kv_c + t * 512 + 16 * lane);
+    dst[0] = out0;
+    dst[1] = out1;
+    if (lane < 8) reinterpret_cast<uint4*>(k_pe + t * 64)[lane] = rope;
+  }
+}
+
+int launch_gather_latent(const uint8_t* cache, int64_t num_slots, int record_bytes, const float* gs,
+                         const int64_t* slots, int64_t n, void* kv_c, void* k_pe, uint32_t* error_word,
+                         cudaStream_t stream, int num_sms) {
+  if (n == 0) return MLA_OK;
+  const int64_t want = (n + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  auto kv = static_cast<__nv_bfloat16*>(kv_c);
+  auto pe = static_cast<__nv_bfloat16*>(k_pe);
+  if (record_bytes == 368)
+    gather_latent_kernel<true><<<grid, 256, 0, stream>>>(cache, num_slots, gs, slots, n, kv, pe, error_word);
+  else
+    gather_latent_kernel<false><<<grid, 256, 0, stream>>>(cache, num_slots, gs, slots, n, kv, pe, error_word);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Merge of partial prefill results (e.g. a context chunk's and the new
+// tokens' causal attention) by their natural-log LSE, written as the fused
+// NVFP4 output: O = sum_i exp(lse_i - LSE) O_i (each O_i normalised), then
+// the prefill epilogue's quantiser, codes at [t, h*64 + d/2] and the scales
+// 128x4-swizzled; LSE = ln sum_i exp(lse_i).  Thread = one block of 16
+// features of one (token, head); padding rows of the scale buffer get zeros.
+// Source: "#2244", first commit message (natural-log LSE for chunked-context
+// merging); "feat: MLA prefill NVFP4 fused output - #8" (the fused output).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) merge_fused_out_kernel(const float* __restrict__ o_parts,
+                                                              const float* __restrict__ lse_parts, int parts,
+                                                              int64_t T, int H, const float* __restrict__ gs_ptr,
+                                                              uint8_t* __restrict__ codes,
+                                                              uint8_t* __restrict__ scales, float* __restrict__ lse,
+                                                              uint32_t* error_word) {
+  const int64_t K = static_cast<int64_t>(H) * 8;  // scale columns
+  const int64_t Kp = (K + 3) & ~int64_t(3);
+  const int64_t Tp = (T + 127) & ~int64_t(127);
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= Tp * Kp) return;
+  const int64_t t = idx / Kp, kc = idx % Kp;
+  const float gs = *gs_ptr;
+  const bool gs_valid = scale_ok(gs);
+  if (!gs_valid && idx == 0) flag_error(error_word, MLA_DEVERR_SCALE);
+  uint32_t sb = 0;
+  if (t < T && kc < K) {
+    const int h = static_cast<int>(kc >> 3), blk = static_cast<int>(kc & 7);
+    float m = -INFINITY;
+    for (int i = 0; i < parts; ++i) m = fmaxf(m, lse_parts[(static_cast<int64_t>(i) * H + h) * T + t]);
+    float v[16], tot = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+    if (m != -INFINITY) {
+      for (int i = 0; i < parts; ++i) {
+        const float l = lse_parts[(static_cast<int64_t>(i) * H + h) * T + t];
+        if (l == -INFINITY) continue;
+        const float wgt = expf(l - m);
+        tot += wgt;
+        const float4* src = reinterpret_cast<const float4*>(o_parts + ((static_cast<int64_t>(i) * T + t) * H + h) * 128 + 16 * blk);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = src[q];
+          v[4 * q] = fmaf(wgt, f.x, v[4 * q]);
+          v[4 * q + 1] = fmaf(wgt, f.y, v[4 * q + 1]);
+          v[4 * q + 2] = fmaf(wgt, f.z, v[4 * q + 2]);
+          v[4 * q + 3] = fmaf(wgt, f.w, v[4 * q + 3]);
+        }
+      }
+    }
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] *= inv;
+    uint32_t lo = 0, hi = 0;
+    if (gs_valid) {
+      float R;
+      sb = block_scale(fmaxf(amax8(v), amax8(v + 8)), scale_factor(gs), gs, R);
+      lo = encode8(v, R);
+      hi = encode8(v + 8, R);
+    }
+    *reinterpret_cast<uint2*>(codes + t * (K * 8) + kc * 8) = make_uint2(lo, hi);
+    if (lse != nullptr && blk == 0) lse[static_cast<int64_t>(h) * T + t] = tot > 0.f ? m + logf(tot) : -INFINITY;
+  }
+  scales[sf_offset(t, kc, Kp / 4)] = static_cast<uint8_t>(sb);
+}
+
+int launch_merge_fused_out(const float* o_parts, const float* lse_parts, int parts, int64_t T, int H,
+                           const float* gs, uint8_t* codes, uint8_t* scales, float* lse, uint32_t* error_word,
+                           cudaStream_t stream) {
+  const int64_t Kp = (static_cast<int64_t>(H) * 8 + 3) / 4 * 4;
+  const int64_t n = (T + 127) / 128 * 128 * Kp;
+  if (n == 0) return MLA_OK;
+  const int64_t grid = (n + 255) / 256;
+  if (grid > 0x7FFFFFFF) return MLA_ERR_INVALID_ARG;
+  merge_fused_out_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(o_parts, lse_parts, parts, T, H, gs, codes,
+                                                                          scales, lse, error_word);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
 // Quantise rows (fp32 [M, N] -> packed codes + swizzled scales).  One thread
 // per scale slot of the padded [Mp, Kp] scale matrix: real slots quantise a
 // block of 16, padding slots write a zero scale byte.

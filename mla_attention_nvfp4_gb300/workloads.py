@@ -21,6 +21,10 @@ Named workloads (all seeded, default seed 0):
                    replaced by -1; the global slot of (b, t) is b * 65536 + t.
   prefill_8x4096   8 sequences x 4096 tokens, 128 heads, q/k head dim 192,
                    v head dim 128, all ~N(0,1) bf16.
+  prefill_context  new tokens after a cached context: per sequence a chunk
+                   of context keys / values (k_ctx [Tc, H, 192], v_ctx
+                   [Tc, H, 128], ~N(0,1) bf16, rows cu_ctx[s]..cu_ctx[s+1])
+                   besides the new tokens' q / k / v.
 """
 from __future__ import annotations
 
@@ -74,6 +78,9 @@ class PrefillWorkload:
     cu_seqlens: torch.Tensor  # [S+1] int32
     max_seqlen: int
     softmax_scale: float = 1.0 / math.sqrt(192.0)
+    k_ctx: Optional[torch.Tensor] = None  # [Tc, H, 192] bf16 (context chunk keys)
+    v_ctx: Optional[torch.Tensor] = None  # [Tc, H, 128] bf16
+    cu_ctx: Optional[torch.Tensor] = None  # [S+1] int32
 
     @property
     def total_tokens(self) -> int:
@@ -190,3 +197,15 @@ def prefill(name="prefill_8x4096", seq_lens=(4096,) * 8, heads=128, d_qk=192, d_
 
 def prefill_8x4096(seed=0, device="cpu") -> PrefillWorkload:
     return prefill(seed=seed, device=device)
+
+
+def prefill_context(seq_lens, ctx_lens, heads=16, seed=0, device="cpu") -> PrefillWorkload:
+    w = prefill("prefill_context", seq_lens=seq_lens, heads=heads, seed=seed, device=device)
+    g = _gen(seed + 7, device)
+    Tc = int(sum(ctx_lens))
+    w.k_ctx = _randn_bf16((Tc, heads, 192), g, device)
+    w.v_ctx = _randn_bf16((Tc, heads, 128), g, device)
+    cc = torch.zeros(len(ctx_lens) + 1, dtype=torch.int32)
+    cc[1:] = torch.cumsum(torch.tensor(ctx_lens, dtype=torch.int32), 0)
+    w.cu_ctx = cc.to(device)
+    return w
