@@ -32,6 +32,9 @@ Modules:
   cache      the 432 / 368 byte cache record.
   attention  absorbed decode (paged and top-k), LSE merge, causal prefill.
   swizzle    the 128x4 scale-factor layout and the fused prefill output.
+  gemm       the NVFP4 x NVFP4 product of packed codes and swizzled scales.
+  fakequant  the causal prefill with NVFP4 fake-quantised Q, K, P, V and
+             2:4 score sparsity.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, hand-worked examples, library routines (torch's
