@@ -399,6 +399,53 @@ int mla_nvfp4_merge_fused_out(const float* o_parts, const float* lse_parts, int 
                               float* lse, uint32_t* error_word, void* stream);
 
 /*
+ * Prefill with fake-quantised operands (an accuracy-study mode), in two
+ * calls.  Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for
+ * MLA (vLLM TRITON_MLA) - #2244", first commit message (mla_prefill: fused
+ * Q/K/P/V fake quant, token-exact N:M score sparsity) and PR description
+ * ("What does this PR do?": the projected Q/K/P/V operands quantised once,
+ * optional 2:4 score sparsity on new-token attention; "Contract notes":
+ * NVFP4 1x16 along the contraction axis, e4m3 block scale, amax/(6*448),
+ * the softmax denominator unquantised).
+ *
+ * mla_nvfp4_prefill_qdq: each operand quantised to NVFP4 once along the axis
+ * its product contracts, and written as the exact f16 value code * e4m3
+ * scale (the global scale left out):
+ *   q, k : bf16 [T, H, 192] (strides as in mla_nvfp4_prefill_fused_out), in
+ *          blocks of 16 features of a (token, head) row, scales *gs_q / *gs_k;
+ *   v    : bf16 [T, H, 128], in blocks of 16 tokens of a (head, feature)
+ *          column counted from each sequence's first token (cu_seqlens), the
+ *          last block of a sequence ragged, scale *gs_v;
+ *   q_out, k_out : f16 [T, H, 192] contiguous;  v_out : f16 [T, H, 128].
+ * The quotients are rounded exactly as the definition's float32 divisions.
+ * Global scales are amax/(6*448) of each tensor (mla_nvfp4_global_scale).
+ */
+int mla_nvfp4_prefill_qdq(const void* q, const void* k, const void* v, int64_t q_stride_t, int64_t q_stride_h,
+                          int64_t k_stride_t, int64_t k_stride_h, int64_t v_stride_t, int64_t v_stride_h,
+                          const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int max_seqlen,
+                          int num_heads, const float* gs_q, const float* gs_k, const float* gs_v, void* q_out,
+                          void* k_out, void* v_out, uint32_t* error_word, void* stream);
+
+/*
+ * mla_nvfp4_prefill_fakequant: the causal varlen prefill of
+ * mla_nvfp4_prefill_fused_out over the outputs of mla_nvfp4_prefill_qdq
+ * (contiguous f16 q [T,H,192], k [T,H,192], v [T,H,128]) with their global
+ * scales, and P quantised to NVFP4 in blocks of 16 keys (counted from the
+ * sequence's first key) before P.V, relative to the power-of-two reference
+ * 2^ceil(row max, log2 units) so that P <= 1 and gs_p = 1/2688; the row sum
+ * takes the unquantised P.  sparse24 = 1: in each group of 4 keys (same
+ * alignment) each query keeps its 2 largest scores (equal scores: the lower
+ * key first) and drops the rest from numerator and denominator; keys hidden
+ * by the causal mask count as dropped.  The output is written as by
+ * mla_nvfp4_prefill_fused_out (codes, swizzled scales, optional LSE).
+ */
+int mla_nvfp4_prefill_fakequant(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int num_seqs,
+                                int64_t total_tokens, int max_seqlen, int num_heads, float softmax_scale,
+                                const float* gs_q, const float* gs_k, const float* gs_v, int sparse24,
+                                const float* global_scale, uint8_t* out_codes, uint8_t* out_scales, float* lse,
+                                uint32_t* error_word, void* stream);
+
+/*
  * NVFP4 x NVFP4 GEMM on block-scaled tensor cores, reading the fused
  * prefill output as written (the attention output projection, o_proj):
  *     out[m, n] = gs_a * gs_w * sum_k a_hat[m, k] * w_hat[n, k]   (bf16)

@@ -22,7 +22,8 @@ __all__ = [
     "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode_default_splits", "decode_launches",
     "mla_nvfp4_decode", "mla_nvfp4_decode_q4", "mla_nvfp4_prefill_fused_out",
     "mla_nvfp4_quantize_rows", "mla_nvfp4_gemm", "mla_nvfp4_gather_latent", "mla_nvfp4_prefill_partial",
-    "mla_nvfp4_merge_fused_out", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
+    "mla_nvfp4_merge_fused_out", "mla_nvfp4_prefill_qdq", "mla_nvfp4_prefill_fakequant",
+    "mla_nvfp4_prefill_quantized", "abi_symbols", "RECORD_BF16_ROPE", "RECORD_FP8_ROPE",
     "LAUNCHES_PER_CALL",
 ]
 
@@ -35,7 +36,8 @@ DEVERR_BOUNDS, DEVERR_TIMEOUT, DEVERR_SCALE, DEVERR_RANGE = 0x1, 0x2, 0x4, 0x8
 # uniform splits and three (plan, decode, merge) when planned, see
 # decode_launches().
 LAUNCHES_PER_CALL = {"cache_write": 1, "decode": 3, "prefill": 1, "global_scale": 2, "gemm": 1,
-                     "gather_latent": 1, "prefill_partial": 1, "merge_fused_out": 1}
+                     "gather_latent": 1, "prefill_partial": 1, "merge_fused_out": 1, "prefill_qdq": 2,
+                     "prefill_fakequant": 1}
 # What bounds each hot kernel as built: "hbm", "tensor" (tcgen05 MMA) or
 # "alu" (CUDA-core arithmetic).
 KERNEL_BOUND = {"cache_write": "hbm", "decode": "tensor", "prefill": "tensor", "gemm": "tensor"}
@@ -87,6 +89,11 @@ _SIGS = {
                                            _c_vp, _c_vp, _c_vp]),
     "mla_nvfp4_merge_fused_out": (_c_int, [_c_vp, _c_vp, _c_int, _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp,
                                            _c_vp, _c_vp]),
+    "mla_nvfp4_prefill_qdq": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp,
+                                       _c_int, _c_i64, _c_int, _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                       _c_vp, _c_vp]),
+    "mla_nvfp4_prefill_fakequant": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_int, _c_int, _c_f,
+                                             _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_nvfp4_gemm": (_c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64,
                                 _c_vp, _c_vp]),
     "mla_nvfp4_selftest_wait": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp]),
@@ -542,3 +549,73 @@ def mla_nvfp4_merge_fused_out(o_parts, lse_parts, global_scale, *, out_codes=Non
             _ptr(o_parts), _ptr(lse_parts), P, T, H, _ptr(global_scale), _ptr(out_codes), _ptr(out_scales),
             _ptr(lse), _ptr(error_word), _stream(o_parts)))
     return out_codes, out_scales
+
+
+def mla_nvfp4_prefill_qdq(q, k, v, cu_seqlens, max_seqlen, gs_q, gs_k, gs_v, *, error_word=None):
+    """NVFP4 fake quantisation of the prefill operands along their
+    contraction axes: (q_cs f16 [T,H,192], k_cs f16 [T,H,192], v_cs f16
+    [T,H,128]) holding code * e4m3 scale (global scales left out)."""
+    dev = q.device
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, dev)
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError(f"{n} must be [T, H, D] with a contiguous last dimension")
+    for t, n in ((gs_q, "gs_q"), (gs_k, "gs_k"), (gs_v, "gs_v")):
+        _need(t, n, torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    T, H, _ = q.shape
+    if q.shape[2] != 192 or k.shape != (T, H, 192) or v.shape != (T, H, 128):
+        raise ValueError("expected q, k [T,H,192] and v [T,H,128]")
+    q_out = torch.empty((T, H, 192), dtype=torch.float16, device=dev)
+    k_out = torch.empty((T, H, 192), dtype=torch.float16, device=dev)
+    v_out = torch.empty((T, H, 128), dtype=torch.float16, device=dev)
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_prefill_qdq", load_library().mla_nvfp4_prefill_qdq(
+            _ptr(q), _ptr(k), _ptr(v), q.stride(0), q.stride(1), k.stride(0), k.stride(1), v.stride(0), v.stride(1),
+            _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), H, _ptr(gs_q), _ptr(gs_k), _ptr(gs_v),
+            _ptr(q_out), _ptr(k_out), _ptr(v_out), _ptr(error_word), _stream(q)))
+    return q_out, k_out, v_out
+
+
+def mla_nvfp4_prefill_fakequant(q_cs, k_cs, v_cs, cu_seqlens, max_seqlen, softmax_scale, gs_q, gs_k, gs_v,
+                                global_scale, *, sparse24=False, out_codes=None, out_scales=None,
+                                return_lse=False, lse=None, error_word=None):
+    """Causal prefill over fake-quantised operands (mla_nvfp4_prefill_qdq's
+    outputs), P quantised to NVFP4, optional 2:4 score sparsity; the output
+    as mla_nvfp4_prefill_fused_out writes it."""
+    dev = q_cs.device
+    for t, n in ((q_cs, "q_cs"), (k_cs, "k_cs"), (v_cs, "v_cs")):
+        _need(t, n, torch.float16, dev)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((gs_q, "gs_q"), (gs_k, "gs_k"), (gs_v, "gs_v"), (global_scale, "global_scale")):
+        _need(t, n, torch.float32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(error_word, "error_word", torch.int32, dev)
+    T, H, _ = q_cs.shape
+    if q_cs.shape[2] != 192 or k_cs.shape != (T, H, 192) or v_cs.shape != (T, H, 128):
+        raise ValueError("expected q_cs, k_cs [T,H,192] and v_cs [T,H,128]")
+    if out_codes is None:
+        out_codes = torch.empty((T, H * 64), dtype=torch.uint8, device=dev)
+    if out_scales is None:
+        out_scales = torch.empty(prefill_scale_bytes(T, H), dtype=torch.uint8, device=dev)
+    if return_lse and lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check("mla_nvfp4_prefill_fakequant", load_library().mla_nvfp4_prefill_fakequant(
+            _ptr(q_cs), _ptr(k_cs), _ptr(v_cs), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), H,
+            float(softmax_scale), _ptr(gs_q), _ptr(gs_k), _ptr(gs_v), 1 if sparse24 else 0, _ptr(global_scale),
+            _ptr(out_codes), _ptr(out_scales), _ptr(lse), _ptr(error_word), _stream(q_cs)))
+    return (out_codes, out_scales, lse) if return_lse else (out_codes, out_scales)
+
+
+def mla_nvfp4_prefill_quantized(q, k, v, cu_seqlens, max_seqlen, softmax_scale, global_scale, *, sparse24=False,
+                                return_lse=False, error_word=None):
+    """The fake-quantised prefill end to end: the global scales of q, k, v
+    (amax/2688 each), their NVFP4 fake quantisation, and the prefill with P
+    quantised (and optional 2:4 sparsity) writing the NVFP4 output."""
+    gs = [mla_nvfp4_global_scale(t) for t in (q, k, v)]
+    q_cs, k_cs, v_cs = mla_nvfp4_prefill_qdq(q, k, v, cu_seqlens, max_seqlen, *gs, error_word=error_word)
+    return mla_nvfp4_prefill_fakequant(q_cs, k_cs, v_cs, cu_seqlens, max_seqlen, softmax_scale, *gs, global_scale,
+                                       sparse24=sparse24, return_lse=return_lse, error_word=error_word)

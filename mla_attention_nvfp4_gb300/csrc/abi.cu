@@ -374,6 +374,62 @@ int mla_nvfp4_prefill_partial(const void* q, const void* k, const void* v, int64
   return mla::launch_prefill(a, static_cast<cudaStream_t>(stream), sms);
 }
 
+int mla_nvfp4_prefill_qdq(const void* q, const void* k, const void* v, int64_t q_stride_t, int64_t q_stride_h,
+                          int64_t k_stride_t, int64_t k_stride_h, int64_t v_stride_t, int64_t v_stride_h,
+                          const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens, int max_seqlen,
+                          int num_heads, const float* gs_q, const float* gs_k, const float* gs_v, void* q_out,
+                          void* k_out, void* v_out, uint32_t* error_word, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || num_heads < 1) return MLA_ERR_INVALID_ARG;
+  if (total_tokens == 0 || num_seqs == 0) return total_tokens != 0 ? MLA_ERR_INVALID_ARG : MLA_OK;
+  if (max_seqlen < 1 || total_tokens > (int64_t(1) << 31) - 1) return MLA_ERR_INVALID_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || cu_seqlens == nullptr || gs_q == nullptr ||
+      gs_k == nullptr || gs_v == nullptr || q_out == nullptr || k_out == nullptr || v_out == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (q_stride_h < MLA_D_QK_PREFILL || k_stride_h < MLA_D_QK_PREFILL || v_stride_h < MLA_D_V_PREFILL ||
+      q_stride_t < q_stride_h * (num_heads - 1) + MLA_D_QK_PREFILL ||
+      k_stride_t < k_stride_h * (num_heads - 1) + MLA_D_QK_PREFILL ||
+      v_stride_t < v_stride_h * (num_heads - 1) + MLA_D_V_PREFILL)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_out) || !aligned16(k_out) ||
+      (reinterpret_cast<uintptr_t>(v) & 3u) != 0 || (reinterpret_cast<uintptr_t>(v_out) & 3u) != 0 ||
+      (q_stride_t * 2) % 16 || (q_stride_h * 2) % 16 || (k_stride_t * 2) % 16 || (k_stride_h * 2) % 16 ||
+      (v_stride_t * 2) % 4 || (v_stride_h * 2) % 4)
+    return MLA_ERR_ALIGNMENT;
+  mla::QdqArgs a{q, k, v, q_stride_t, q_stride_h, k_stride_t, k_stride_h, v_stride_t, v_stride_h, cu_seqlens,
+                 num_seqs, total_tokens, max_seqlen, num_heads, gs_q, gs_k, gs_v, q_out, k_out, v_out, error_word};
+  return mla::launch_qdq_operands(a, static_cast<cudaStream_t>(stream));
+}
+
+int mla_nvfp4_prefill_fakequant(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int num_seqs,
+                                int64_t total_tokens, int max_seqlen, int num_heads, float softmax_scale,
+                                const float* gs_q, const float* gs_k, const float* gs_v, int sparse24,
+                                const float* global_scale, uint8_t* out_codes, uint8_t* out_scales, float* lse,
+                                uint32_t* error_word, void* stream) {
+  if (gs_q == nullptr || gs_k == nullptr || gs_v == nullptr || (sparse24 != 0 && sparse24 != 1))
+    return MLA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || num_heads < 1) return MLA_ERR_INVALID_ARG;
+  if (total_tokens == 0 || num_seqs == 0) return total_tokens != 0 ? MLA_ERR_INVALID_ARG : MLA_OK;
+  if (max_seqlen < 1 || total_tokens > (int64_t(1) << 31) - 1) return MLA_ERR_INVALID_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || cu_seqlens == nullptr || global_scale == nullptr ||
+      out_codes == nullptr || out_scales == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !(softmax_scale < 3.0e38f)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_codes) ||
+      (reinterpret_cast<uintptr_t>(out_scales) & 3u) != 0)
+    return MLA_ERR_ALIGNMENT;
+  const int sms = device_sms();
+  if (sms < 0) return -sms;
+  const int64_t H = num_heads;
+  mla::PrefillArgs a{q, k, v, H * MLA_D_QK_PREFILL, MLA_D_QK_PREFILL, H * MLA_D_QK_PREFILL, MLA_D_QK_PREFILL,
+                     H * MLA_D_V_PREFILL, MLA_D_V_PREFILL, cu_seqlens, num_seqs, total_tokens, max_seqlen, num_heads,
+                     softmax_scale, global_scale, out_codes, out_scales, lse, error_word};
+  a.gs_q = gs_q;
+  a.gs_k = gs_k;
+  a.gs_v = gs_v;
+  a.sparse24 = sparse24;
+  return mla::launch_prefill(a, static_cast<cudaStream_t>(stream), sms);
+}
+
 int mla_nvfp4_merge_fused_out(const float* o_parts, const float* lse_parts, int num_parts, int64_t total_tokens,
                               int num_heads, const float* global_scale, uint8_t* out_codes, uint8_t* out_scales,
                               float* lse, uint32_t* error_word, void* stream) {

@@ -107,9 +107,37 @@ struct PrefillArgs {
   float* o_out = nullptr;
   const int32_t* cu_seqlens_k = nullptr;
   int64_t total_k = 0;
+  // fake-quant mode (gs_q set): q, k, v hold the f16 code * scale values of
+  // NVFP4 operands (launch_qdq_operands) with these global scales; P is
+  // quantised to NVFP4 along the keys, optionally after 2:4 score sparsity
+  const float* gs_q = nullptr;
+  const float* gs_k = nullptr;
+  const float* gs_v = nullptr;
+  int sparse24 = 0;
 };
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms);
+
+// NVFP4 fake quantisation of the prefill operands (code * scale as f16).
+struct QdqArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
+  const int32_t* cu_seqlens;
+  int num_seqs;
+  int64_t total;
+  int max_seqlen;
+  int num_heads;
+  const float* gs_q;
+  const float* gs_k;
+  const float* gs_v;
+  void* q_out;  // f16 [total, H, 192]
+  void* k_out;  // f16 [total, H, 192]
+  void* v_out;  // f16 [total, H, 128]
+  uint32_t* error_word;
+};
+int launch_qdq_operands(const QdqArgs& a, cudaStream_t stream);
 
 struct GemmArgs {
   const uint8_t* a_codes;

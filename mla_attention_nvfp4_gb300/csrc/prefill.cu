@@ -91,6 +91,12 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
+// fake-quant mode: every operand is an exact f16 value code * scale
+constexpr uint32_t kIdescS16 = idesc_f16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV16 = idesc_f16_f32(128, 128, false, true);
+// P's global scale in fake-quant mode: amax/(6*448) with amax = 1 (P <= 1
+// relative to its power-of-two reference)
+constexpr float kGsP = 1.0f / 2688.0f;
 
 struct Params {
   const int32_t* cu;
@@ -114,7 +120,18 @@ struct Params {
   float* o_out;
   const int32_t* cu_k;
   int64_t total_k;
+  // fake-quant mode (kQuant): global scales of the NVFP4 operands whose
+  // code * scale values q, k, v hold, and 2:4 score sparsity on or off
+  const float* gs_q;
+  const float* gs_k;
+  const float* gs_v;
+  int sparse24;
 };
+
+// 2^d for an integer-valued d <= 0 (exact; 0 below the normal range).
+__device__ __forceinline__ float exp2_int(float d) {
+  return d < -126.f ? 0.f : __int_as_float((127 + static_cast<int>(d)) << 23);
+}
 
 constexpr int kRing = 4;  // item indices in flight from the producer to the other roles
 
@@ -237,7 +254,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, abort));
 }
 
-template <bool kPartial>
+template <bool kPartial, bool kQuant>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, Params p) {
@@ -409,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kDqk / 64; ++c) {
             const uint64_t a = dq + c * (16384 >> 4), bdesc = dk + c * (16384 >> 4);
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) mma_ss(sd, a + k4 * 2, bdesc + k4 * 2, kIdescS, (c | k4) != 0 ? 1u : 0u);
+            for (int k4 = 0; k4 < 4; ++k4)
+              mma_ss(sd, a + k4 * 2, bdesc + k4 * 2, kQuant ? kIdescS16 : kIdescS, (c | k4) != 0 ? 1u : 0u);
           }
           mma_commit(&bars.s_full[w]);
           mma_commit(&bars.k_empty[s]);
@@ -430,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = dv + h * ((4 * 2048) >> 4);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4)
-              mma_ts(od, sd + (4 * h + k4) * 8, bdesc + k4 * (2048 >> 4), kIdescPV, (first & (h == 0) & (k4 == 0)) ? 0u : 1u);
+              mma_ts(od, sd + (4 * h + k4) * 8, bdesc + k4 * (2048 >> 4), kQuant ? kIdescPV16 : kIdescPV,
+                     (first & (h == 0) & (k4 == 0)) ? 0u : 1u);
           }
           mma_commit(&bars.v_empty[s]);
           if (j == j_last) mma_commit(&bars.o_full);
@@ -467,6 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t my_s = wg ? tS[1] : tS[0];
     const uint32_t my_o = wg ? tO[1] : tO[0];
+    // fake-quant mode: the scores are products of code * scale values, so
+    // the global scales of Q and K join the softmax scale
+    const float sl2 = kQuant ? p.scale_log2 * *p.gs_q * *p.gs_k : p.scale_log2;
+    const bool sparse = kQuant && p.sparse24 != 0;
+    const float kf_p = scale_factor(kGsP);
     int gb = 0, cw = 0;  // global block counter; blocks of this warpgroup
     bool ok = true;
     for (int it = 0; ok; ++it) {
@@ -511,13 +535,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; c += 2) mq[(c >> 1) & 7] = max3(mq[(c >> 1) & 7], x[c], x[c + 1]);
         const float mx =
             fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7]))) *
-            p.scale_log2;
-        // lazy reference update
+            sl2;
         float m_use = m_run, alpha = 1.f;
-        const bool raise = mx > m_run + kRescaleThreshold;
-        if (raise) {
-          m_use = mx;
-          alpha = ex2_approx(m_run - mx);  // 0 on this warpgroup's first block
+        bool raise;
+        if constexpr (kQuant) {
+          // power-of-two reference: the running max rounded up (log2 units),
+          // raised whenever it grows, so P <= 1 and O rescales exactly
+          const float m_new = ceilf(mx);
+          raise = m_new > m_run;
+          if (raise) {
+            m_use = m_new;
+            alpha = m_run == -INFINITY ? 0.f : exp2_int(m_run - m_new);
+          }
+        } else {
+          // lazy reference update
+          raise = mx > m_run + kRescaleThreshold;
+          if (raise) {
+            m_use = mx;
+            alpha = ex2_approx(m_run - mx);  // 0 on this warpgroup's first block
+          }
         }
         // The partial O holds only this warpgroup's earlier blocks, whose
         // P.V retired before S of this block was committed.
@@ -535,19 +571,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m_run = m_use;
         // exponent arguments two at a time: x * scale_log2 - m_use
-        const uint64_t sc2 = pk2(p.scale_log2, p.scale_log2), nm2 = pk2(-m_use, -m_use);
+        const uint64_t sc2 = pk2(sl2, sl2), nm2 = pk2(-m_use, -m_use);
         uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial row sums
 #pragma unroll
-        for (int c = 0; c < 128; c += 32) {  // P as bf16 pairs: columns [0, 64) of the S buffer
+        for (int c = 0; c < 128; c += 32) {  // P as 16-bit pairs: columns [0, 64) of the S buffer
           uint32_t v[16];
+          if constexpr (kQuant) {
+            // the row sum takes the unquantised P; the P.V operand is P
+            // quantised to NVFP4 in blocks of 16 keys, as code * scale (f16)
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float a0, a1;
-            unpk2(fma2(pk2(x[c + 2 * i], x[c + 2 * i + 1]), sc2, nm2), a0, a1);
-            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-            ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            v[i] = *reinterpret_cast<uint32_t*>(&h2);
+            for (int blk = 0; blk < 2; ++blk) {
+              float pb[16];
+              if (sparse) {
+                // 2:4: of each group of 4 keys (aligned to the sequence's
+                // first key) keep the 2 largest scores, equal scores by lower
+                // key index; a key's rank counts the keys of its group that
+                // beat it.  A group's max is always kept, so the row max
+                // above is the max of the kept scores.
+#pragma unroll
+                for (int g4 = c + 16 * blk; g4 < c + 16 * blk + 16; g4 += 4) {
+                  const float a = x[g4], b = x[g4 + 1], cc = x[g4 + 2], d = x[g4 + 3];
+                  const int ab = a >= b, ac = a >= cc, ad = a >= d, bc = b >= cc, bd = b >= d, cd = cc >= d;
+                  const int ra = 3 - ab - ac - ad, rb = ab + 2 - bc - bd, rc = ac + bc + 1 - cd, rd = ad + bd + cd;
+                  x[g4] = ra < 2 ? a : -INFINITY;
+                  x[g4 + 1] = rb < 2 ? b : -INFINITY;
+                  x[g4 + 2] = rc < 2 ? cc : -INFINITY;
+                  x[g4 + 3] = rd < 2 ? d : -INFINITY;
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float a0, a1;
+                unpk2(fma2(pk2(x[c + 16 * blk + 2 * i], x[c + 16 * blk + 2 * i + 1]), sc2, nm2), a0, a1);
+                pb[2 * i] = ex2_approx(a0);
+                pb[2 * i + 1] = ex2_approx(a1);
+                ls2[i & 3] = add2(ls2[i & 3], pk2(pb[2 * i], pb[2 * i + 1]));
+              }
+              float R;
+              const uint32_t sb = block_scale(fmaxf(amax8(pb), amax8(pb + 8)), kf_p, kGsP, R);
+              const uint32_t cw2[2] = {encode8(pb, R), encode8(pb + 8, R)};
+              const uint32_t s2 = e4m3x2_to_f16x2_pair(sb | (sb << 8));
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint32_t byte = (cw2[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+                uint32_t h2;
+                asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
+                const __half2 q2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&s2));
+                v[8 * blk + i] = *reinterpret_cast<const uint32_t*>(&q2);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float a0, a1;
+              unpk2(fma2(pk2(x[c + 2 * i], x[c + 2 * i + 1]), sc2, nm2), a0, a1);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+              ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+              v[i] = *reinterpret_cast<uint32_t*>(&h2);
+            }
           }
           tmem_st16(my_s + lane_off + c / 2, v);
         }
@@ -583,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool gs_ok = scale_ok(gs);
     const float kf = scale_factor(gs);
+    const float pv_scale = kQuant ? kGsP * *p.gs_v : 1.f;
     for (int it = 0;; ++it) {
       if (!warp_wait(&bars.item_full[it % kRing], (it / kRing) & 1, err, &abort_s)) break;
       const int idx = ring_s[it % kRing];
@@ -598,10 +681,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m0 = m_s[o][0][r], m1 = m_s[o][1][r];
       const float m_row = fmaxf(m0, m1);
       // a partial with no block (l = 0) carries no weight, and its O is not read
-      const float a0 = l0 > 0.f ? ex2_approx(m0 - m_row) : 0.f;
-      const float a1 = l1 > 0.f ? ex2_approx(m1 - m_row) : 0.f;
+      // (fake-quant mode: integer references, exact powers of two; the
+      // global scales of P and V join the normalisation)
+      const float a0 = l0 > 0.f ? (kQuant ? exp2_int(m0 - m_row) : ex2_approx(m0 - m_row)) : 0.f;
+      const float a1 = l1 > 0.f ? (kQuant ? exp2_int(m1 - m_row) : ex2_approx(m1 - m_row)) : 0.f;
       const float l_tot = a0 * l0 + a1 * l1;
-      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const float inv_l = l_tot > 0.f ? pv_scale / l_tot : 0.f;
       const float c0 = a0 * inv_l, c1 = a1 * inv_l;
       const int qi = w.row0 + r;
       const int64_t m = w.seq_begin + qi;
@@ -775,16 +860,25 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms) {
   p.o_out = a.o_out;
   p.cu_k = a.cu_seqlens_k;
   p.total_k = total_k;
-  const void* kern = partial ? reinterpret_cast<const void*>(prefill_tc_kernel<true>)
-                             : reinterpret_cast<const void*>(prefill_tc_kernel<false>);
-  if (const int st = smem_limit_once(kern, static_cast<int>(kSmemAlloc), partial ? 3 : 0)) return st;
+  p.gs_q = a.gs_q;
+  p.gs_k = a.gs_k;
+  p.gs_v = a.gs_v;
+  p.sparse24 = a.sparse24;
+  const bool quant = a.gs_q != nullptr;
+  if (quant && (partial || a.gs_k == nullptr || a.gs_v == nullptr)) return MLA_ERR_INVALID_ARG;
+  const void* kern = partial ? reinterpret_cast<const void*>(prefill_tc_kernel<true, false>)
+                     : quant ? reinterpret_cast<const void*>(prefill_tc_kernel<false, true>)
+                             : reinterpret_cast<const void*>(prefill_tc_kernel<false, false>);
+  if (const int st = smem_limit_once(kern, static_cast<int>(kSmemAlloc), partial ? 3 : quant ? 7 : 0)) return st;
   if (p.num_items == 0) return MLA_OK;
   // persistent: one CTA per SM
   const int grid = p.num_items < static_cast<uint32_t>(num_sms) ? static_cast<int>(p.num_items) : num_sms;
   if (partial)
-    prefill_tc_kernel<true><<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<true, false><<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
+  else if (quant)
+    prefill_tc_kernel<false, true><<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
   else
-    prefill_tc_kernel<false><<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
+    prefill_tc_kernel<false, false><<<grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, p);
   return launch_status();
 }
 

@@ -368,6 +368,132 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restr
   scales[sf_offset(m, k, Kp / 4)] = static_cast<uint8_t>(sb);
 }
 
+// ---------------------------------------------------------------------------
+// Fake quantisation of the prefill operands: each operand quantised once to
+// NVFP4 along the axis its product contracts and written back as the exact
+// f16 value code * e4m3 scale (the global scale left out, applied by the
+// attention to the fp32 results).  Q and K: blocks of 16 of the 192
+// features of a (token, head) row; V: blocks of 16 tokens of a (head,
+// feature) column counted from the sequence's first token, the last block
+// of a sequence ragged.  Correctly rounded quotients (the cache write's
+// quantiser).  code * scale has at most 6 significant bits and lies in
+// [2^-10, 2688], so it is exact in f16.
+// Source: "Add NVFP4/FP8 Q/K/P/V + 2:4 attention quantization for MLA (vLLM
+// TRITON_MLA) - #2244", first commit message (fused Q/K/P/V fake quant in
+// the prefill) and PR description ("Contract notes": NVFP4 1x16 along the
+// contraction axis, e4m3 block scale, amax/(6*448)).
+// ---------------------------------------------------------------------------
+// 16 values -> 8 f16x2 words of code * scale (element 2i low in word i).
+__device__ __forceinline__ void qdq16_f16(const float* x, bool gs_valid, float inv_gs, float gs, uint32_t* w) {
+  uint32_t c0 = 0, c1 = 0, sb = 0;
+  if (gs_valid) {
+    float R, S;
+    bool bounded;
+    sb = block_scale_rn(fmaxf(amax8(x), amax8(x + 8)), inv_gs, gs, R, S, bounded);
+    c0 = encode8_rn(x, R, S, bounded);
+    c1 = encode8_rn(x + 8, R, S, bounded);
+  }
+  const uint32_t s2 = e4m3x2_to_f16x2_pair(sb | (sb << 8));
+  const __half2 sh = *reinterpret_cast<const __half2*>(&s2);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = ((i < 4 ? c0 : c1) >> (8 * (i & 3))) & 0xFFu;
+    uint32_t h2;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
+    const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), sh);
+    w[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
+// Q and K (blockIdx.y selects): thread = one block of 16 features.
+__global__ void __launch_bounds__(256) qdq_features_kernel(const __nv_bfloat16* __restrict__ q, int64_t q_st,
+                                                           int64_t q_sh, const __nv_bfloat16* __restrict__ k,
+                                                           int64_t k_st, int64_t k_sh, int64_t T, int H,
+                                                           const float* __restrict__ gs_q,
+                                                           const float* __restrict__ gs_k, __half* __restrict__ q_out,
+                                                           __half* __restrict__ k_out, uint32_t* error_word) {
+  const bool is_k = blockIdx.y != 0;
+  const __nv_bfloat16* x = is_k ? k : q;
+  const int64_t st = is_k ? k_st : q_st, sh = is_k ? k_sh : q_sh;
+  __half* out = is_k ? k_out : q_out;
+  const float gs = is_k ? *gs_k : *gs_q;
+  const bool gs_valid = scale_ok(gs);
+  const float inv_gs = inv_scale(gs);
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (!gs_valid && idx == 0) flag_error(error_word, MLA_DEVERR_SCALE);
+  if (idx >= T * H * 12) return;
+  const int64_t row = idx / 12, b = idx % 12;
+  const int64_t t = row / H, h = row % H;
+  const uint4* src = reinterpret_cast<const uint4*>(x + t * st + h * sh + 16 * b);
+  float f[16];
+  unpack8_bf16(src[0], f);
+  unpack8_bf16(src[1], f + 8);
+  uint32_t w[8];
+  qdq16_f16(f, gs_valid, inv_gs, gs, w);
+  uint4* dst = reinterpret_cast<uint4*>(out + row * 192 + 16 * b);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// V: CTA = (block of 16 tokens, sequence); thread = two features of one head
+// over the block's tokens.
+__global__ void __launch_bounds__(256) qdq_tokens_kernel(const __nv_bfloat16* __restrict__ v, int64_t v_st,
+                                                         int64_t v_sh, const int32_t* __restrict__ cu, int64_t T,
+                                                         int H, const float* __restrict__ gs_v,
+                                                         __half* __restrict__ v_out, uint32_t* error_word) {
+  const int seq = blockIdx.y;
+  const int a = cu[seq], e = cu[seq + 1];
+  const float gs = *gs_v;
+  const bool gs_valid = scale_ok(gs);
+  const float inv_gs = inv_scale(gs);
+  if (!gs_valid && blockIdx.x == 0 && seq == 0 && threadIdx.x == 0) flag_error(error_word, MLA_DEVERR_SCALE);
+  if (a < 0 || e > T || a > e) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(error_word, MLA_DEVERR_BOUNDS);
+    return;
+  }
+  const int64_t t0 = a + 16 * static_cast<int64_t>(blockIdx.x);
+  const int64_t rem = e - t0;
+  const int n = rem < 16 ? static_cast<int>(rem) : 16;
+  if (n <= 0) return;
+  for (int pr = threadIdx.x; pr < H * 64; pr += blockDim.x) {
+    const int h = pr >> 6, d = 2 * (pr & 63);
+    float c0[16], c1[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint32_t u = 0;
+      if (i < n) u = *reinterpret_cast<const uint32_t*>(v + (t0 + i) * v_st + h * v_sh + d);
+      bf16x2_to_f32(u, c0[i], c1[i]);
+    }
+    uint32_t w0[8], w1[8];
+    qdq16_f16(c0, gs_valid, inv_gs, gs, w0);
+    qdq16_f16(c1, gs_valid, inv_gs, gs, w1);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      // token i: (feature d, feature d+1) from the two columns' halves i
+      const uint32_t pair = __byte_perm(w0[i >> 1], w1[i >> 1], (i & 1) ? 0x7632 : 0x5410);
+      if (i < n) *reinterpret_cast<uint32_t*>(v_out + ((t0 + i) * H + h) * 128 + d) = pair;
+    }
+  }
+}
+
+int launch_qdq_operands(const QdqArgs& a, cudaStream_t stream) {
+  const int64_t blocks = a.total * a.num_heads * 12;
+  if (blocks > 0) {
+    const dim3 grid(static_cast<unsigned>((blocks + 255) / 256), 2);
+    qdq_features_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.q), a.q_st, a.q_sh, static_cast<const __nv_bfloat16*>(a.k), a.k_st,
+        a.k_sh, a.total, a.num_heads, a.gs_q, a.gs_k, static_cast<__half*>(a.q_out), static_cast<__half*>(a.k_out),
+        a.error_word);
+  }
+  if (a.num_seqs > 0 && a.max_seqlen > 0) {
+    const dim3 grid(static_cast<unsigned>((a.max_seqlen + 15) / 16), static_cast<unsigned>(a.num_seqs));
+    qdq_tokens_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(a.v), a.v_st, a.v_sh, a.cu_seqlens,
+                                                a.total, a.num_heads, a.gs_v, static_cast<__half*>(a.v_out),
+                                                a.error_word);
+  }
+  return launch_status();
+}
+
 int launch_quantize_rows(const float* x, int64_t M, int64_t N, const float* gs, uint8_t* codes,
                          uint8_t* scales, uint32_t* error_word, cudaStream_t stream) {
   const int64_t K = N / 16;
