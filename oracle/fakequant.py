@@ -199,7 +199,7 @@ def _allowance(p, s_dense, s_kept, vv, o, l, rel, mids_c, mids_s):
                 continue
             srt = -np.sort(-grp, axis=1)
             fin = np.isfinite(srt[:, 2])
-            gap = np.abs(srt[:, 1] - srt[:, 2])
+            gap = np.abs(srt[:, 1] - np.where(fin, srt[:, 2], 0.0))  # (hidden 3rd key: no tie)
             near = fin & (gap <= rel * (1.0 + np.abs(srt[:, 1])))
             if near.any():
                 w = x[:, g0:g0 + 4] * near[:, None]
