@@ -43,9 +43,17 @@
 //   j+2 may be written while QK_T(j+2) runs, so two buffers of each part
 //   (one per tile parity) suffice.
 //
-// Warp roles (384 threads):
-//   warps 0..3   Q staging, online softmax (thread = head), lazy O rescale,
-//                partial-output epilogue.
+// Warp roles (512 threads):
+//   warps 0..3, 12..15  Q staging, online softmax, lazy O rescale,
+//                partial-output epilogue: two threads per head, warp w
+//                reading TMEM lanes 32 (w % 4)..+32; warps 0..3 take keys
+//                [0, 32) of each tile and O columns [0, 128), warps 12..15
+//                keys [32, 64) and O columns [128, 256).  The pair exchanges
+//                each tile's maximum through shared memory (both then take
+//                the same reference and rescale decisions) and keeps two row
+//                sums, added at the end.  Halving the per-thread softmax
+//                (~3,300 cycles a 64-key tile on one thread per head) was
+//                the kernel's shortest path to a shorter tile.
 //   warps 4, 11  MMA issuers (one thread each) for even and odd tiles;
 //                warp 4 owns the TMEM allocation.
 //   warps 5..10  dequantisation: thread = (key, third of the record), 16-byte
@@ -71,7 +79,9 @@ using namespace sm100;
 
 constexpr int kTok = 64;           // keys per tile (MMA N of the score product)
 constexpr int kHeads = 128;        // heads per work unit (MMA M)
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;    // NVFP4-query kernel: one softmax thread per head
+constexpr int kThreadsTc = 512;  // exact kernel: two softmax threads per head
+constexpr int kSoftWarp2 = 12;   // exact kernel: warps 12..15 take the second half of each tile's keys
 constexpr int kMmaWarp = 4;    // MMA issuer for even tiles, TMEM owner
 constexpr int kMmaWarp2 = 11;  // MMA issuer for odd tiles
 constexpr int kDeqWarp0 = 5;
@@ -138,6 +148,19 @@ __device__ __noinline__ bool bar_wait_poll(uint64_t* bar, uint32_t parity, uint3
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint32_t* error_word, volatile int* abort) {
   return mbar_test(bar, parity) || bar_wait_poll(bar, parity, error_word, abort);
 }
+
+// Exchange between the two softmax threads of a head (exact kernel): one
+// value per half and head row, behind an mbarrier that both halves arrive
+// on: the query maxima of the staging pass (qx), each tile's maxima
+// (mx_full, by tile parity), the row sums at the end (fin).  One slot per
+// half serves all three; a value is overwritten only after the partner has
+// read the previous one (the partner's P of the previous tile is in, or the
+// item's last P.V has retired).
+struct alignas(8) SoftX {
+  uint64_t mx_full[2], fin, qx;
+  float v[2][kHeads];
+};
+static_assert(kSmAlloc + sizeof(SoftX) + 256 <= 232448, "shared memory budget of the exact kernel");
 
 struct alignas(8) Barriers {
   uint64_t q_ready;
@@ -447,51 +470,81 @@ __device__ bool dequant_role(const DeqCtx& c) {
 // padding keys, lazy max raise with an O rescale, probabilities as f16 into
 // the scores' columns for P.V, running row sum.  Shared by both decode
 // kernels.
+//
+// kSplit = 2 (exact kernel): two threads per head, thread `half` taking keys
+// [32 half, 32 half + 32) of each tile and O columns [128 half, 128 half +
+// 128) for the rescale; the halves exchange their tile maxima through `x`
+// (so both take the same reference and the same rescale decisions) and keep
+// separate row sums.  The exchange also orders the halves' score loads
+// before the P stores that overwrite them.
+template <int kSplit>
 __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, volatile int& abort_s, uint32_t tmem,
                                               uint32_t lane_off, int b, int tile0, int nt, int n_keys,
-                                              float score_scale, bool& ok, float& m_run, float& l_run) {
+                                              float score_scale, bool& ok, float& m_run, float& l_run, int half,
+                                              SoftX* x_ch, int hr) {
+  constexpr int kKeys = kTok / kSplit;  // keys of a tile per thread
   uint32_t* err = p.error_word;
   const int lane = threadIdx.x & 31;
-  // per-tile validity: lane checks keys `lane` and `lane + 32`
-  int32_t ia = load_index(p, b, tile0 * kTok + lane), ib = load_index(p, b, tile0 * kTok + 32 + lane);
+  const int kb = half * kKeys;  // first key of this thread's part of a tile
+  // per-tile validity: lane checks keys kb + lane (and kb + lane + 32)
+  int32_t ia = load_index(p, b, tile0 * kTok + kb + lane);
+  int32_t ib = kSplit == 1 ? load_index(p, b, tile0 * kTok + 32 + lane) : 0;
   for (int j = 0; j < nt; ++j) {
     const int pb = j & 1;
-    const int key = (tile0 + j) * kTok + lane;
+    const int key = (tile0 + j) * kTok + kb + lane;
     bool badv = false;
     const unsigned va = __ballot_sync(0xffffffffu, key_slot(p, ia, key, n_keys, badv) >= 0);
-    const unsigned vb = __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0);
+    const unsigned vb = kSplit == 1 ? __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0)
+                                    : 0xffffffffu;
     if (j + 1 < nt) {
       ia = load_index(p, b, key + kTok);
-      ib = load_index(p, b, key + kTok + 32);
+      if (kSplit == 1) ib = load_index(p, b, key + kTok + 32);
     }
     if (!bar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    // raw scores: four loads in flight, one wait
-    float x[kTok];
+    // raw scores: all loads in flight, one wait
+    float x[kKeys];
     {
-      uint32_t v[4][16];
+      uint32_t v[kKeys / 16][16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld16(tmem + lane_off + col_s(pb) + 16 * c, v[c]);
+      for (int c = 0; c < kKeys / 16; ++c) tmem_ld16(tmem + lane_off + col_s(pb) + kb + 16 * c, v[c]);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < kTok; ++c) x[c] = __uint_as_float(v[c >> 4][c & 15]);
+      for (int c = 0; c < kKeys; ++c) x[c] = __uint_as_float(v[c >> 4][c & 15]);
     }
     // max of the raw scores (score_scale > 0), padding keys at -inf; the
     // scale is applied inside the exponent below
     float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if ((va & vb) != 0xffffffffu) {
 #pragma unroll
-      for (int c = 0; c < kTok; ++c) {
+      for (int c = 0; c < kKeys; ++c) {
         const unsigned m = c < 32 ? va : vb;
         x[c] = ((m >> (c & 31)) & 1u) ? x[c] : -INFINITY;
       }
     }
 #pragma unroll
-    for (int c = 0; c < kTok; c += 2) mq[(c >> 1) & 3] = max3(mq[(c >> 1) & 3], x[c], x[c + 1]);
-    const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * score_scale;  // log2 units
+    for (int c = 0; c < kKeys; c += 2) mq[(c >> 1) & 3] = max3(mq[(c >> 1) & 3], x[c], x[c + 1]);
+    float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * score_scale;  // log2 units
+    if constexpr (kSplit == 2) {
+      // the partner has read this slot's previous value once its P of the
+      // previous tile is in
+      if (j > 0 && !bar_wait(&bars.p_full[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s)) {
+        ok = false;
+        break;
+      }
+      x_ch->v[half][hr] = mx;
+      tc_fence_before();
+      mbar_arrive(&x_ch->mx_full[pb]);
+      if (!bar_wait(&x_ch->mx_full[pb], (j >> 1) & 1, err, &abort_s)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      mx = fmaxf(mx, x_ch->v[half ^ 1][hr]);
+    }
     float m_use = m_run, alpha = 1.f;
     const bool raise = mx > m_run + kRescaleThreshold;
     if (raise) {
@@ -509,13 +562,14 @@ __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, v
       }
       tc_fence_after();
 #pragma unroll 4
-      for (int c = 0; c < 256; c += 16) {
+      for (int c = 0; c < 256 / kSplit; c += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem + lane_off + kTO + c, v);
+        const uint32_t col = kTO + half * (256 / kSplit) + c;
+        tmem_ld16(tmem + lane_off + col, v);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tmem_st16(tmem + lane_off + kTO + c, v);
+        tmem_st16(tmem + lane_off + col, v);
       }
       tmem_st_wait();
     }
@@ -524,9 +578,9 @@ __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, v
     // exponent arguments and row sums two at a time
     const uint64_t sc2 = pk2(score_scale, score_scale), nm2 = pk2(-m_ref, -m_ref);
     uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial sums
-    uint32_t pv[kTok / 2];
+    uint32_t pv[kKeys / 2];
 #pragma unroll
-    for (int i = 0; i < kTok / 2; ++i) {
+    for (int i = 0; i < kKeys / 2; ++i) {
       float a0, a1;
       unpk2(fma2(pk2(x[2 * i], x[2 * i + 1]), sc2, nm2), a0, a1);
       const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
@@ -538,15 +592,14 @@ __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, v
     for (int i = 0; i < 4; ++i) unpk2(ls2[i], ls[2 * i], ls[2 * i + 1]);
     l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
     // P(j) over S(j): the buffer's previous P was read by PV(j-2), which
-    // ran before QK(j) wrote S(j)
-    uint32_t v0[16], v1[16];
+    // ran before QK(j) wrote S(j); key pair i of the tile in column i
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      v0[i] = pv[i];
-      v1[i] = pv[16 + i];
+    for (int c = 0; c < kKeys / 32; ++c) {
+      uint32_t v0[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v0[i] = pv[16 * c + i];
+      tmem_st16(tmem + lane_off + col_s(pb) + kb / 2 + 16 * c, v0);
     }
-    tmem_st16(tmem + lane_off + col_s(pb), v0);
-    tmem_st16(tmem + lane_off + col_s(pb) + 16, v1);
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&bars.p_full[pb]);
@@ -557,9 +610,23 @@ __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, v
 // gs, and the LSE, as the final bf16 output when the item is its sequence's
 // only one, else as an fp32 partial row for the merge.  TMEM loads are
 // warp-collective, so every lane loads; only stores depend on the head.
+// kSplit = 2: thread `half` writes O columns [128 half, 128 half + 128) of
+// this CTA's 256 with the row sum of both halves (exchanged through x).
+template <int kSplit>
 __device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, uint32_t lane_off, bool ok, int nt,
                                               float m_run, float l_run, float gs, int64_t row0, int b, int head,
-                                              bool head_ok, bool direct, int rank) {
+                                              bool head_ok, bool direct, int rank, int half, SoftX* x_ch, int hr,
+                                              volatile int* abort_s) {
+  if constexpr (kSplit == 2) {
+    if (nt > 0) {
+      x_ch->v[half][hr] = l_run;
+      mbar_arrive(&x_ch->fin);
+      if (bar_wait(&x_ch->fin, 0, p.error_word, abort_s))
+        l_run += x_ch->v[half ^ 1][hr];
+      else
+        ok = false;
+    }
+  }
   // partial output of this split: O half / l (scaled by gs), lse.  TMEM
   // loads are warp-collective, so every lane loads; only stores depend on
   // the head.
@@ -570,14 +637,16 @@ __device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, ui
   // For a sequence's only item the merge is the identity (weight
   // exp(0) = 1, sum 1): the final bf16 output and the LSE are written here
   // and no merge touches the sequence.
-  float4* dst = reinterpret_cast<float4*>(p.part_o + row * 512 + 256 * rank);
-  uint4* dst_bf = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + head) * 512 + 256 * rank);
+  constexpr int kCols = 256 / kSplit;
+  float4* dst = reinterpret_cast<float4*>(p.part_o + row * 512 + 256 * rank + kCols * half);
+  uint4* dst_bf = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + head) * 512 + 256 * rank +
+                                           kCols * half);
   if (live) tc_fence_after();
 #pragma unroll 2
-  for (int c = 0; c < 256; c += 16) {
+  for (int c = 0; c < kCols; c += 16) {
     uint32_t v[16];
     if (live) {
-      tmem_ld16(tmem + lane_off + kTO + c, v);
+      tmem_ld16(tmem + lane_off + kTO + kCols * half + c, v);
       tmem_ld_wait();
     } else {
 #pragma unroll
@@ -601,7 +670,7 @@ __device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, ui
       }
     }
   }
-  if (head_ok && rank == 0) {
+  if (head_ok && rank == 0 && half == 0) {
     const float l = have ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     if (!direct)
       p.part_lse[row] = l;
@@ -611,9 +680,10 @@ __device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, ui
 }
 
 template <int kRecord>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_tc_kernel(Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
+  __shared__ SoftX xch;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
 
@@ -662,17 +732,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 
   if (threadIdx.x == 0) {
     abort_s = 0;
-    mbar_init(&bars.q_ready, 128);
+    mbar_init(&bars.q_ready, 256);  // both softmax halves stage part of Q
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.t_full[i], 128);
       mbar_init(&bars.t_empty[i], 1);
       mbar_init(&bars.v_full[i], 128);
       mbar_init(&bars.v_empty[i], 1);
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 128);
+      mbar_init(&bars.p_full[i], 256);
+      mbar_init(&xch.mx_full[i], 256);
       mbar_init(&bars.pv_done[i], 1);
     }
     mbar_init(&bars.o_full, 2);
+    mbar_init(&xch.fin, 256);
+    mbar_init(&xch.qx, 256);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -776,10 +849,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     if (bad && rank == 0 && q == 0) flag_error(err, MLA_DEVERR_BOUNDS);
   } else {
     // ------------------------------------------- softmax and epilogue
-    const int hr = warp * 32 + lane;  // head row within the group
+    // warps 0..3 (half 0) and 12..15 (half 1): two threads per head; warp w
+    // reads TMEM lanes 32 (w % 4) .. +32
+    const int half = warp >= kSoftWarp2 ? 1 : 0;
+    const int hr = (warp & 3) * 32 + lane;  // head row within the group
     const int head = hg * kHeads + hr;
     const bool head_ok = head < p.num_heads;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float gs = *p.gs;
     const bool gs_ok = scale_ok(gs);
     float score_scale = p.softmax_scale * gs * kLog2e;
@@ -795,22 +871,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       // unit), 32..71 = q_lat units 24..63 (shared memory chunks 0..4).
       // One pass in three batches of 24 loads converts with the given sigma
       // and returns max(|q_lat|, |q_pe/gs|).
+      // Each half stages 36 of the units, in three batches of 12 loads.
       auto stage = [&](float sigma) -> float {
         float qmax = 0.f;
 #pragma unroll 1
         for (int g = 0; g < 3; ++g) {
-          uint4 w[24];
+          const int ub = 36 * half + 12 * g;  // first unit position of the batch
+          uint4 w[12];
 #pragma unroll
-          for (int i = 0; i < 24; ++i) {
-            const int up = 24 * g + i, u = up < 8 ? 64 + up : up - 8;
+          for (int i = 0; i < 12; ++i) {
+            const int up = ub + i, u = up < 8 ? 64 + up : up - 8;
             w[i] = head_ok ? ldg16(qrow + 16 * u) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
-          for (int i4 = 0; i4 < 24; i4 += 4) {
+          for (int i4 = 0; i4 < 12; i4 += 4) {
             uint32_t v[16];
 #pragma unroll
             for (int i = i4; i < i4 + 4; ++i) {
-              const int up = 24 * g + i;
+              const int up = ub + i;
               const float f = up < 8 ? inv_gs : 1.f;
               const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
@@ -823,7 +901,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
                 v[4 * (i - i4) + kx] = pack_f16(lo * sigma, hi * sigma);
               }
             }
-            const int up0 = 24 * g + i4;
+            const int up0 = ub + i4;
             if (up0 < 32) {
               tmem_st16(tmem + lane_off + kTQRope + 4 * up0, v);
             } else {
@@ -840,7 +918,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       };
       // sigma = 2^-a with sigma*qmax < 2^16 (f16 max 65504); a = 0 unless a
       // query value reaches 2^15, in which case the row is staged again
-      const float qmax = stage(1.f);
+      float qmax = stage(1.f);
+      xch.v[half][hr] = qmax;  // the row's max over both halves' units
+      mbar_arrive(&xch.qx);
+      if (!bar_wait(&xch.qx, 0, err, &abort_s)) ok = false;
+      qmax = fmaxf(qmax, xch.v[half ^ 1][hr]);
       const int qexp = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFFu) - 127;
       const int a_sh = max(0, min(qexp - 14, 100));
       if (__any_sync(0xffffffffu, a_sh > 0)) {
@@ -853,17 +935,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 16) tmem_st16(tmem + lane_off + kTO + c, z);
+        for (int c = 0; c < 128; c += 16) tmem_st16(tmem + lane_off + kTO + 128 * half + c, z);
       }
       fence_async_smem();
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.q_ready);
 
-      softmax_tiles(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run);
+      if (ok)
+        softmax_tiles<2>(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run, half,
+                         &xch, hr);
       if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
     }
-    write_partial(p, tmem, lane_off, ok, nt, m_run, l_run, gs, row0, b, head, head_ok, direct, rank);
+    write_partial<2>(p, tmem, lane_off, ok, nt, m_run, l_run, gs, row0, b, head, head_ok, direct, rank, half, &xch,
+                     hr, &abort_s);
   }
   tc_fence_before();
   __syncthreads();
@@ -1294,10 +1379,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       tc_fence_before();
       mbar_arrive(&bars.q_ready);
       if (!scales_ok && hr == 0 && rank == 0) flag_error(err, MLA_DEVERR_SCALE);
-      softmax_tiles(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run);
+      softmax_tiles<1>(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run, 0,
+                       nullptr, hr);
       if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
     }
-    write_partial(p, tmem, lane_off, ok, nt, m_run, l_run, gs, row0, b, head, head_ok, direct, rank);
+    write_partial<1>(p, tmem, lane_off, ok, nt, m_run, l_run, gs, row0, b, head, head_ok, direct, rank, 0, nullptr,
+                     hr, &abort_s);
   }
   tc_fence_before();
   __syncthreads();
@@ -1709,7 +1796,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
   if (const int st = smem_limit_once(kern, static_cast<int>(smem), slot)) return st;
   {
     void* args[] = {&p};
-    if (const int st = launch_ex(kern, grid, dim3(kThreads), smem, stream, a.planned, args)) return st;
+    const int threads = a.gs_q != nullptr ? kThreads : kThreadsTc;
+    if (const int st = launch_ex(kern, grid, dim3(threads), smem, stream, a.planned, args)) return st;
   }
   if (a.planned) {
     const float* po = p.part_o;
