@@ -235,15 +235,13 @@ int mla_nvfp4_decode_q4(const void* q, int batch, int num_heads, const uint8_t* 
  *                  sequence) must fit.  num_splits == 1 uses no scratch.
  *                  Calls beyond the limit return MLA_ERR_WORKSPACE without
  *                  launching, and mla_nvfp4_last_error() names the sizes.
- *   First call   : the first call on a device that uses the scratch, with
- *                  that device current, looks up the scratch's device
- *                  address (cudaGetSymbolAddress, which may load the
- *                  library's device code) and keeps it for later calls on
- *                  that device; make that first call before any stream
- *                  capture begins.  A failed lookup returns MLA_ERR_LAUNCH.
- *                  The address belongs to the device's current context: after
- *                  cudaDeviceReset the kept address is stale, so do not call
- *                  this entry point on a device that has been reset.
+ *   Scratch      : every call that uses the scratch looks up its device
+ *                  address in the current context (cudaGetSymbolAddress,
+ *                  which allocates nothing; the first call in a process may
+ *                  load the library's device code, so make it before any
+ *                  stream capture begins).  A reset device gets the address
+ *                  of its new context.  A failed lookup returns
+ *                  MLA_ERR_LAUNCH.
  *   Concurrency  : all calls on one device share the one scratch, so calls
  *                  whose work may overlap on the device (different
  *                  streams, or several host threads without ordering) race
@@ -322,9 +320,10 @@ int mla_nvfp4_decode_host(const void* q_host, void* q_dev, int batch, int num_he
  *   Scheduling   : one CTA per SM takes work items from a device counter in
  *                  the library (64 counters, used in turn, each back at zero
  *                  when its launch ends).  Up to 64 calls may run at once on
- *                  one device (different streams); the first call on a
- *                  device looks the counters up (cudaGetSymbolAddress) and
- *                  should come before any stream capture begins.
+ *                  one device (different streams).  Every call looks the
+ *                  counters up (cudaGetSymbolAddress, which allocates
+ *                  nothing); the first call in a process loads the module
+ *                  and should come before any stream capture begins.
  *   Errors       : MLA_ERR_INVALID_ARG for bad sizes, strides or alignment
  *                  (nothing launched); device-side, MLA_DEVERR_BOUNDS in
  *                  *error_word when cu_seqlens is out of range or a sequence

@@ -9,9 +9,7 @@
 // whose work overlaps on the device race; calls on one stream are ordered.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdio>
-#include <mutex>
 
 #include "launch.h"
 
@@ -24,27 +22,15 @@ static_assert(kScratchBytes % 256 == 0, "scratch must stay a whole number of 256
 // decode writes every partial row it merges.
 __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch[kMaxDevices];
-std::mutex g_setup;
 thread_local char t_message[512];
 
-// Device address of the current device's scratch, looked up on the first
-// call for that device and kept afterwards.
+// Device address of the current device's scratch, looked up on every call
+// (the lookup allocates nothing and follows the current context, so a reset
+// device that loaded the module again gets the new address).
 int scratch_address(void** ptr) {
-  int dev = -1;
-  if (const int st = mla::cuda_status(cudaGetDevice(&dev))) return st;
-  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED_DEVICE;
-  void* p = g_scratch[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    std::lock_guard<std::mutex> lock(g_setup);
-    p = g_scratch[dev].load(std::memory_order_relaxed);
-    if (p == nullptr) {
-      if (const int st = mla::cuda_status(cudaGetSymbolAddress(&p, g_decode_scratch))) return st;
-      if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 255u) != 0) return MLA_ERR_LAUNCH;
-      g_scratch[dev].store(p, std::memory_order_release);
-    }
-  }
+  void* p = nullptr;
+  if (const int st = mla::cuda_status(cudaGetSymbolAddress(&p, g_decode_scratch))) return st;
+  if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 255u) != 0) return MLA_ERR_LAUNCH;
   *ptr = p;
   return MLA_OK;
 }

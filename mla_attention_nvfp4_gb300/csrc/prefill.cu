@@ -63,7 +63,6 @@
 
 #include <atomic>
 #include <cmath>
-#include <mutex>
 
 #include "launch.h"
 #include "nvfp4.cuh"
@@ -807,27 +806,14 @@ bool make_map(CUtensorMap* m, const void* base, int64_t D, int64_t H, int64_t T,
 constexpr int kSchedSlots = 64;
 __device__ uint32_t g_sched[kSchedSlots][2];
 
-constexpr int kMaxDevices = 64;
-std::atomic<uint32_t*> g_sched_base[kMaxDevices];
 std::atomic<uint32_t> g_sched_next{0};
-std::mutex g_sched_setup;
 
+// A counter slot for the next launch.  The counters' address is looked up on
+// every call: the lookup allocates nothing and follows the current context.
 int sched_counter(uint32_t** out) {
-  int dev = 0;
-  if (const int st = cuda_status(cudaGetDevice(&dev))) return st;
-  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_LAUNCH;
-  uint32_t* base = g_sched_base[dev].load(std::memory_order_acquire);
-  if (base == nullptr) {
-    std::lock_guard<std::mutex> lock(g_sched_setup);
-    base = g_sched_base[dev].load(std::memory_order_relaxed);
-    if (base == nullptr) {
-      void* ptr = nullptr;
-      if (const int st = cuda_status(cudaGetSymbolAddress(&ptr, g_sched))) return st;
-      base = static_cast<uint32_t*>(ptr);
-      g_sched_base[dev].store(base, std::memory_order_release);
-    }
-  }
-  *out = base + 2 * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+  void* ptr = nullptr;
+  if (const int st = cuda_status(cudaGetSymbolAddress(&ptr, g_sched))) return st;
+  *out = static_cast<uint32_t*>(ptr) + 2 * (g_sched_next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
   return MLA_OK;
 }
 
