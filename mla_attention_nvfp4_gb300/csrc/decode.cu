@@ -317,12 +317,12 @@ __device__ __forceinline__ void dequant_segment(const uint4& c, uint32_t s0, uin
 // T units 0..15 and V units 24..31, Q = 2 T units 16..31 and the RoPE chunk
 // (V = latent features [256 rank, +256), T = the other 256; a unit is 8
 // features).  Each thread loads the raw bytes of its part with 16-byte loads
-// straight from global memory into one register buffer, right after it has
-// converted the previous tile: the loads land while the thread waits for the
-// next tile's operand buffers (one buffer, and one copy of the conversion
-// code, ran faster than two buffers a tile apart).  (A bulk L2 prefetch of
-// each record, issued per key, held the issuing thread for thousands of
-// cycles per tile and was dropped.)
+// straight from global memory into one register buffer, in two groups, each
+// reloaded with the next tile's bytes as soon as this tile's conversion has
+// read it: the loads land while the thread converts the rest and waits for
+// the next tile's operand buffers (one buffer, and one copy of the conversion
+// code, ran faster than two buffers a tile apart; a bulk L2 prefetch of each
+// record, issued per key, made the kernel slower and was dropped).
 
 template <int Q, int kRecord>
 struct RawPart {
@@ -354,6 +354,43 @@ __device__ __forceinline__ void load_part(RawPart<Q, kRecord>& r, const uint8_t*
   }
 }
 
+// Group g of part Q's raw bytes (g = 0: the registers the first conversion
+// step reads, g = 1: the rest), from record `rec`, or zeros for rec == null.
+template <int Q, int kRecord>
+__device__ __forceinline__ void load_group(RawPart<Q, kRecord>& r, const uint8_t* rec, int rank, int g) {
+  const int other = 1 - rank;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  if constexpr (Q == 0) {
+    if (g == 0) {
+#pragma unroll
+      for (int i = 0; i < 3; ++i) r.v[i] = rec ? ldg16(rec + 128 * rank + 16 * i) : z;
+    } else {
+#pragma unroll
+      for (int i = 3; i < 6; ++i) r.v[i] = rec ? ldg16(rec + 128 * rank + 16 * i) : z;
+      r.v[6] = rec ? ldg16(rec + 256 + 16 * rank) : z;
+    }
+  } else if constexpr (Q == 1) {
+    if (g == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) r.v[i] = rec ? ldg16(rec + 128 * other + 16 * i) : z;
+      r.v[4] = rec ? ldg16(rec + 256 + 16 * other) : z;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) r.v[5 + i] = rec ? ldg16(rec + 128 * rank + 96 + 16 * i) : z;
+      r.v[7] = rec ? ldg16(rec + 256 + 16 * rank) : z;
+    }
+  } else {
+    if (g == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) r.v[i] = rec ? ldg16(rec + 128 * other + 64 + 16 * i) : z;
+      r.v[4] = rec ? ldg16(rec + 256 + 16 * other) : z;
+    } else {
+#pragma unroll
+      for (int i = 0; i < RawPart<Q, kRecord>::kRope; ++i) r.v[5 + i] = rec ? ldg16(rec + 288 + 16 * i) : z;
+    }
+  }
+}
+
 struct DeqCtx {
   const Params& p;
   Barriers* bars;
@@ -365,7 +402,8 @@ struct DeqCtx {
 // Convert part Q of key k of tile j (raw bytes in r, or zeros for a padding
 // key) into the tile's operand buffers.  False if a wait gave up.
 template <int Q, int kRecord>
-__device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPart<Q, kRecord>& r, float& rope_max) {
+__device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, RawPart<Q, kRecord>& r, float& rope_max,
+                                             bool more, const uint8_t* nrec) {
   uint32_t* err = c.p.error_word;
   Barriers& bars = *c.bars;
   const int k = c.k;
@@ -374,19 +412,25 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
   if constexpr (Q == 0) {
     if (!bar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
 #pragma unroll
-    for (int i = 0; i < 6; ++i) dequant_segment(r.v[i], byte_of(r.v[6], 2 * i), byte_of(r.v[6], 2 * i + 1), tV, 4 * i, k);
+    for (int i = 0; i < 3; ++i) dequant_segment(r.v[i], byte_of(r.v[6], 2 * i), byte_of(r.v[6], 2 * i + 1), tV, 4 * i, k);
+    if (more) load_group<Q, kRecord>(r, nrec, c.rank, 0);
+#pragma unroll
+    for (int i = 3; i < 6; ++i) dequant_segment(r.v[i], byte_of(r.v[6], 2 * i), byte_of(r.v[6], 2 * i + 1), tV, 4 * i, k);
+    if (more) load_group<Q, kRecord>(r, nrec, c.rank, 1);
     fence_async_smem();
     mbar_arrive(&bars.v_full[j & 1]);
   } else if constexpr (Q == 1) {
     if (!bar_wait(&bars.t_empty[j & 1], ph, err, c.abort_s)) return false;
 #pragma unroll
     for (int i = 0; i < 4; ++i) dequant_segment(r.v[i], byte_of(r.v[4], 2 * i), byte_of(r.v[4], 2 * i + 1), tT, 4 * i, k);
+    if (more) load_group<Q, kRecord>(r, nrec, c.rank, 0);
     fence_async_smem();
     mbar_arrive(&bars.t_full[j & 1]);
     if (!bar_wait(&bars.v_empty[j & 1], ph, err, c.abort_s)) return false;
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       dequant_segment(r.v[5 + i], byte_of(r.v[7], 12 + 2 * i), byte_of(r.v[7], 13 + 2 * i), tV, 24 + 4 * i, k);
+    if (more) load_group<Q, kRecord>(r, nrec, c.rank, 1);
     fence_async_smem();
     mbar_arrive(&bars.v_full[j & 1]);
   } else {
@@ -396,6 +440,7 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         dequant_segment(r.v[i], byte_of(r.v[4], 8 + 2 * i), byte_of(r.v[4], 9 + 2 * i), tT, 16 + 4 * i, k);
+      if (more) load_group<Q, kRecord>(r, nrec, c.rank, 0);
       if constexpr (kRecord == 368) {  // e4m3 -> f16, exact
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -418,6 +463,7 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, const RawPa
                             bf16x2_to_f16x2_sat(x.z, rope_max), bf16x2_to_f16x2_sat(x.w, rope_max)));
         }
       }
+      if (more) load_group<Q, kRecord>(r, nrec, c.rank, 1);
     }
     fence_async_smem();
     mbar_arrive(&bars.t_full[j & 1]);
@@ -457,8 +503,10 @@ __device__ bool dequant_role(const DeqCtx& c) {
   for (int j = 0; j < nt; ++j) {
     const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
     i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
-    if (!convert_part<Q, kRecord>(c, j, ra, rope_max)) break;
-    if (j + 1 < nt) load_or_zero(ra, s_nxt);
+    // the next tile's bytes load into each register group as soon as this
+    // tile's conversion has read it
+    if (!convert_part<Q, kRecord>(c, j, ra, rope_max, j + 1 < nt, s_nxt >= 0 ? p.cache + s_nxt * kRecord : nullptr))
+      break;
     s_nxt = s_2;
   }
   if (rope_max > 65504.f) flag_error(p.error_word, MLA_DEVERR_RANGE);
