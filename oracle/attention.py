@@ -244,3 +244,27 @@ def prefill_rows(q, k, v, cu_seqlens, softmax_scale, rows, head, with_abs=False)
         if with_abs:
             o_abs[i] = attend(q[r:r + 1, head], kk, np.abs(v[a:r + 1, head]), softmax_scale)[0][0]
     return (o, lse, o_abs) if with_abs else (o, lse)
+
+
+def prefill_with_context_rows(q, k, v, cu_seqlens, k_ctx, v_ctx, cu_ctx, softmax_scale, rows, head, with_abs=False):
+    """prefill_with_context for selected global query rows of one head
+    (sampling at full size).  Returns (o [len(rows), Dv], lse [len(rows)])
+    and with ``with_abs`` also softmax @ |v|."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    cc = np.asarray(cu_ctx, dtype=np.int64)
+    Dv = np.asarray(v).shape[2]
+    o = np.zeros((len(rows), Dv))
+    o_abs = np.zeros((len(rows), Dv))
+    lse = np.zeros(len(rows))
+    for i, r in enumerate(rows):
+        s_ = int(np.searchsorted(cu, r, side="right") - 1)
+        a, ca, ce = int(cu[s_]), int(cc[s_]), int(cc[s_ + 1])
+        keys = np.concatenate([np.asarray(k_ctx[ca:ce, head], np.float64), np.asarray(k[a:r + 1, head], np.float64)])
+        vals = np.concatenate([np.asarray(v_ctx[ca:ce, head], np.float64), np.asarray(v[a:r + 1, head], np.float64)])
+        qr = np.asarray(q[r:r + 1, head], np.float64)
+        oo, ll = attend(qr, keys, vals, softmax_scale)
+        o[i], lse[i] = oo[0], ll[0]
+        if with_abs:
+            o_abs[i] = attend(qr, keys, np.abs(vals), softmax_scale)[0][0]
+    return (o, lse, o_abs) if with_abs else (o, lse)
+

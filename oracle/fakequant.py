@@ -205,3 +205,35 @@ def _allowance(p, s_dense, s_kept, vv, o, l, rel, mids_c, mids_s):
                 w = x[:, g0:g0 + 4] * near[:, None]
                 allow += 2.0 * (w @ np.abs(vv[g0:g0 + 4]) + w.sum(axis=1, keepdims=True) * np.abs(o))
     return allow / l
+
+
+def prefill_fakequant_seq_rows(q_seq, k_seq, v_seq, softmax_scale, gs_q, gs_k, gs_v, rows, sparse24=False,
+                               tie_rel=None):
+    """prefill_fakequant for selected rows of one sequence and head (sampling
+    at full size): q_seq, k_seq [n, 192], v_seq [n, 128] are the head's
+    values over the whole sequence; rows are indices within it.  Returns
+    (o [len(rows), 128], lse [len(rows)], o_abs, allowance) as
+    prefill_fakequant does for those rows."""
+    q_hat = qdq(q_seq, gs_q)
+    k_hat = qdq(k_seq, gs_k)
+    n = np.asarray(v_seq).shape[0]
+    v_hat = qdq_tokens(np.asarray(v_seq)[:, None, :], [0, n], gs_v)[:, 0, :]
+    mids_c = (nvfp4.E2M1_MAGNITUDES[:-1] + nvfp4.E2M1_MAGNITUDES[1:]) / 2
+    grid_s = nvfp4.e4m3_decode(np.arange(0x7F))
+    mids_s = (grid_s[:-1] + grid_s[1:]) / 2
+    Dv = v_hat.shape[1]
+    o = np.zeros((len(rows), Dv))
+    o_abs = np.zeros((len(rows), Dv))
+    allow = np.zeros((len(rows), Dv))
+    lse = np.zeros(len(rows))
+    for i, r in enumerate(rows):
+        s = softmax_scale * (q_hat[r:r + 1] @ k_hat[:r + 1].T)
+        s_kept = select_2of4(s) if sparse24 else s
+        vv = v_hat[:r + 1]
+        oo, ll, p, p_hat, l = softmax_fq(s_kept, vv)
+        o[i], lse[i] = oo[0], ll[0]
+        o_abs[i] = ((p_hat @ np.abs(vv)) / l)[0]
+        if tie_rel is not None:
+            allow[i] = _allowance(p, s if sparse24 else None, s_kept, vv, oo, l, tie_rel, mids_c, mids_s)[0]
+    return o, lse, o_abs, allow
+

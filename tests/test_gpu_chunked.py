@@ -10,8 +10,8 @@ import torch
 import mla_attention_nvfp4_gb300 as mla
 from mla_attention_nvfp4_gb300 import workloads
 from oracle import attention, cache as ocache, nvfp4, swizzle
-from tests.helpers import (MEAN_REL, P_ROUNDING, assert_lse_close, check_fused_output, f32, oracle_cache, oracle_gs,
-                           quant_flips)
+from tests.helpers import (MEAN_REL, P_ROUNDING, assert_lse_close, check_fused_blocks, check_fused_output, f32,
+                           oracle_cache, oracle_gs, quant_flips)
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
@@ -195,3 +195,47 @@ def test_chunked_prefill_end_to_end(record_bytes):
     ref_deq = swizzle.dequantize_rows(*swizzle.quantize_rows(o_ref2.astype(np.float32), gso), T, H * 128, gso)
     rel = np.abs(deq - ref_deq).sum() / np.abs(ref_deq).sum()
     assert rel <= 5e-3, rel
+
+
+def test_chunked_full_size_sampled():
+    """The benchmark's chunked-context shape: 8 x 4096 new tokens after 8 x
+    4096 context tokens per sequence, 128 heads, in its launch order
+    (partial over the context, partial causal, merge); sampled rows of two
+    sequences and two heads against the oracle's single-softmax prefill."""
+    w = workloads.prefill_context((4096,) * 8, (4096,) * 8, heads=128, seed=3, device=DEV)
+    err = _err()
+    o1, l1 = mla.mla_nvfp4_prefill_partial(w.q, w.k_ctx, w.v_ctx, w.cu_seqlens, w.max_seqlen, w.softmax_scale,
+                                           cu_seqlens_k=w.cu_ctx, error_word=err)
+    o2, l2 = mla.mla_nvfp4_prefill_partial(w.q, w.k, w.v, w.cu_seqlens, w.max_seqlen, w.softmax_scale,
+                                           error_word=err)
+    gs_out = nvfp4.global_scale(max(float(w.v.abs().max()), float(w.v_ctx.abs().max())))
+    lse = torch.empty((w.heads, w.total_tokens), device=DEV)
+    codes, sf = mla.mla_nvfp4_merge_fused_out(torch.stack([o1, o2]), torch.stack([l1, l2]),
+                                              torch.tensor([gs_out], device=DEV), lse=lse, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    del o1, o2
+    H = w.heads
+    cu, cc = w.cu_seqlens.cpu().numpy(), w.cu_ctx.cpu().numpy()
+    rng = np.random.default_rng(23)
+    rows = sorted({a + r for a in (0, 3 * 4096, 6 * 4096)
+                   for r in (0, 1, 127, 128, 4095, *rng.integers(2, 4095, 11).tolist())})
+    sf_np, lse_np = sf.cpu().numpy(), f32(lse)
+    # the flip rate is a rate over many codes: taken over all sampled rows
+    # of both heads (each flip is checked to lie at a rounding boundary)
+    total = {"scale_flips": 0, "code_flips": 0, "zero_sign": 0, "codes": 0}
+    for h in (0, 100):
+        sl = slice(h, h + 1)
+        o_ref, l_ref, o_abs = attention.prefill_with_context_rows(
+            f32(w.q[:, sl]), f32(w.k[:, sl]), f32(w.v[:, sl]), cu, f32(w.k_ctx[:, sl]), f32(w.v_ctx[:, sl]), cc,
+            w.softmax_scale, rows, 0, with_abs=True)
+        c_rows = codes[rows][:, h * 64:(h + 1) * 64].cpu().numpy()
+        m, kk = np.meshgrid(np.array(rows), np.arange(h * 8, h * 8 + 8), indexing="ij")
+        counts = check_fused_blocks(c_rows, sf_np[swizzle.sf_offset(m, kk, H * 8)], o_ref, o_abs, gs_out,
+                                    f"chunked 8x4096+4096 head {h} sampled rows")
+        for key in total:
+            total[key] += counts[key]
+        assert_lse_close(lse_np[h, rows], l_ref, f"chunked lse head {h}")
+    rate = (17 * total["scale_flips"] + total["code_flips"] + total["zero_sign"]) / total["codes"]
+    print(f"[fused] chunked 8x4096+4096, both heads: {total} -> mismatch rate {rate:.2e}")
+    assert rate <= FUSED_FLIP_RATE, total

@@ -13,7 +13,7 @@ import torch
 import mla_attention_nvfp4_gb300 as mla
 from mla_attention_nvfp4_gb300 import workloads
 from oracle import fakequant, nvfp4, swizzle
-from tests.helpers import P_ROUNDING, assert_lse_close, check_fused_output, f32
+from tests.helpers import P_ROUNDING, assert_lse_close, check_fused_blocks, check_fused_output, f32
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
@@ -95,3 +95,41 @@ def test_fakequant_sparse_differs_from_dense():
     b = _run(w, True, np.float32(1e-3))
     assert not np.array_equal(a[2], b[2])
     assert np.array_equal(a[2][:, :2], b[2][:, :2])  # rows 0 and 1 see at most 2 keys
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_fakequant_full_size_sampled(sparse):
+    """8 sequences x 4096 tokens x 128 heads (the benchmark's fake-quant
+    legs): sampled rows of two sequences and two heads against the oracle,
+    one sequence-head at a time."""
+    w = workloads.prefill_8x4096(device=DEV)
+    gs = [nvfp4.global_scale(float(t.abs().max())) for t in (w.q, w.k, w.v)]
+    gs_out = nvfp4.global_scale(float(w.v.abs().max()))
+    codes, sf, lse = _run(w, sparse, gs_out)
+    H = w.heads
+    rng = np.random.default_rng(17)
+    # rates over all sampled rows: magnitude decisions (a differing scale
+    # byte counting 17) and, separately, the sign of a code that is zero on
+    # both sides (a value within its error of zero; each checked so)
+    total = {"scale_flips": 0, "code_flips": 0, "zero_sign": 0, "codes": 0}
+    for s in (0, 5):
+        a = 4096 * s
+        local = sorted({0, 1, 127, 128, 2047, 4095, *rng.integers(2, 4095, 3).tolist()})
+        rows = [a + r for r in local]
+        for h in (0, 77):
+            o, l_ref, o_abs, allow = fakequant.prefill_fakequant_seq_rows(
+                f32(w.q[a:a + 4096, h]), f32(w.k[a:a + 4096, h]), f32(w.v[a:a + 4096, h]), w.softmax_scale, *gs,
+                local, sparse24=sparse, tie_rel=TIE_REL)
+            c_rows = codes[rows][:, h * 64:(h + 1) * 64]
+            m, kk = np.meshgrid(np.array(rows), np.arange(h * 8, h * 8 + 8), indexing="ij")
+            sf_rows = sf[swizzle.sf_offset(m, kk, H * 8)]
+            err = allow + ACCUM_REL * o_abs
+            counts = check_fused_blocks(c_rows, sf_rows, o, err / P_ROUNDING, gs_out,
+                                        f"fake-quant 8x4096 seq {s} head {h} sparse={sparse}")
+            for key in total:
+                total[key] += counts[key]
+            assert_lse_close(lse[h, rows], l_ref, f"fake-quant lse seq {s} head {h}", tol=2e-4)
+    flips = (17 * total["scale_flips"] + total["code_flips"]) / total["codes"]
+    signs = total["zero_sign"] / total["codes"]
+    print(f"[fakequant] 8x4096 sparse={sparse}: {total} -> magnitude flips {flips:.2e}, zero signs {signs:.2e}")
+    assert flips <= 2e-3 and signs <= 1e-2, total

@@ -97,3 +97,36 @@ def test_prefill_output_into_gemm():
     rel = float(np.abs(f32(out) - ref).sum() / np.abs(ref).sum())
     print(f"[gemm] prefill output -> gemm: mean rel {rel:.2e}")
     assert rel <= 2e-2
+
+
+def test_gemm_full_size_sampled():
+    """The benchmark's GEMM: the fused output of the 8 x 4096 x 128 prefill
+    ([32768, 16384] codes + swizzled scales, as written) times a random
+    NVFP4 weight [7168, 16384] drawn as the benchmark draws it; 64 x 64
+    sampled outputs against the oracle."""
+    w = workloads.prefill_8x4096(device=DEV)
+    gsp = nvfp4.global_scale(float(w.v.abs().max()))
+    gst = torch.tensor([gsp], device=DEV)
+    codes, sf = mla.mla_nvfp4_prefill_fused_out(w.q, w.k, w.v, w.cu_seqlens, w.max_seqlen, w.softmax_scale, gst)
+    n_out, k_in = 7168, w.heads * 128
+    g = torch.Generator(device=DEV)
+    g.manual_seed(7)
+    wc = torch.randint(0, 256, (n_out, k_in // 2), dtype=torch.uint8, device=DEV, generator=g)
+    wsf = torch.randint(0x28, 0x48, (n_out * k_in // 16,), dtype=torch.uint8, device=DEV, generator=g)
+    gs_w = np.float32(1.0 / 4096)
+    out = mla.mla_nvfp4_gemm(codes, sf, wc, wsf, gst, torch.tensor([gs_w], device=DEV))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(29)
+    rows = np.unique(np.concatenate([[0, 127, 128, 32767], rng.integers(0, 32768, 60)]))
+    cols = np.unique(np.concatenate([[0, 255, 256, 7167], rng.integers(0, 7168, 60)]))
+    ac, asf = codes.cpu().numpy(), sf.cpu().numpy()
+    wc_np, wsf_np = wc.cpu().numpy(), wsf.cpu().numpy()
+    ref = gemm.nvfp4_gemm_entries(ac, asf, wc_np, wsf_np, k_in, gsp, gs_w, rows, cols)
+
+    def rows_abs(c, buf, idx, gs):
+        m, kk = np.meshgrid(idx, np.arange(k_in // 16), indexing="ij")
+        sfb = buf[swizzle.sf_offset(m, kk, k_in // 16)]
+        return np.abs(nvfp4.dequantize_blocks(nvfp4.unpack_e2m1(c[idx]), sfb, gs))
+
+    absprod = rows_abs(ac, asf, rows, gsp) @ rows_abs(wc_np, wsf_np, cols, gs_w).T
+    _check(f32(out[rows][:, cols]), ref, absprod, k_in, "32768x7168x16384 sampled")

@@ -290,3 +290,18 @@ def test_context_prefill_is_the_merge_of_its_parts():
     z = np.zeros((0, H, 192))
     o0, l0 = attention.prefill_with_context(q, k, v, cu, z, np.zeros((0, H, 128)), np.zeros(4, dtype=int), 0.07)
     assert np.allclose(o0, o2, atol=1e-12) and np.allclose(l0, l2, atol=1e-12)
+
+
+def test_context_rows_match_the_full_oracle():
+    rng = np.random.default_rng(9)
+    H, lens, ctx = 2, (5, 9), (7, 0)
+    T, Tc = sum(lens), sum(ctx)
+    q, k = rng.standard_normal((T, H, 192)), rng.standard_normal((T, H, 192))
+    v = rng.standard_normal((T, H, 128))
+    kc, vc = rng.standard_normal((Tc, H, 192)), rng.standard_normal((Tc, H, 128))
+    cu, cc = np.array([0, 5, 14]), np.array([0, 7, 7])
+    o, lse, o_abs = attention.prefill_with_context(q, k, v, cu, kc, vc, cc, 0.07, with_abs=True)
+    rows = [0, 4, 5, 13]
+    ro, rl, ra = attention.prefill_with_context_rows(q, k, v, cu, kc, vc, cc, 0.07, rows, 1, with_abs=True)
+    assert np.allclose(ro, o[rows, 1], rtol=1e-12) and np.allclose(rl, lse[1, rows], rtol=1e-12)
+    assert np.allclose(ra, o_abs[rows, 1], rtol=1e-12)

@@ -216,3 +216,20 @@ def test_allowance_is_zero_without_near_ties_and_covers_a_planted_flip():
     o2, _, _, allow2 = fakequant.prefill_fakequant(q, k, v, cu, scale, *g, with_abs=True, tie_rel=2e-2)
     assert np.array_equal(o, o2)
     assert (allow2 > 0).any() and (allow2 >= allow).all()
+
+
+def test_seq_rows_match_the_full_oracle():
+    """The sampling form (one sequence and head, selected rows) gives the
+    full oracle's rows, dense and 2:4, with the same allowances."""
+    q, k, v, cu, g = _case([37], H=1, seed=8)
+    scale = 1 / math.sqrt(192)
+    rows = [0, 1, 15, 16, 17, 36]
+    for sparse in (False, True):
+        o, lse, o_abs, allow = fakequant.prefill_fakequant(q, k, v, cu, scale, *g, sparse24=sparse, with_abs=True,
+                                                           tie_rel=1e-3)
+        ro, rl, ra, rw = fakequant.prefill_fakequant_seq_rows(q[:, 0], k[:, 0], v[:, 0], scale, *g, rows,
+                                                              sparse24=sparse, tie_rel=1e-3)
+        assert np.allclose(ro, o[rows, 0], rtol=1e-12, atol=1e-15)
+        assert np.allclose(rl, lse[0, rows], rtol=1e-12)
+        assert np.allclose(ra, o_abs[rows, 0], rtol=1e-12, atol=1e-15)
+        assert np.allclose(rw, allow[rows, 0], rtol=1e-12, atol=1e-15)

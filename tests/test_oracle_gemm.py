@@ -70,3 +70,16 @@ def test_gemm_lossless_on_grid():
     wc, wsf = swizzle.quantize_rows(w, gs)
     got = gemm.nvfp4_gemm(ac, asf, wc, wsf, M, N, K, gs, gs)
     assert np.array_equal(got, a.astype(np.float64) @ w.astype(np.float64).T)
+
+
+def test_gemm_entries_match_the_full_product():
+    rng = np.random.default_rng(5)
+    M, N, K = 300, 256, 512
+    ac = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    wc = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    asf = swizzle.swizzle_scales(rng.integers(0x28, 0x48, (M, K // 16)).astype(np.uint8))
+    wsf = swizzle.swizzle_scales(rng.integers(0x28, 0x48, (N, K // 16)).astype(np.uint8))
+    full = gemm.nvfp4_gemm(ac, asf, wc, wsf, M, N, K, np.float32(0.5), np.float32(0.25))
+    rows, cols = [0, 7, 128, 299], [1, 130, 255]
+    sub = gemm.nvfp4_gemm_entries(ac, asf, wc, wsf, K, np.float32(0.5), np.float32(0.25), rows, cols)
+    assert np.array_equal(sub, full[np.ix_(rows, cols)])
