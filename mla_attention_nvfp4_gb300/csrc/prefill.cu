@@ -606,8 +606,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pb[2 * i + 1] = ex2_approx(a1);
                 ls2[i & 3] = add2(ls2[i & 3], pk2(pb[2 * i], pb[2 * i + 1]));
               }
+              // amax of the block: P >= 0, so a plain three-input max
+              float am = max3(pb[0], pb[1], pb[2]);
+#pragma unroll
+              for (int i = 3; i < 15; i += 2) am = max3(am, pb[i], pb[i + 1]);
+              am = fmaxf(am, pb[15]);
+              // block scale and 1/S in the reciprocal form, 1/S by the
+              // approximate reciprocal: its decisions differ from the exact
+              // quotient's only within a few float32 ulps of a midpoint
+              const uint32_t sb = cvt_e4m3(__fmul_rn(am, kf_p));
+              const float S = __fmul_rn(e4m3_to_f32(sb), kGsP);
               float R;
-              const uint32_t sb = block_scale(fmaxf(amax8(pb), amax8(pb + 8)), kf_p, kGsP, R);
+              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(R) : "f"(S));
+              if (!(S > 0.f)) R = 0.f;
               const uint32_t cw2[2] = {encode8(pb, R), encode8(pb + 8, R)};
               const uint32_t s2 = e4m3x2_to_f16x2_pair(sb | (sb << 8));
 #pragma unroll
