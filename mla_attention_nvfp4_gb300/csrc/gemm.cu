@@ -23,11 +23,13 @@
 //                 four tcgen05.mma kind::mxf4nvf4 (M 128, N 256, K 64, block
 //                 scale 1x16 ue4m3) into the TMEM accumulator,
 //   warps 2..5    epilogue: accumulator -> x gs_a gs_w -> bf16 -> C,
-//   warp 6        scale copies: per stage, tcgen05.cp of the scale tiles
-//                 into TMEM (32x128b, replicated to the four lane quarters),
-//                 their completion releasing the stage to the MMA issuer
-//                 (issued from the MMA thread itself the copies cost ~10 %
-//                 more: 1.99 against 1.78 ms on 32768 x 7168 x 16384).
+//   warps 6, 7    scale copies: per stage, the twelve tcgen05.cp of the
+//                 scale tiles into TMEM (32x128b, replicated to the four
+//                 lane quarters), split between the two warps, their
+//                 completion releasing the stage to the MMA issuer.  The
+//                 copies' issue rate, not the tensor pipe, set the pace when
+//                 the MMA thread issued them itself (1.99 ms on 32768 x 7168
+//                 x 16384 against 1.78 with one copy warp and 1.44 with two).
 // TMEM: accumulator columns [0, 256), then per stage 16 columns of A scales
 // and 32 of W scales.
 #include <cuda.h>
@@ -47,7 +49,8 @@ using namespace sm100;
 constexpr int kBM = 128, kBN = 256;
 constexpr int kBKBytes = 128;            // K per stage: 256 fp4 codes
 constexpr int kStages = 4;
-constexpr int kThreads = 224;
+constexpr int kCopyWarps = 2;  // 1: 1.78 ms, 2: 1.44, 3-4: 1.48, 6: 1.55 on 32768 x 7168 x 16384
+constexpr int kThreads = 192 + 32 * kCopyWarps;
 constexpr uint32_t kABytes = kBM * kBKBytes;      // 16 KB
 constexpr uint32_t kBBytes = kBN * kBKBytes;      // 32 KB
 constexpr uint32_t kSfTile = 512;                 // 128 rows x 4 blocks
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.full[s], 1);
       mbar_init(&bars.empty[s], 1);
-      mbar_init(&bars.sf_full[s], 1);
+      mbar_init(&bars.sf_full[s], kCopyWarps);
     }
     mbar_init(&bars.acc_full, 1);
     mbar_init(&bars.acc_empty, 128);
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars.acc_full);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp >= 6) {
     // ------------------------------------------------------ scale copies
     // per stage, once its bytes have landed: scales into TMEM, k tile j of
     // A to columns sfa + 4 j; of W, row tiles 0 and 1 to columns sfb + 8 j
@@ -236,10 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            sf_copy(tmem + col_sfa(s) + 4 * j, sf_desc(sSfa(s) + j * kSfTile));
-            sf_copy(tmem + col_sfb(s) + 8 * j, sf_desc(sSfb(s) + j * kSfTile));
-            sf_copy(tmem + col_sfb(s) + 8 * j + 4, sf_desc(sSfb(s) + kSfaBytes + j * kSfTile));
+          for (int c = warp - 6; c < 12; c += kCopyWarps) {
+            const int j = c & 3, kind = c >> 2;  // 0: A, 1: W rows 0..127, 2: W rows 128..255
+            const uint32_t col = kind == 0 ? col_sfa(s) + 4 * j : col_sfb(s) + 8 * j + 4 * (kind - 1);
+            const uint32_t src = kind == 0 ? sSfa(s) + j * kSfTile : sSfb(s) + (kind - 1) * kSfaBytes + j * kSfTile;
+            sf_copy(tmem + col, sf_desc(src));
           }
           mma_commit(&bars.sf_full[s]);
         }
