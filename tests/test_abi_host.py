@@ -123,3 +123,49 @@ def test_selftest_wait_arguments_checked():
     assert lib.mla_nvfp4_selftest_wait(None, 50_000_000, None, None) == 1   # no error word
     assert lib.mla_nvfp4_selftest_wait(p, 0, None, None) == 1               # limit below 1 us
     assert lib.mla_nvfp4_selftest_wait(p, 2_000_000_000, None, None) == 1   # limit above 1 s
+
+
+def test_extension_entry_points_reject_bad_arguments():
+    """The chunked-context, fake-quant and NVFP4-query entry points check
+    their arguments on the host (status codes: 1 invalid, 2 record width,
+    3 alignment) before any launch; empty work is a no-op."""
+    lib = mla.load_library()
+    p = ctypes.c_void_p(16)
+    odd = ctypes.c_void_p(8)
+    # gather: record width, negative count, empty, misaligned cache
+    assert lib.mla_nvfp4_gather_latent(p, 10, 400, p, p, 4, p, p, None, None) == 2
+    assert lib.mla_nvfp4_gather_latent(p, 10, 432, p, p, -1, p, p, None, None) == 1
+    assert lib.mla_nvfp4_gather_latent(p, 10, 432, p, p, 0, p, p, None, None) == 0
+    assert lib.mla_nvfp4_gather_latent(odd, 10, 432, p, p, 4, p, p, None, None) == 3
+    # partial prefill: no heads, null lse, short head stride, misaligned out, empty
+    H = 2
+    args = [p, p, p, H * 192, 192, H * 192, 192, H * 128, 128, p, None, 1, 4, 0, 4, H, 0.1, p, p, None, None]
+    bad = list(args); bad[15] = 0
+    assert lib.mla_nvfp4_prefill_partial(*bad) == 1
+    bad = list(args); bad[18] = None
+    assert lib.mla_nvfp4_prefill_partial(*bad) == 1
+    bad = list(args); bad[4] = 100
+    assert lib.mla_nvfp4_prefill_partial(*bad) == 1
+    bad = list(args); bad[17] = odd
+    assert lib.mla_nvfp4_prefill_partial(*bad) == 3
+    bad = list(args); bad[12] = 0; bad[11] = 0
+    assert lib.mla_nvfp4_prefill_partial(*bad) == 0
+    # merge: no parts, null scale, empty
+    assert lib.mla_nvfp4_merge_fused_out(p, p, 0, 4, H, p, p, p, None, None, None) == 1
+    assert lib.mla_nvfp4_merge_fused_out(p, p, 2, 4, H, None, p, p, None, None, None) == 1
+    assert lib.mla_nvfp4_merge_fused_out(p, p, 2, 0, H, p, p, p, None, None, None) == 0
+    # operand fake quant: a missing global scale, a short v stride
+    q = [p, p, p, H * 192, 192, H * 192, 192, H * 128, 128, p, 1, 4, 4, H, p, p, p, p, p, p, None, None]
+    bad = list(q); bad[16] = None
+    assert lib.mla_nvfp4_prefill_qdq(*bad) == 1
+    bad = list(q); bad[7] = 100
+    assert lib.mla_nvfp4_prefill_qdq(*bad) == 1
+    # fake-quant prefill: sparse24 must be 0 or 1, global scales required
+    f = [p, p, p, p, 1, 4, 4, H, 0.1, p, p, p, 2, p, p, p, None, None, None]
+    assert lib.mla_nvfp4_prefill_fakequant(*f) == 1
+    f[12] = 0
+    f[10] = None
+    assert lib.mla_nvfp4_prefill_fakequant(*f) == 1
+    # NVFP4-query decode: the query's global scale is required
+    assert lib.mla_nvfp4_decode_q4(p, 1, 1, p, 1, 432, p, 1, 64, p, None, 0, 1.0, p, None, p, None, None, 0, 1,
+                                   None, None) == 1
