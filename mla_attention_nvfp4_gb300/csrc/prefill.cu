@@ -85,7 +85,8 @@ constexpr uint32_t kSmemBytes = kSmemV + 2 * kVBytes;  // 212992
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;      // + alignment slack
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 256
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 256 where the block's max is taken
+constexpr float kSumLimit = 65536.0f;      // a block's P row sum formed against the reference: P <= 2^16
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
@@ -518,135 +519,152 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
         }
         tmem_ld_wait();
-        // max of the raw scores (scale_log2 > 0); the scale is applied
-        // inside the exponent below
         const int key0 = j * kBN;
-        float mq[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mq[i] = -INFINITY;
         // the last visible key: the query itself (causal), or the chunk's last
         const int lim = (kPartial && p.cu_k != nullptr) ? w.n_k - 1 : qi;
         if (key0 + kBN - 1 > lim) {  // diagonal (or last) block: mask the keys beyond
 #pragma unroll
           for (int c = 0; c < 128; ++c) x[c] = (key0 + c <= lim) ? x[c] : -INFINITY;
         }
+        // Exact mode, once the row has a reference max: P is first formed
+        // against it without looking for the block's max; only a row whose
+        // block sum then exceeds kSumLimit (or is not finite) takes the
+        // block's max, raises its reference as below and forms P again.
+        // Otherwise, and in fake-quant mode, the block's max comes first.
+        bool fast = !kQuant && __all_sync(0xffffffffu, m_run != -INFINITY);
+        float m_use = m_run, alpha = 1.f, l_blk = 0.f;
+#pragma unroll 1
+        for (int attempt = 0; attempt < 2; ++attempt) {
+          if (!fast) {
+            // max of the raw scores (scale_log2 > 0); the scale is applied
+            // inside the exponent below
+            float mq[8];
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) mq[(c >> 1) & 7] = max3(mq[(c >> 1) & 7], x[c], x[c + 1]);
-        const float mx =
-            fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7]))) *
-            sl2;
-        float m_use = m_run, alpha = 1.f;
-        bool raise;
-        if constexpr (kQuant) {
-          // power-of-two reference: the running max rounded up (log2 units),
-          // raised whenever it grows, so P <= 1 and O rescales exactly
-          const float m_new = ceilf(mx);
-          raise = m_new > m_run;
-          if (raise) {
-            m_use = m_new;
-            alpha = m_run == -INFINITY ? 0.f : exp2_int(m_run - m_new);
-          }
-        } else {
-          // lazy reference update
-          raise = mx > m_run + kRescaleThreshold;
-          if (raise) {
-            m_use = mx;
-            alpha = ex2_approx(m_run - mx);  // 0 on this warpgroup's first block
-          }
-        }
-        // The partial O holds only this warpgroup's earlier blocks, whose
-        // P.V retired before S of this block was committed.
-        if (__any_sync(0xffffffffu, raise && any)) {
+            for (int i = 0; i < 8; ++i) mq[i] = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 128; c += 16) {
+            for (int c = 0; c < 128; c += 2) mq[(c >> 1) & 7] = max3(mq[(c >> 1) & 7], x[c], x[c + 1]);
+            const float mx =
+                fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7]))) *
+                sl2;
+            bool raise;
+            if constexpr (kQuant) {
+              // power-of-two reference: the running max rounded up (log2 units),
+              // raised whenever it grows, so P <= 1 and O rescales exactly
+              const float m_new = ceilf(mx);
+              raise = m_new > m_run;
+              if (raise) {
+                m_use = m_new;
+                alpha = m_run == -INFINITY ? 0.f : exp2_int(m_run - m_new);
+              }
+            } else {
+              // lazy reference update
+              raise = mx > m_run + kRescaleThreshold;
+              if (raise) {
+                m_use = mx;
+                alpha = ex2_approx(m_run - mx);  // 0 on this warpgroup's first block
+              }
+            }
+            // The partial O holds only this warpgroup's earlier blocks, whose
+            // P.V retired before S of this block was committed.
+            if (__any_sync(0xffffffffu, raise && any)) {
+#pragma unroll
+              for (int c = 0; c < 128; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(my_o + lane_off + c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                tmem_st16(my_o + lane_off + c, v);
+              }
+              tmem_st_wait();
+            }
+            m_run = m_use;
+          }
+          // exponent arguments two at a time: x * scale_log2 - m_use
+          const uint64_t sc2 = pk2(sl2, sl2), nm2 = pk2(-m_use, -m_use);
+          uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial row sums
+#pragma unroll
+          for (int c = 0; c < 128; c += 32) {  // P as 16-bit pairs: columns [0, 64) of the S buffer
             uint32_t v[16];
-            tmem_ld16(my_o + lane_off + c, v);
-            tmem_ld_wait();
+            if constexpr (kQuant) {
+              // the row sum takes the unquantised P; the P.V operand is P
+              // quantised to NVFP4 in blocks of 16 keys, as code * scale (f16)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st16(my_o + lane_off + c, v);
-          }
-          tmem_st_wait();
-        }
-        m_run = m_use;
-        // exponent arguments two at a time: x * scale_log2 - m_use
-        const uint64_t sc2 = pk2(sl2, sl2), nm2 = pk2(-m_use, -m_use);
-        uint64_t ls2[4] = {0, 0, 0, 0};  // packed (+0, +0) partial row sums
+              for (int blk = 0; blk < 2; ++blk) {
+                float pb[16];
+                if (sparse) {
+                  // 2:4: of each group of 4 keys (aligned to the sequence's
+                  // first key) keep the 2 largest scores, equal scores by lower
+                  // key index; a key's rank counts the keys of its group that
+                  // beat it.  A group's max is always kept, so the row max
+                  // above is the max of the kept scores.
 #pragma unroll
-        for (int c = 0; c < 128; c += 32) {  // P as 16-bit pairs: columns [0, 64) of the S buffer
-          uint32_t v[16];
-          if constexpr (kQuant) {
-            // the row sum takes the unquantised P; the P.V operand is P
-            // quantised to NVFP4 in blocks of 16 keys, as code * scale (f16)
+                  for (int g4 = c + 16 * blk; g4 < c + 16 * blk + 16; g4 += 4) {
+                    const float a = x[g4], b = x[g4 + 1], cc = x[g4 + 2], d = x[g4 + 3];
+                    const int ab = a >= b, ac = a >= cc, ad = a >= d, bc = b >= cc, bd = b >= d, cd = cc >= d;
+                    const int ra = 3 - ab - ac - ad, rb = ab + 2 - bc - bd, rc = ac + bc + 1 - cd, rd = ad + bd + cd;
+                    x[g4] = ra < 2 ? a : -INFINITY;
+                    x[g4 + 1] = rb < 2 ? b : -INFINITY;
+                    x[g4 + 2] = rc < 2 ? cc : -INFINITY;
+                    x[g4 + 3] = rd < 2 ? d : -INFINITY;
+                  }
+                }
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-              float pb[16];
-              if (sparse) {
-                // 2:4: of each group of 4 keys (aligned to the sequence's
-                // first key) keep the 2 largest scores, equal scores by lower
-                // key index; a key's rank counts the keys of its group that
-                // beat it.  A group's max is always kept, so the row max
-                // above is the max of the kept scores.
+                for (int i = 0; i < 8; ++i) {
+                  float a0, a1;
+                  unpk2(fma2(pk2(x[c + 16 * blk + 2 * i], x[c + 16 * blk + 2 * i + 1]), sc2, nm2), a0, a1);
+                  pb[2 * i] = ex2_approx(a0);
+                  pb[2 * i + 1] = ex2_approx(a1);
+                  ls2[i & 3] = add2(ls2[i & 3], pk2(pb[2 * i], pb[2 * i + 1]));
+                }
+                // amax of the block: P >= 0, so a plain three-input max
+                float am = max3(pb[0], pb[1], pb[2]);
 #pragma unroll
-                for (int g4 = c + 16 * blk; g4 < c + 16 * blk + 16; g4 += 4) {
-                  const float a = x[g4], b = x[g4 + 1], cc = x[g4 + 2], d = x[g4 + 3];
-                  const int ab = a >= b, ac = a >= cc, ad = a >= d, bc = b >= cc, bd = b >= d, cd = cc >= d;
-                  const int ra = 3 - ab - ac - ad, rb = ab + 2 - bc - bd, rc = ac + bc + 1 - cd, rd = ad + bd + cd;
-                  x[g4] = ra < 2 ? a : -INFINITY;
-                  x[g4 + 1] = rb < 2 ? b : -INFINITY;
-                  x[g4 + 2] = rc < 2 ? cc : -INFINITY;
-                  x[g4 + 3] = rd < 2 ? d : -INFINITY;
+                for (int i = 3; i < 15; i += 2) am = max3(am, pb[i], pb[i + 1]);
+                am = fmaxf(am, pb[15]);
+                // block scale and 1/S in the reciprocal form, 1/S by the
+                // approximate reciprocal: its decisions differ from the exact
+                // quotient's only within a few float32 ulps of a midpoint
+                const uint32_t sb = cvt_e4m3(__fmul_rn(am, kf_p));
+                const float S = __fmul_rn(e4m3_to_f32(sb), kGsP);
+                float R;
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(R) : "f"(S));
+                if (!(S > 0.f)) R = 0.f;
+                const uint32_t cw2[2] = {encode8(pb, R), encode8(pb + 8, R)};
+                const uint32_t s2 = e4m3x2_to_f16x2_pair(sb | (sb << 8));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const uint32_t byte = (cw2[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+                  uint32_t h2;
+                  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
+                  const __half2 q2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&s2));
+                  v[8 * blk + i] = *reinterpret_cast<const uint32_t*>(&q2);
                 }
               }
+            } else {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
+              for (int i = 0; i < 16; ++i) {
                 float a0, a1;
-                unpk2(fma2(pk2(x[c + 16 * blk + 2 * i], x[c + 16 * blk + 2 * i + 1]), sc2, nm2), a0, a1);
-                pb[2 * i] = ex2_approx(a0);
-                pb[2 * i + 1] = ex2_approx(a1);
-                ls2[i & 3] = add2(ls2[i & 3], pk2(pb[2 * i], pb[2 * i + 1]));
-              }
-              // amax of the block: P >= 0, so a plain three-input max
-              float am = max3(pb[0], pb[1], pb[2]);
-#pragma unroll
-              for (int i = 3; i < 15; i += 2) am = max3(am, pb[i], pb[i + 1]);
-              am = fmaxf(am, pb[15]);
-              // block scale and 1/S in the reciprocal form, 1/S by the
-              // approximate reciprocal: its decisions differ from the exact
-              // quotient's only within a few float32 ulps of a midpoint
-              const uint32_t sb = cvt_e4m3(__fmul_rn(am, kf_p));
-              const float S = __fmul_rn(e4m3_to_f32(sb), kGsP);
-              float R;
-              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(R) : "f"(S));
-              if (!(S > 0.f)) R = 0.f;
-              const uint32_t cw2[2] = {encode8(pb, R), encode8(pb + 8, R)};
-              const uint32_t s2 = e4m3x2_to_f16x2_pair(sb | (sb << 8));
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const uint32_t byte = (cw2[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-                uint32_t h2;
-                asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
-                const __half2 q2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&s2));
-                v[8 * blk + i] = *reinterpret_cast<const uint32_t*>(&q2);
+                unpk2(fma2(pk2(x[c + 2 * i], x[c + 2 * i + 1]), sc2, nm2), a0, a1);
+                const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                v[i] = *reinterpret_cast<uint32_t*>(&h2);
               }
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float a0, a1;
-              unpk2(fma2(pk2(x[c + 2 * i], x[c + 2 * i + 1]), sc2, nm2), a0, a1);
-              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-              ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-              v[i] = *reinterpret_cast<uint32_t*>(&h2);
-            }
+            tmem_st16(my_s + lane_off + c / 2, v);
           }
-          tmem_st16(my_s + lane_off + c / 2, v);
-        }
-        float ls[8];
+          float ls[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) unpk2(ls2[i], ls[2 * i], ls[2 * i + 1]);
-        l_run = l_run * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+          for (int i = 0; i < 4; ++i) unpk2(ls2[i], ls[2 * i], ls[2 * i + 1]);
+          l_blk = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+          if (!fast || !__any_sync(0xffffffffu, !(l_blk <= kSumLimit))) break;
+          // P is formed again against the raised reference; its stores
+          // replace these before P_g is signalled
+          tmem_st_wait();
+          fast = false;
+        }
+        l_run = l_run * alpha + l_blk;
         tmem_st_wait();
         tc_fence_before();
         if (!warp_wait(&bars.v_full[gb & 1], (gb >> 1) & 1, err, &abort_s)) {
