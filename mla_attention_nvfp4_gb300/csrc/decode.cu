@@ -727,12 +727,6 @@ __device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, ui
   }
 }
 
-// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte-aligned address;
-// writes nothing and completes on its own.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 template <int kRecord>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -751,15 +745,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decod
   int64_t row0;
   bool direct;
   if (p.plan_items != nullptr) {
-    // While the plan is built: a plan with one chunk per sequence lists
-    // the sequences in order, so this pair's likely sequence is its item
-    // index; its query rows are brought into L2 (one head row per thread,
-    // the pair's two CTAs taking alternate heads; a prefetch changes no result)
-    {
-      const int guess = blockIdx.x >> 1, h = hg * kHeads + static_cast<int>(threadIdx.x);
-      if (guess < p.batch && threadIdx.x < kHeads && (threadIdx.x & 1) == rank && h < p.num_heads)
-        prefetch_l2(p.q + (static_cast<int64_t>(guess) * p.num_heads + h) * 576, 576 * 2);
-    }
     // launched as a programmatic dependent of the plan kernel: its tables
     // are read only once that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
