@@ -168,3 +168,26 @@ def test_prefill_random_mixes(seed):
                                 f"prefill mix {lens} H{heads}")
     assert counts["rate"] <= FUSED_FLIP_RATE, counts
     assert_lse_close(lse, l_ref, f"prefill lse mix {lens} H{heads}")
+
+
+@pytest.mark.parametrize("growth", [3.0, 12.0])
+def test_prefill_growing_scores(growth):
+    # keys of key block j scaled by 1 + growth * j: a row's scores jump by
+    # tens of log2 units from block to block, so the softmax's P formed
+    # against its running reference overflows its limit and is formed again
+    # against the block's max, and the partial O is rescaled, on most blocks
+    w = workloads.prefill("growing", seq_lens=(700, 300, 129), heads=2, seed=int(growth))
+    blk = torch.zeros(w.total_tokens)
+    cu = w.cu_seqlens.tolist()
+    for a, e in zip(cu[:-1], cu[1:]):
+        blk[a:e] = torch.arange(e - a) // 128
+    w.k = (w.k.float() * (1.0 + growth * blk)[:, None, None]).to(torch.bfloat16)
+    gs = oracle_gs(w.v)
+    codes, sf, lse = _run(w, gs)
+    o_ref, l_ref, o_abs = attention.prefill(f32(w.q), f32(w.k), f32(w.v), w.cu_seqlens.numpy(),
+                                             w.softmax_scale, with_abs=True)
+    T = w.total_tokens
+    counts = check_fused_output(codes, sf, o_ref.reshape(T, 2 * 128), o_abs.reshape(T, 2 * 128), gs,
+                                f"prefill growing scores x{growth}")
+    assert counts["rate"] <= FUSED_FLIP_RATE, counts
+    assert_lse_close(lse, l_ref, f"prefill lse growing scores x{growth}")
