@@ -512,11 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float x[128];
 #pragma unroll
-        for (int c = 0; c < 128; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(my_s + lane_off + c, v);
+        for (int c = 0; c < 128; c += 64) {
+          uint32_t v[64];
+          tmem_ld64(my_s + lane_off + c, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 64; ++i) x[c + i] = __uint_as_float(v[i]);
         }
         tmem_ld_wait();
         const int key0 = j * kBN;
