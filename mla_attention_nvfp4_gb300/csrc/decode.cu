@@ -121,6 +121,12 @@ struct Params {
   const int32_t* page_table;
   int64_t pt_stride;
   int page_size;
+  // t / page_size for 0 <= t < 2^31 as (umulhi(t, pg_magic) + t) >> pg_shift
+  // (division by an invariant integer using multiplication, Granlund and
+  // Montgomery 1994): pg_shift = ceil(log2 page_size),
+  // pg_magic = floor(2^32 (2^pg_shift - page_size) / page_size) + 1
+  uint32_t pg_magic;
+  int pg_shift;
   const int32_t* seq_lens;
   const int32_t* topk;
   int topk_n;
@@ -182,12 +188,17 @@ __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) {
   return v;
 }
 
+__device__ __forceinline__ int page_of(const Params& p, int t) {
+  const uint32_t u = static_cast<uint32_t>(t);
+  return static_cast<int>((__umulhi(u, p.pg_magic) + u) >> p.pg_shift);
+}
+
 __device__ __forceinline__ int32_t load_index(const Params& p, int b, int t) {
   if (p.topk != nullptr) {
     const int tc = min(max(t, 0), max(p.topk_n - 1, 0));
     return ldg_i32(p.topk + static_cast<int64_t>(b) * p.topk_n + tc);
   }
-  const int pi = min(max(t, 0) / p.page_size, static_cast<int>(p.pt_stride) - 1);
+  const int pi = min(page_of(p, max(t, 0)), static_cast<int>(p.pt_stride) - 1);
   return ldg_i32(p.page_table + static_cast<int64_t>(b) * p.pt_stride + pi);
 }
 
@@ -198,11 +209,12 @@ __device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t,
     if (idx < 0) return -1;  // padding entry
     slot = idx;
   } else {
-    if (t / p.page_size >= p.pt_stride || idx < 0) {
+    const int pg = page_of(p, t);
+    if (pg >= p.pt_stride || idx < 0) {
       bad = true;
       return -1;
     }
-    slot = static_cast<int64_t>(idx) * p.page_size + t % p.page_size;
+    slot = static_cast<int64_t>(idx) * p.page_size + (t - pg * p.page_size);
   }
   if (slot >= p.num_slots) {
     bad = true;
@@ -1785,6 +1797,13 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
   p.page_table = a.page_table;
   p.pt_stride = a.page_table_stride;
   p.page_size = a.page_size;
+  {  // the page division's multiplier and shift (page_size >= 1 in paged mode)
+    const int d = a.page_size > 0 ? a.page_size : 1;
+    int l = 0;
+    while ((int64_t(1) << l) < d) ++l;
+    p.pg_shift = l;
+    p.pg_magic = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  }
   p.seq_lens = a.seq_lens;
   p.topk = a.topk_indices;
   p.topk_n = a.topk;
