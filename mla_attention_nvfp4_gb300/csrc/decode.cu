@@ -121,10 +121,7 @@ struct Params {
   const int32_t* page_table;
   int64_t pt_stride;
   int page_size;
-  // t / page_size for 0 <= t < 2^31 as (umulhi(t, pg_magic) + t) >> pg_shift
-  // (division by an invariant integer using multiplication, Granlund and
-  // Montgomery 1994): pg_shift = ceil(log2 page_size),
-  // pg_magic = floor(2^32 (2^pg_shift - page_size) / page_size) + 1
+  // page_size's multiplier and shift for div_magic
   uint32_t pg_magic;
   int pg_shift;
   const int32_t* seq_lens;
@@ -188,9 +185,9 @@ __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) {
   return v;
 }
 
+// t / page_size for 0 <= t < 2^31
 __device__ __forceinline__ int page_of(const Params& p, int t) {
-  const uint32_t u = static_cast<uint32_t>(t);
-  return static_cast<int>((__umulhi(u, p.pg_magic) + u) >> p.pg_shift);
+  return static_cast<int>(div_magic(static_cast<uint32_t>(t), p.pg_magic, p.pg_shift));
 }
 
 __device__ __forceinline__ int32_t load_index(const Params& p, int b, int t) {
@@ -1797,13 +1794,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
   p.page_table = a.page_table;
   p.pt_stride = a.page_table_stride;
   p.page_size = a.page_size;
-  {  // the page division's multiplier and shift (page_size >= 1 in paged mode)
-    const int d = a.page_size > 0 ? a.page_size : 1;
-    int l = 0;
-    while ((int64_t(1) << l) < d) ++l;
-    p.pg_shift = l;
-    p.pg_magic = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
-  }
+  magic_divisor(a.page_size, &p.pg_magic, &p.pg_shift);
   p.seq_lens = a.seq_lens;
   p.topk = a.topk_indices;
   p.topk_n = a.topk;

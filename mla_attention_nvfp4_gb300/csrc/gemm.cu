@@ -80,6 +80,9 @@ struct Params {
   const float* gs_w;
   __nv_bfloat16* c;
   int64_t ldc;
+  int tiles_n;        // 256-column tiles
+  uint32_t tn_magic;  // tiles_n's multiplier and shift for div_magic
+  int tn_shift;
   uint32_t* error_word;
 };
 
@@ -143,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sSfa = [&](int s) { return s0 + s * kStageBytes + kABytes + kBBytes; };
   auto sSfb = [&](int s) { return s0 + s * kStageBytes + kABytes + kBBytes + kSfaBytes; };
 
-  const int64_t tiles_m = (p.M + kBM - 1) / kBM, tiles_n = p.N / kBN + (p.N % kBN != 0);
-  const int64_t n_tiles = tiles_m * tiles_n;
+  const int64_t tiles_m = (p.M + kBM - 1) / kBM, tiles_n = p.tiles_n;
+  const int64_t n_tiles = tiles_m * tiles_n;  // < 2^31 (checked at launch)
   const int nk = static_cast<int>(p.K / 256);
   uint32_t* err = p.error_word;
 
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_w);
       int it = 0;  // stage fills so far
       for (int64_t t = blockIdx.x; t < n_tiles && !abort_s; t += gridDim.x) {
-        const int64_t mt = t / tiles_n, ntile = t % tiles_n;
+        const int64_t mt = div_magic(static_cast<uint32_t>(t), p.tn_magic, p.tn_shift), ntile = t - mt * tiles_n;
         // the W scale rows of this tile: one or two 128-row tiles (N is a
         // multiple of 128; the second is absent on a half tile at the end)
         const int sfb_tiles = (ntile * kBN + 128 < p.N) ? 2 : 1;
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_i) {
       if (!mbar_wait(&bars.acc_full, tile_i & 1, err, &abort_s)) break;
       tc_fence_after();
-      const int64_t mt = t / tiles_n, ntile = t % tiles_n;
+      const int64_t mt = div_magic(static_cast<uint32_t>(t), p.tn_magic, p.tn_shift), ntile = t - mt * tiles_n;
       const int64_t row = mt * kBM + r;
       const int64_t n0 = ntile * kBN;
       __nv_bfloat16* crow = p.c + row * p.ldc + n0;
@@ -350,6 +353,9 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream, int num_sms) {
   p.ldc = a.ldc;
   p.error_word = a.error_word;
   const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
+  if (tiles > (int64_t(1) << 31) - 1) return MLA_ERR_INVALID_ARG;
+  p.tiles_n = static_cast<int>((a.N + kBN - 1) / kBN);
+  magic_divisor(p.tiles_n, &p.tn_magic, &p.tn_shift);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   if (const int st = smem_limit_once(reinterpret_cast<const void*>(nvfp4_gemm_kernel), static_cast<int>(kSmAlloc), 4))
     return st;

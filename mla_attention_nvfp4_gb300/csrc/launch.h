@@ -10,6 +10,18 @@
 
 namespace mla {
 
+// Division by an invariant integer using multiplication (Granlund and
+// Montgomery 1994): for a divisor d >= 1, shift = ceil(log2 d) and
+// magic = floor(2^32 (2^shift - d) / d) + 1 give n / d as
+// (umulhi(n, magic) + n) >> shift, exactly, for every n < 2^31.
+inline void magic_divisor(int d, uint32_t* magic, int* shift) {
+  d = d > 0 ? d : 1;
+  int l = 0;
+  while ((int64_t(1) << l) < d) ++l;
+  *shift = l;
+  *magic = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+}
+
 // Record a CUDA failure for mla_nvfp4_last_error() and map it to a status.
 int cuda_status(cudaError_t e);
 // MLA_OK after a successful launch sequence, else the recorded failure.

@@ -105,9 +105,7 @@ struct Params {
   int num_heads;
   int q_tiles;          // query tiles of the longest sequence
   uint32_t num_items;   // q_tiles * num_seqs * num_heads
-  // n / q_tiles and n / num_heads (n < 2^31) as (umulhi(n, magic) + n) >> shift
-  // (division by an invariant integer using multiplication, Granlund and
-  // Montgomery 1994)
+  // multipliers and shifts of q_tiles and num_heads for div_magic
   uint32_t qt_magic, h_magic;
   int qt_shift, h_shift;
   uint32_t* sched;      // [0] next item, [1] CTAs finished; zero between launches
@@ -162,10 +160,6 @@ struct Item {
   int k_begin, n_k;  // key rows of the item's sequence (its own tokens unless a key table is given)
   bool valid;
 };
-
-__device__ __forceinline__ uint32_t div_magic(uint32_t n, uint32_t magic, int shift) {
-  return (__umulhi(n, magic) + n) >> shift;
-}
 
 __device__ __forceinline__ Item item_at(const Params& p, uint32_t idx, bool& bad) {
   const uint32_t group = div_magic(idx, p.qt_magic, p.qt_shift);
@@ -856,16 +850,6 @@ int sched_counter(uint32_t** out) {
   return MLA_OK;
 }
 
-// Multiplier and shift for div_magic by d >= 1: shift = ceil(log2 d),
-// magic = floor(2^32 (2^shift - d) / d) + 1 (exact for every n < 2^31).
-void magic_of(int d, uint32_t* magic, int* shift) {
-  d = d > 0 ? d : 1;
-  int l = 0;
-  while ((int64_t(1) << l) < d) ++l;
-  *shift = l;
-  *magic = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
-}
-
 }  // namespace
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms) {
@@ -885,8 +869,8 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int num_sms) {
   const int64_t items = static_cast<int64_t>(p.q_tiles) * a.num_seqs * a.num_heads;
   if (items > (int64_t(1) << 31) - 1) return MLA_ERR_INVALID_ARG;
   p.num_items = static_cast<uint32_t>(items);
-  magic_of(p.q_tiles, &p.qt_magic, &p.qt_shift);
-  magic_of(a.num_heads, &p.h_magic, &p.h_shift);
+  magic_divisor(p.q_tiles, &p.qt_magic, &p.qt_shift);
+  magic_divisor(a.num_heads, &p.h_magic, &p.h_shift);
   if (const int st = sched_counter(&p.sched)) return st;
   p.scale_log2 = a.softmax_scale * kLog2e;
   p.gs = a.gs;

@@ -236,5 +236,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// n / d for n < 2^31 from the divisor's multiplier and shift (see
+// mla::magic_divisor).
+__device__ __forceinline__ uint32_t div_magic(uint32_t n, uint32_t magic, int shift) {
+  return (__umulhi(n, magic) + n) >> shift;
+}
+
 }  // namespace sm100
 }  // namespace mla
