@@ -56,6 +56,7 @@ class DecodeWorkload:
     page_table: Optional[torch.Tensor] = None  # [B, max_pages] int32 (paged mode)
     topk_indices: Optional[torch.Tensor] = None  # [B, topk] int32 (top-k mode)
     softmax_scale: float = 1.0 / math.sqrt(192.0)
+    page_size: int = PAGE  # tokens per page (paged mode)
     meta: dict = field(default_factory=dict)
 
     @property
@@ -97,9 +98,9 @@ def _randn_bf16(shape, g, device) -> torch.Tensor:
     return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
-def _paged_layout(seq_lens, perm_pages: bool, g, device):
+def _paged_layout(seq_lens, perm_pages: bool, g, device, page=PAGE):
     """Page table and slot mapping for sequences laid out page by page."""
-    pages_per_seq = [(int(L) + PAGE - 1) // PAGE for L in seq_lens]
+    pages_per_seq = [(int(L) + page - 1) // page for L in seq_lens]
     n_pages = sum(pages_per_seq)
     if perm_pages:
         ids = torch.randperm(n_pages, generator=g, device=device).to("cpu")
@@ -113,15 +114,15 @@ def _paged_layout(seq_lens, perm_pages: bool, g, device):
         table[b, :npg] = ids[pos:pos + npg].to(torch.int32)
         pos += npg
         t = torch.arange(int(L))
-        slots.append(table[b, t // PAGE].to(torch.int64) * PAGE + t % PAGE)
-    return table, torch.cat(slots), n_pages * PAGE
+        slots.append(table[b, t // page].to(torch.int64) * page + t % page)
+    return table, torch.cat(slots), n_pages * page
 
 
 def decode_paged(name, batch, heads, seq_lens, record_bytes, perm_pages, outlier_frac=0.0,
-                 outlier_mult=1.0, seed=0, device="cpu") -> DecodeWorkload:
+                 outlier_mult=1.0, seed=0, device="cpu", page_size=PAGE) -> DecodeWorkload:
     g = _gen(seed, device)
     seq_lens = [int(x) for x in seq_lens]
-    table, slots, num_slots = _paged_layout(seq_lens, perm_pages, g, device)
+    table, slots, num_slots = _paged_layout(seq_lens, perm_pages, g, device, page_size)
     T = int(sum(seq_lens))
     q = _randn_bf16((batch, heads, D_QK), g, device)
     kv = torch.randn((T, D_LATENT), generator=g, device=device, dtype=torch.float32)
@@ -134,7 +135,7 @@ def decode_paged(name, batch, heads, seq_lens, record_bytes, perm_pages, outlier
         name=name, batch=batch, heads=heads, record_bytes=record_bytes, q=q, kv_c=kv_c,
         k_pe=k_pe, slot_mapping=slots.to(device), num_slots=num_slots,
         seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=device),
-        page_table=table.to(device))
+        page_table=table.to(device), page_size=page_size)
 
 
 def decode_tiny(seed=0, device="cpu", heads=16, seq_lens=(64, 100), record_bytes=432) -> DecodeWorkload:

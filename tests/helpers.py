@@ -39,7 +39,7 @@ def oracle_cache(w, gs) -> np.ndarray:
 
 def oracle_slots(w):
     if w.paged:
-        return attention.decode_slots_paged(w.page_table.cpu().numpy(), w.seq_lens.cpu().numpy(), 64)
+        return attention.decode_slots_paged(w.page_table.cpu().numpy(), w.seq_lens.cpu().numpy(), w.page_size)
     return attention.decode_slots_topk(w.topk_indices.cpu().numpy())
 
 

@@ -21,13 +21,28 @@ def run_gpu(w, gs, num_splits=0):
     gst = torch.tensor([gs], device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     mla.mla_nvfp4_cache_write(w.kv_c.to(DEV), w.k_pe.to(DEV), w.slot_mapping.to(DEV), cache, gst, err)
-    kw = dict(page_table=w.page_table.to(DEV), seq_lens=w.seq_lens.to(DEV)) if w.paged else \
-        dict(topk_indices=w.topk_indices.to(DEV))
+    kw = dict(page_table=w.page_table.to(DEV), seq_lens=w.seq_lens.to(DEV), page_size=w.page_size) if w.paged \
+        else dict(topk_indices=w.topk_indices.to(DEV))
     out, lse = mla.mla_nvfp4_decode(w.q.to(DEV), cache, gst, w.softmax_scale, num_splits=num_splits,
                                     error_word=err, return_lse=True, **kw)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     return f32(out), f32(lse)
+
+
+@pytest.mark.parametrize("page_size", [1, 16, 48, 100, 64])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_decode_page_sizes(page_size, splits):
+    # a key's page and offset within it are taken with the page size's
+    # multiplier and shift: page sizes that are and are not powers of two,
+    # sequences over several pages ending mid-page, permuted pages
+    w = workloads.decode_paged("pages", 4, 32, (1, 257, 700, 1000), 432, perm_pages=True, seed=page_size,
+                               page_size=page_size)
+    gs = oracle_gs(w.kv_c)
+    out, lse = run_gpu(w, gs, splits)
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(out, o_ref, f"decode page size {page_size} splits={splits}", o_abs)
+    assert_lse_close(lse, l_ref, f"decode page size {page_size} lse")
 
 
 def run_oracle(w, gs):
