@@ -163,7 +163,7 @@ struct alignas(8) SoftX {
   uint64_t mx_full[2], fin, qx;
   float v[2][kHeads];
 };
-static_assert(kSmAlloc + sizeof(SoftX) + 256 <= 232448, "shared memory budget of the exact kernel");
+static_assert(kSmAlloc + sizeof(SoftX) + kHeads * sizeof(float) + 256 <= 232448, "shared memory budget of the exact kernel");
 
 struct alignas(8) Barriers {
   uint64_t q_ready;
@@ -736,11 +736,220 @@ __device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, ui
   }
 }
 
+// The exact kernel's online softmax over an item's tiles, with four threads
+// per pair of heads: the warp of TMEM subpartition q and group g (warps
+// 0..3: g = 0, 12..15: g = 1) takes heads 32q + 16g .. +15, and its thread t
+// heads 32q + 16g + t/4 and + 8, keys 8i + 2(t%4) and + 1 (i = 0..7) of each
+// 64-key tile, the tcgen05.ld 16x256b layout.  A head's four threads are
+// lanes of one warp: they share the tile maxima (and, at the end, the row
+// sums) by shuffles, and each writes its keys' P pairs into the columns the
+// 16x128b store gives it, which are its own (key pair k in column k).
+// Otherwise as softmax_tiles: masking of padding keys, lazy reference raise
+// with an O rescale, P as f16 for P.V, running row sums.
+__device__ __forceinline__ void softmax_quad(const Params& p, Barriers& bars, volatile int& abort_s, uint32_t tmem,
+                                             uint32_t lane_base, int b, int tile0, int nt, int n_keys,
+                                             const float (&score_scale)[2], bool& ok, float (&m_run)[2],
+                                             float (&l_run)[2]) {
+  uint32_t* err = p.error_word;
+  const int lane = threadIdx.x & 31, kq = 2 * (lane & 3);  // the thread's first key of each 8
+  // per-tile validity: lane checks keys lane and 32 + lane
+  int32_t ia = load_index(p, b, tile0 * kTok + lane);
+  int32_t ib = load_index(p, b, tile0 * kTok + 32 + lane);
+  for (int j = 0; j < nt; ++j) {
+    const int pb = j & 1;
+    const int key = (tile0 + j) * kTok + lane;
+    bool badv = false;
+    const unsigned va = __ballot_sync(0xffffffffu, key_slot(p, ia, key, n_keys, badv) >= 0);
+    const unsigned vb = __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0);
+    if (j + 1 < nt) {
+      ia = load_index(p, b, key + kTok);
+      ib = load_index(p, b, key + kTok + 32);
+    }
+    if (!bar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // raw scores of both heads: x[h][2i + e] is key 8i + kq + e
+    float x[2][16];
+    {
+      uint32_t v[32];
+      tmem_ld_16x256b_x8(tmem + lane_base + col_s(pb), v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[0][2 * i] = __uint_as_float(v[4 * i]);
+        x[0][2 * i + 1] = __uint_as_float(v[4 * i + 1]);
+        x[1][2 * i] = __uint_as_float(v[4 * i + 2]);
+        x[1][2 * i + 1] = __uint_as_float(v[4 * i + 3]);
+      }
+    }
+    // padding keys at -inf; the maxima of the raw scores (score_scale > 0),
+    // over the head's four threads; the scale is applied in the exponent
+    if ((va & vb) != 0xffffffffu) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 8 * i + kq + e;
+          if (!(((k < 32 ? va : vb) >> (k & 31)) & 1u)) {
+            x[0][2 * i + e] = -INFINITY;
+            x[1][2 * i + e] = -INFINITY;
+          }
+        }
+    }
+    float mx[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float m0 = max3(x[h][0], x[h][1], x[h][2]), m1 = max3(x[h][3], x[h][4], x[h][5]);
+      m0 = max3(m0, x[h][6], x[h][7]);
+      m1 = max3(m1, x[h][8], x[h][9]);
+      m0 = max3(m0, x[h][10], x[h][11]);
+      m1 = max3(m1, x[h][12], x[h][13]);
+      float m = max3(m0, m1, fmaxf(x[h][14], x[h][15]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      mx[h] = m * score_scale[h];  // log2 units
+    }
+    float m_use[2], alpha[2];
+    bool raise = false;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      m_use[h] = m_run[h];
+      alpha[h] = 1.f;
+      if (mx[h] > m_run[h] + kRescaleThreshold) {
+        m_use[h] = mx[h];
+        alpha[h] = ex2_approx(m_run[h] - mx[h]);
+        raise = true;
+      }
+    }
+    // an O rescale must follow every earlier P.V and precede PV(j).
+    // PV(j-1) and PV(j-2) come from different issuers; each issuer's
+    // earlier P.V products retire before its later ones.
+    if (__any_sync(0xffffffffu, raise && j > 0)) {
+      if (!bar_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, &abort_s) ||
+          (j >= 2 && !bar_wait(&bars.pv_done[j & 1], ((j - 2) >> 1) & 1, err, &abort_s))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 256; c += 64) {
+        uint32_t v[32];
+        tmem_ld_16x256b_x8(tmem + lane_base + kTO + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[(i >> 1) & 1]);
+        tmem_st_16x256b_x8(tmem + lane_base + kTO + c, v);
+      }
+      tmem_st_wait();
+    }
+    // probabilities two at a time: x * score_scale - m_use, P <= 2^14
+    // (lazy reference), f16 operand pairs; the row sums in packed halves
+    uint32_t pv[16];  // pv[2i + h]: head h, key pair 8i + kq (column 4i + kq / 2)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      m_run[h] = m_use[h];
+      const float m_ref = (m_use[h] == -INFINITY) ? 0.f : m_use[h];  // no valid key so far
+      const uint64_t sc2 = pk2(score_scale[h], score_scale[h]), nm2 = pk2(-m_ref, -m_ref);
+      uint64_t ls2[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float a0, a1;
+        unpk2(fma2(pk2(x[h][2 * i], x[h][2 * i + 1]), sc2, nm2), a0, a1);
+        const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+        ls2[i & 1] = add2(ls2[i & 1], pk2(p0, p1));
+        pv[2 * i + h] = pack_f16(p0, p1);
+      }
+      float s0, s1, s2, s3;
+      unpk2(ls2[0], s0, s1);
+      unpk2(ls2[1], s2, s3);
+      l_run[h] = l_run[h] * alpha[h] + ((s0 + s1) + (s2 + s3));
+    }
+    // P(j) over S(j): the warp's own lanes, read above; the buffer's
+    // previous P was read by PV(j-2), which ran before QK(j) wrote S(j)
+    tmem_st_16x128b_x8(tmem + lane_base + col_s(pb), pv);
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&bars.p_full[pb]);
+  }
+}
+
+// The output of an item for softmax_quad's heads (thread: heads `head0`
+// and head0 + 8, O columns 8i + 2(t%4), +1 of each 64): O / l with the row
+// sums of the head's four threads, scaled by gs, and the LSE, as the final
+// bf16 output when the item is its sequence's only one, else as an fp32
+// partial row for the merge.  TMEM loads are warp-collective, so every lane
+// loads; only stores depend on the head.
+__device__ __forceinline__ void write_partial_quad(const Params& p, uint32_t tmem, uint32_t lane_base, bool ok, int nt,
+                                                   const float (&m_run)[2], float (&l_run)[2], float gs,
+                                                   int64_t row0, int b, int head0, bool direct, int rank) {
+  const int lane = threadIdx.x & 31, kq = 2 * (lane & 3);
+  const bool live = __all_sync(0xffffffffu, ok) && nt > 0;
+  float f[2];
+  bool have[2], head_ok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float l = l_run[h];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l_run[h] = l;
+    have[h] = live && l > 0.f;
+    f[h] = have[h] ? gs / l : 0.f;
+    head_ok[h] = head0 + 8 * h < p.num_heads;
+  }
+  if (live) tc_fence_after();
+#pragma unroll 1
+  for (int c = 0; c < 256; c += 64) {
+    uint32_t v[32];
+    if (live) {
+      tmem_ld_16x256b_x8(tmem + lane_base + kTO + c, v);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0u;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (!head_ok[h]) continue;
+      const int head = head0 + 8 * h;
+      if (direct) {
+        __nv_bfloat16* dst = p.out + (static_cast<int64_t>(b) * p.num_heads + head) * 512 + 256 * rank + c + kq;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[4 * i + 2 * h]) * f[h],
+                                                    __uint_as_float(v[4 * i + 2 * h + 1]) * f[h]);
+          *reinterpret_cast<__nv_bfloat162*>(dst + 8 * i) = h2;
+        }
+      } else {
+        float* dst = p.part_o + (row0 + head) * 512 + 256 * rank + c + kq;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float2*>(dst + 8 * i) =
+              make_float2(__uint_as_float(v[4 * i + 2 * h]) * f[h], __uint_as_float(v[4 * i + 2 * h + 1]) * f[h]);
+      }
+    }
+  }
+  if (rank == 0 && (lane & 3) == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (!head_ok[h]) continue;
+      const int head = head0 + 8 * h;
+      const float l = have[h] ? (m_run[h] + log2f(l_run[h])) * kLn2 : -INFINITY;
+      if (!direct)
+        p.part_lse[row0 + head] = l;
+      else if (p.lse != nullptr)
+        p.lse[static_cast<int64_t>(b) * p.num_heads + head] = l;
+    }
+  }
+}
+
 template <int kRecord>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   __shared__ SoftX xch;
+  __shared__ float score_scale_s[kHeads];  // per head row: the softmax scale with its query's sigma
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
 
@@ -917,7 +1126,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decod
     const bool gs_ok = scale_ok(gs);
     float score_scale = p.softmax_scale * gs * kLog2e;
     bool ok = true;
-    float m_run = -INFINITY, l_run = 0.f;
     if (nt > 0) {
       // Q -> f16 operands: TMEM [sigma*q_pe/gs, sigma*q_lat[0:192]], shared
       // memory sigma*q_lat[192:512] (swizzled rows).
@@ -994,18 +1202,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decod
 #pragma unroll 1
         for (int c = 0; c < 128; c += 16) tmem_st16(tmem + lane_off + kTO + 128 * half + c, z);
       }
+      if (half == 0) score_scale_s[hr] = score_scale;
       fence_async_smem();
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.q_ready);
-
-      if (ok)
-        softmax_tiles<2>(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run, half,
-                         &xch, hr);
+    }
+    // the softmax and the output: four threads per pair of heads (the
+    // 16-lane TMEM shapes), heads qh and qh + 8 of the group
+    const int qh = (warp & 3) * 32 + 16 * half + (lane >> 2);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32 + 16 * half) << 16;
+    float m_q[2] = {-INFINITY, -INFINITY}, l_q[2] = {0.f, 0.f};
+    if (nt > 0) {
+      // every head's scale is written before q_ready completes
+      if (ok) ok = bar_wait(&bars.q_ready, 0, err, &abort_s);
+      const float sc[2] = {score_scale_s[qh], score_scale_s[qh + 8]};
+      if (ok) softmax_quad(p, bars, abort_s, tmem, lane_base, b, tile0, nt, n_keys, sc, ok, m_q, l_q);
       if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
     }
-    write_partial<2>(p, tmem, lane_off, ok, nt, m_run, l_run, gs, row0, b, head, head_ok, direct, rank, half, &xch,
-                     hr, &abort_s);
+    write_partial_quad(p, tmem, lane_base, ok, nt, m_q, l_q, gs, row0, b, hg * kHeads + qh, direct, rank);
   }
   tc_fence_before();
   __syncthreads();
