@@ -44,16 +44,16 @@
 //   (one per tile parity) suffice.
 //
 // Warp roles (512 threads):
-//   warps 0..3, 12..15  Q staging, online softmax, lazy O rescale,
-//                partial-output epilogue: two threads per head, warp w
-//                reading TMEM lanes 32 (w % 4)..+32; warps 0..3 take keys
-//                [0, 32) of each tile and O columns [0, 128), warps 12..15
-//                keys [32, 64) and O columns [128, 256).  The pair exchanges
-//                each tile's maximum through shared memory (both then take
-//                the same reference and rescale decisions) and keeps two row
-//                sums, added at the end.  Halving the per-thread softmax
-//                (~3,300 cycles a 64-key tile on one thread per head) was
-//                the kernel's shortest path to a shorter tile.
+//   warps 0..3, 12..15  Q staging (two threads per head: warp w writes
+//                TMEM lanes 32 (w % 4)..+32, warps 0..3 one half of each
+//                query row, warps 12..15 the other), then the online
+//                softmax, lazy O rescale and partial-output epilogue with
+//                four threads per pair of heads: warp w takes TMEM lanes
+//                32 (w % 4) + 16 [w >= 12] .. +16 through the 16-lane
+//                shapes, thread t heads t/4 and t/4 + 8 of them and 16 of a
+//                tile's 64 keys, so a head's threads share maxima and row
+//                sums by shuffles (an earlier split over two warps had to
+//                meet in shared memory behind an mbarrier every tile).
 //   warps 4, 11  MMA issuers (one thread each) for even and odd tiles;
 //                warp 4 owns the TMEM allocation.
 //   warps 5..10  dequantisation: thread = (key, third of the record), 16-byte
@@ -525,13 +525,13 @@ __device__ bool dequant_role(const DeqCtx& c) {
 // The online softmax over an item's tiles (thread = head row; warps 0..3
 // read their lane quarter of the scores): raw scores from TMEM, masking of
 // padding keys, lazy max raise with an O rescale, probabilities as f16 into
-// the scores' columns for P.V, running row sum.  Shared by both decode
-// kernels.
+// the scores' columns for P.V, running row sum.  The NVFP4-query kernel's
+// (kSplit = 1; the exact kernel uses softmax_quad).
 //
-// kSplit = 2 (exact kernel): two threads per head, thread `half` taking keys
-// [32 half, 32 half + 32) of each tile and O columns [128 half, 128 half +
-// 128) for the rescale; the halves exchange their tile maxima through `x`
-// (so both take the same reference and the same rescale decisions) and keep
+// kSplit = 2: two threads per head, thread `half` taking keys [32 half,
+// 32 half + 32) of each tile and O columns [128 half, 128 half + 128) for
+// the rescale; the halves exchange their tile maxima through `x` (so both
+// take the same reference and the same rescale decisions) and keep
 // separate row sums.  The exchange also orders the halves' score loads
 // before the P stores that overwrite them.
 template <int kSplit>
@@ -1115,8 +1115,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decod
     if (bad && rank == 0 && q == 0) flag_error(err, MLA_DEVERR_BOUNDS);
   } else {
     // ------------------------------------------- softmax and epilogue
-    // warps 0..3 (half 0) and 12..15 (half 1): two threads per head; warp w
-    // reads TMEM lanes 32 (w % 4) .. +32
+    // warps 0..3 (half 0) and 12..15 (half 1): two threads per head for the
+    // query staging, warp w writing TMEM lanes 32 (w % 4) .. +32
     const int half = warp >= kSoftWarp2 ? 1 : 0;
     const int hr = (warp & 3) * 32 + lane;  // head row within the group
     const int head = hg * kHeads + hr;
