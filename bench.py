@@ -47,7 +47,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA NVFP4 decode HBM GB/s (% peak); prefill TFLOP/s with fused NVFP4 output"
 UNIT = "GB/s"
 WORKLOAD = ("decode_dsv3: B64 H128 L4096 paged 432B NVFP4 cache (cache write of its 262144 tokens + "
-            "planned split-K decode) + prefill_8x4096: causal varlen H128 qk192 v128 fused NVFP4 out + "
+            "split-K decode, planned from the host-held lengths) + prefill_8x4096: causal varlen H128 qk192 v128 fused NVFP4 out + "
             "decode_mixed: B128 H128 L~logU(1k,32k) 368B fp8-RoPE records (cache write + decode) + "
             "decode_topk: B32 H128 2048 of 65536 tokens, 432B + gemm_oproj: NVFP4 [32768 x 16384] x [7168 x 16384]^T "
             "on the prefill output")
@@ -381,7 +381,7 @@ def summarize(leg_ms, meta, world, peaks, peak_src, headline="decode_dsv3"):
     }
 
 
-def extension_legs(mla, w, ds, p, gsp, codes, scales, err, dev):
+def extension_legs(mla, w, ds, p, gsp, codes, scales, err, dev, step_splits):
     """Legs of the extensions of the hot path, timed in the full case:
     decode with the NVFP4 query, the chunked-context prefill, the
     fake-quantised prefill (dense and 2:4).  Returns (legs, meta, launches
@@ -393,7 +393,7 @@ def extension_legs(mla, w, ds, p, gsp, codes, scales, err, dev):
 
     def leg_q4():
         mla.mla_nvfp4_decode_q4(w.q, ds["cache"], ds["gs"], w.softmax_scale, gq, out=ds["out"], lse=ds["lse"],
-                                workspace=ds["ws"], error_word=err, num_splits=ds["splits"], **ds["kw"])
+                                workspace=ds["ws"], error_word=err, num_splits=step_splits(ds), **ds["kw"])
 
     # chunked-context prefill: the prefill's tokens after a context of the
     # same length per sequence; the context's latent gathered from the
@@ -442,7 +442,7 @@ def extension_legs(mla, w, ds, p, gsp, codes, scales, err, dev):
     legs = [("decode_dsv3_q4", leg_q4), ("prefill_chunked", leg_chunked), ("prefill_fakequant", fq(False)),
             ("prefill_fakequant_24", fq(True))]
     L = mla.LAUNCHES_PER_CALL
-    launches = mla.decode_launches(w.batch, w.heads, ds["splits"]) + L["gather_latent"] + 2 * L["prefill_partial"] + \
+    launches = mla.decode_launches(w.batch, w.heads, ds["splits_used"]) + L["gather_latent"] + 2 * L["prefill_partial"] + \
         L["merge_fused_out"] + 2 * (L["prefill_qdq"] + L["prefill_fakequant"])
     return legs, meta, launches
 
@@ -482,7 +482,18 @@ def run_ours(args, rank, world):
         ws = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
         kw = dict(page_table=wl.page_table, seq_lens=wl.seq_lens) if wl.paged else \
             dict(topk_indices=wl.topk_indices)
-        return dict(w=wl, gs=gs, cache=cache, out=out, lse=lse, ws=ws, kw=kw, splits=splits)
+        d = dict(w=wl, gs=gs, cache=cache, out=out, lse=lse, ws=ws, kw=kw, splits=splits,
+                 lens_host=wl.seq_lens.cpu() if wl.paged else None)
+        d["splits_used"] = step_splits(d)
+        return d
+
+    def step_splits(d):
+        # paged calls left to the plan: the lengths are also held on the host
+        # (a serving scheduler has them there), so the plan's choice is made
+        # there each step; one chunk per sequence runs as the one-split launch
+        if d["splits"] == 0 and d["lens_host"] is not None and d["ws"] is not None:
+            return mla.mla_nvfp4_decode_plan_splits(d["lens_host"], d["w"].heads, d["ws"].numel())
+        return d["splits"]
 
     def cache_write(d):
         wl = d["w"]
@@ -491,7 +502,7 @@ def run_ours(args, rank, world):
     def decode(d):
         wl = d["w"]
         return lambda: mla.mla_nvfp4_decode(wl.q, d["cache"], d["gs"], wl.softmax_scale, out=d["out"], lse=d["lse"],
-                                            workspace=d["ws"], error_word=err, num_splits=d["splits"], **d["kw"])
+                                            workspace=d["ws"], error_word=err, num_splits=step_splits(d), **d["kw"])
 
     ds = decode_setup(w, decode_splits)
     gsp = mla.mla_nvfp4_global_scale(p.v)
@@ -531,7 +542,7 @@ def run_ours(args, rank, world):
                            bound=mla.kernel_kind("gemm"), dtype=mla.operand_dtype("gemm"), kernel=None,
                            peak_x=FP4_OVER_BF16),
     }
-    launches = mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(w.batch, w.heads, decode_splits) + \
+    launches = mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(w.batch, w.heads, ds["splits_used"]) + \
         mla.LAUNCHES_PER_CALL["prefill"] + (mla.LAUNCHES_PER_CALL["gemm"] if with_gemm else 0)
     if full:
         dm, dt = decode_setup(wm, 0), decode_setup(wt, 0)
@@ -546,9 +557,9 @@ def run_ours(args, rank, world):
             "decode_topk": dict(bytes=decode_bytes(wt), flops=decode_flops(wt), bound=mla.kernel_kind("decode"),
                                 dtype=mla.operand_dtype("decode"), kernel=None),
         })
-        launches += mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(wm.batch, wm.heads, 0) + \
+        launches += mla.LAUNCHES_PER_CALL["cache_write"] + mla.decode_launches(wm.batch, wm.heads, dm["splits_used"]) + \
             mla.decode_launches(wt.batch, wt.heads, 0, paged=False)
-        legs_next, meta_next, launches_next = extension_legs(mla, w, ds, p, gsp, codes, scales, err, dev)
+        legs_next, meta_next, launches_next = extension_legs(mla, w, ds, p, gsp, codes, scales, err, dev, step_splits)
         legs += legs_next
         meta.update(meta_next)
         launches += launches_next

@@ -132,6 +132,25 @@ size_t mla_nvfp4_decode_workspace_size(int batch, int num_heads, int num_splits)
 int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits);
 
 /*
+ * The paged decode's length-aware plan, evaluated on the host for sequence
+ * lengths the caller holds in host memory (seq_lens_host, int32 [batch]),
+ * with the same makespan estimate as the device plan and the workspace that
+ * would be passed (workspace_bytes, which bounds the partial rows).  Returns
+ * 1 when that plan keeps one chunk per sequence: mla_nvfp4_decode with
+ * num_splits = 1 then runs the same tiles in the same order, without the
+ * plan and merge kernels and without a workspace (one launch instead of
+ * three).  Returns 0 when the plan would cut sequences (pass num_splits = 0
+ * and the workspace, so the device plans), and 0 for a NULL pointer,
+ * batch < 1, num_heads < 1 or no usable device.  Costs O(32 * batch) host
+ * work; enqueues nothing.  mla_nvfp4_decode_host applies it itself.
+ * Source: "#2244", first commit message (split-K over the paged latent
+ * cache, natural-log LSE merge): splitting a sequence is only needed to fill
+ * the SMs.
+ */
+int mla_nvfp4_decode_plan_splits(const int32_t* seq_lens_host, int batch, int num_heads,
+                                 size_t workspace_bytes);
+
+/*
  * Absorbed MLA decode over the NVFP4 latent cache, split along the keys and
  * merged by natural-log LSE.
  * Source: "#2244", first commit message (split-K absorbed decode over the
@@ -278,7 +297,11 @@ int mla_nvfp4_decode_noalloc(const void* q, int batch, int num_heads, const uint
  *                  copy back (q_dev and out_dev 16-byte aligned).  Each host
  *                  pointer comes with its device pointer (both NULL or both
  *                  set).
- *   Other arguments and the result are those of mla_nvfp4_decode.
+ *   Other arguments and the result are those of mla_nvfp4_decode.  In paged
+ *                  mode with num_splits <= 0 and a workspace, the lengths are
+ *                  read on the host first (mla_nvfp4_decode_plan_splits): where
+ *                  the plan would keep one chunk per sequence the call launches
+ *                  the one-split decode instead of plan, decode and merge.
  *   Return       : argument checks run before anything is enqueued; a copy
  *                  that cannot be enqueued returns MLA_ERR_LAUNCH (see
  *                  mla_nvfp4_last_error).  The host buffers must stay

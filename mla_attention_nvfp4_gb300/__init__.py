@@ -19,7 +19,8 @@ from . import build as _build
 
 __all__ = [
     "load_library", "MLAError", "mla_nvfp4_global_scale", "mla_nvfp4_cache_write",
-    "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode_default_splits", "decode_launches",
+    "mla_nvfp4_decode_workspace_size", "mla_nvfp4_decode_default_splits", "mla_nvfp4_decode_plan_splits",
+    "decode_launches",
     "mla_nvfp4_decode", "mla_nvfp4_decode_q4", "mla_nvfp4_prefill_fused_out",
     "mla_nvfp4_quantize_rows", "mla_nvfp4_gemm", "mla_nvfp4_gather_latent", "mla_nvfp4_prefill_partial",
     "mla_nvfp4_merge_fused_out", "mla_nvfp4_prefill_qdq", "mla_nvfp4_prefill_fakequant",
@@ -66,6 +67,7 @@ _SIGS = {
                                        _c_int, _c_vp, _c_vp, _c_vp]),
     "mla_nvfp4_decode_workspace_size": (ctypes.c_size_t, [_c_int, _c_int, _c_int]),
     "mla_nvfp4_decode_default_splits": (_c_int, [_c_int, _c_int, _c_int]),
+    "mla_nvfp4_decode_plan_splits": (_c_int, [_c_vp, _c_int, _c_int, ctypes.c_size_t]),
     "mla_nvfp4_decode": (_c_int, [_c_vp, _c_int, _c_int, _c_vp, _c_i64, _c_int, _c_vp, _c_i64, _c_int,
                                   _c_vp, _c_vp, _c_int, _c_f, _c_vp, _c_vp, _c_vp, _c_vp,
                                   ctypes.c_size_t, _c_int, _c_vp, _c_vp]),
@@ -211,6 +213,19 @@ def mla_nvfp4_decode_default_splits(batch: int, num_heads: int, num_splits: int 
     > 0, else the library default on the current device (top-k calls, and
     paged calls without a workspace; paged calls with one are planned)."""
     return int(load_library().mla_nvfp4_decode_default_splits(batch, num_heads, num_splits))
+
+
+def mla_nvfp4_decode_plan_splits(seq_lens_host, num_heads: int, workspace_bytes: int = 0) -> int:
+    """The device plan's choice, made on the host from lengths held there
+    (int32 CPU tensor or array [batch]): 1 when it would keep one chunk per
+    sequence (call mla_nvfp4_decode with num_splits=1: one launch, no
+    workspace), 0 when it would cut sequences (num_splits=0 with a
+    workspace of workspace_bytes)."""
+    lens = torch.as_tensor(seq_lens_host, device="cpu").to(torch.int32).contiguous()
+    if lens.dim() != 1:
+        raise ValueError("seq_lens_host must be one-dimensional")
+    return int(load_library().mla_nvfp4_decode_plan_splits(lens.data_ptr(), int(lens.shape[0]), num_heads,
+                                                           int(workspace_bytes)))
 
 
 def decode_launches(batch: int, num_heads: int, num_splits: int = 0, *, paged: bool = True,

@@ -125,6 +125,13 @@ int mla_nvfp4_decode_default_splits(int batch, int num_heads, int num_splits) {
   return mla::decode_default_splits(batch, num_heads, sms > 0 ? sms : 152);
 }
 
+int mla_nvfp4_decode_plan_splits(const int32_t* seq_lens_host, int batch, int num_heads, size_t workspace_bytes) {
+  if (seq_lens_host == nullptr || batch < 1 || num_heads < 1) return 0;
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  return mla::decode_plan_one_chunk(seq_lens_host, batch, num_heads, sms, workspace_bytes);
+}
+
 }  // extern "C"
 
 namespace {
@@ -245,6 +252,11 @@ int mla_nvfp4_decode_host(const void* q_host, void* q_dev, int batch, int num_he
     return record_bytes != MLA_RECORD_BF16_ROPE && record_bytes != MLA_RECORD_FP8_ROPE
                ? MLA_ERR_RECORD_BYTES
                : MLA_ERR_INVALID_ARG;
+  // the lengths are on the host: where the length-aware plan would keep one
+  // chunk per sequence, launch that directly (no plan or merge kernel)
+  if (num_splits <= 0 && seq_lens_host != nullptr && workspace != nullptr &&
+      mla_nvfp4_decode_plan_splits(seq_lens_host, batch, num_heads, workspace_bytes) == 1)
+    num_splits = 1;
   mla::DecodeArgs a;
   int sms = 0;
   if (const int st = decode_prepare(q_dev, batch, num_heads, cache, num_slots, record_bytes,

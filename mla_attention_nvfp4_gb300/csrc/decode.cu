@@ -1744,6 +1744,52 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 64;
 constexpr float kItemOverhead = 2.f;
 
+// Key tiles of a sequence of n keys.
+__host__ __device__ inline int plan_tiles_of(int n) {
+  n = n > 0 ? n : 0;
+  return n / kTok + (n % kTok != 0);
+}
+
+// Products and quotients rounded once on both sides, so that the device plan
+// and its host form (decode_plan_one_chunk) rank the candidates alike.
+__host__ __device__ inline float plan_mul(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fmul_rn(a, b);
+#else
+  return a * b;
+#endif
+}
+
+// The makespan estimate of chunk size C for a batch of `tot` tiles that C
+// cuts into n items, `full` full chunks, `rows` partial rows (the chunks of
+// sequences cut more than once) and `last` shorter last chunks (empty
+// sequences included); infinity when the items or rows do not fit.
+__host__ __device__ inline float plan_estimate(long long tot, long long n, long long full, long long rows,
+                                               long long last, int C, int pairs, int max_items, int max_rows) {
+  const float P = static_cast<float>(pairs > 1 ? pairs : 1), o = kItemOverhead;
+  const float waves = plan_mul(ceilf(static_cast<float>(full) / P), static_cast<float>(C) + o);
+  const float rem = static_cast<float>(tot - full * static_cast<long long>(C));
+  const float spread = (static_cast<float>(tot) + plan_mul(o, static_cast<float>(n))) / P;
+  const float tail = last > 0 ? plan_mul(0.5f, rem / static_cast<float>(last) + o) : 0.f;
+  const float avg = spread + tail;
+  const bool fits = n <= max_items && rows <= max_rows;
+  return fits ? fmaxf(waves, avg) : INFINITY;
+}
+
+// The counts plan_estimate takes, of chunk size C over a sequence of t tiles.
+struct PlanCounts {
+  long long n = 0, full = 0, rows = 0, last = 0;
+  __host__ __device__ void add(int t, int C) {
+    const int f = t / C;
+    const int chunks = f + (t % C != 0 ? 1 : 0);
+    const int nb = chunks > 1 ? chunks : 1;  // an empty sequence is one empty chunk
+    n += nb;
+    full += f;
+    rows += nb > 1 ? nb : 0;
+    last += (t == 0 || t % C != 0) ? 1 : 0;
+  }
+};
+
 struct PlanArgs {
   const int32_t* seq_lens;  // paged mode; null in top-k mode
   int topk_n;
@@ -1754,8 +1800,7 @@ struct PlanArgs {
 };
 
 __device__ __forceinline__ int plan_tiles(const PlanArgs& a, int b) {
-  const int n = a.seq_lens != nullptr ? max(0, a.seq_lens[b]) : a.topk_n;
-  return n / kTok + (n % kTok != 0);
+  return plan_tiles_of(a.seq_lens != nullptr ? a.seq_lens[b] : a.topk_n);
 }
 
 // Tile counts of the first kPlanStaged sequences, read from global memory
@@ -1843,32 +1888,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) decode_plan_kernel(PlanArgs a
   // candidate C = ceil(tmax / (warp + 1)), evaluated by one warp each
   {
     const int C = max(1, (tmax + warp) / (warp + 1));
-    long long n = 0, full = 0, rows = 0, last = 0;
-    for (int b = lane; b < B; b += 32) {
-      const int t = staged_tiles(a, s_tiles, b);
-      const int nb = max(1, t / C + (t % C != 0));
-      const int f = t / C;
-      n += nb;
-      full += f;
-      rows += nb > 1 ? nb : 0;
-      last += (t == 0 || t % C != 0) ? 1 : 0;
-    }
+    PlanCounts c;
+    for (int b = lane; b < B; b += 32) c.add(staged_tiles(a, s_tiles, b), C);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      n += __shfl_xor_sync(0xffffffffu, n, o);
-      full += __shfl_xor_sync(0xffffffffu, full, o);
-      rows += __shfl_xor_sync(0xffffffffu, rows, o);
-      last += __shfl_xor_sync(0xffffffffu, last, o);
+      c.n += __shfl_xor_sync(0xffffffffu, c.n, o);
+      c.full += __shfl_xor_sync(0xffffffffu, c.full, o);
+      c.rows += __shfl_xor_sync(0xffffffffu, c.rows, o);
+      c.last += __shfl_xor_sync(0xffffffffu, c.last, o);
     }
-    if (lane == 0) {
-      const float P = static_cast<float>(max(1, a.pairs)), o = kItemOverhead;
-      const float waves = ceilf(static_cast<float>(full) / P) * (static_cast<float>(C) + o);
-      const float rem = static_cast<float>(tot - full * static_cast<long long>(C));
-      const float avg = (static_cast<float>(tot) + o * static_cast<float>(n)) / P +
-                        (last > 0 ? 0.5f * (rem / static_cast<float>(last) + o) : 0.f);
-      const bool fits = n <= a.max_items && rows <= a.max_rows;
-      s_est[warp] = fits ? fmaxf(waves, avg) : INFINITY;
-    }
+    if (lane == 0) s_est[warp] = plan_estimate(tot, c.n, c.full, c.rows, c.last, C, a.pairs, a.max_items, a.max_rows);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1969,6 +1998,32 @@ DecodePlanLayout decode_plan_layout(int batch, int num_heads, int num_sms, size_
   l.lse = align256(l.rows + static_cast<size_t>(l.max_rows) * num_heads * 512 * sizeof(float));
   l.total = align256(l.lse + static_cast<size_t>(l.max_rows) * num_heads * sizeof(float));
   return l;
+}
+
+int decode_plan_one_chunk(const int32_t* lens, int batch, int num_heads, int num_sms, size_t bytes) {
+  if (lens == nullptr || batch < 1 || num_heads < 1) return 0;
+  const DecodePlanLayout l = decode_plan_layout(batch, num_heads, num_sms, bytes);
+  long long tot = 0;
+  int tmax = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int t = plan_tiles_of(lens[b]);
+    tot += t;
+    tmax = t > tmax ? t : tmax;
+  }
+  // candidate 0 (C = tmax) against C = ceil(tmax / k), k = 2..32, exactly
+  // as the device plan ranks them: the first minimum wins
+  float est0 = 0.f;
+  for (int w = 0; w < 32; ++w) {
+    const int C = (tmax + w) / (w + 1) > 1 ? (tmax + w) / (w + 1) : 1;
+    PlanCounts c;
+    for (int b = 0; b < batch; ++b) c.add(plan_tiles_of(lens[b]), C);
+    const float est = plan_estimate(tot, c.n, c.full, c.rows, c.last, C, l.pairs, l.max_items, l.max_rows);
+    if (w == 0)
+      est0 = est;
+    else if (est < est0)
+      return 0;
+  }
+  return 1;
 }
 
 int decode_default_splits(int batch, int num_heads, int num_sms) {

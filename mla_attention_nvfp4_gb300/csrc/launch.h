@@ -95,6 +95,11 @@ struct DecodePlanLayout {
   size_t items, seqs, rows, lse, total;
 };
 DecodePlanLayout decode_plan_layout(int batch, int num_heads, int num_sms, size_t bytes);
+// 1 when the planned decode of these (host) sequence lengths would keep one
+// chunk per sequence, i.e. the one-split launch does the same work without
+// the plan and merge kernels; 0 otherwise.  The same estimate as the device
+// plan, on the host.
+int decode_plan_one_chunk(const int32_t* lens, int batch, int num_heads, int num_sms, size_t bytes);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms);
 
 struct PrefillArgs {

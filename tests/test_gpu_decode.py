@@ -300,6 +300,10 @@ def test_decode_plan_covers_every_chunk_once(lens):
     seqs = raw[seq_off:seq_off + 8 * B].view(np.int32).reshape(-1, 2)
     tiles = [-(-L // 64) for L in lens]
     assert C == _plan_choice(tiles, pairs, max_items, max_items)
+    # the host form of the plan makes the same choice between one chunk per
+    # sequence and cut sequences
+    one = mla.mla_nvfp4_decode_plan_splits(torch.tensor(lens, dtype=torch.int32), 16, ws.numel())
+    assert one == (1 if C >= max(1, max(tiles)) else 0)
     nb = [max(1, -(-t // C)) for t in tiles]
     # every (sequence, chunk) exactly once
     assert sorted(map(tuple, items.tolist())) == sorted((b, c) for b in range(B) for c in range(nb[b]))
@@ -317,6 +321,42 @@ def test_decode_plan_covers_every_chunk_once(lens):
     assert all(s_ == C for s_ in size[:n_full])
     buckets = [63 - s_ * 64 // C for s_ in size[n_full:]]
     assert buckets == sorted(buckets)
+
+
+@pytest.mark.parametrize("lens,one", [((640,) * 48, 1), ((700, 64, 1500), 0), ((0,) * 49 + (64,), 1)])
+def test_decode_host_plans_from_host_lengths(lens, one):
+    # mla_nvfp4_decode_host reads the lengths on the host: where the plan
+    # keeps one chunk per sequence it launches the one-split decode (the plan
+    # kernel never writes the workspace), otherwise the device plans; either
+    # way the output is the planned device call's, bit for bit
+    B, H = len(lens), 16
+    w = workloads.decode_paged("hostplan", B, H, lens, 432, perm_pages=True, seed=44)
+    gs = oracle_gs(w.kv_c)
+    cache, err = _written_cache(w, gs)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = [-(-L // 64) for L in lens]
+    ws_bytes = mla.mla_nvfp4_decode_workspace_size(B, H, 0)
+    assert (_plan_choice(tiles, sms // 2, B + sms // 2, B + sms // 2) == max(1, max(tiles))) == bool(one)
+    assert mla.mla_nvfp4_decode_plan_splits(w.seq_lens, H, ws_bytes) == one
+    out_d, lse_d = _decode(w, gs, cache, err, num_splits=0,
+                           workspace=torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV))
+    ws = torch.full((ws_bytes,), 0xFF, dtype=torch.uint8, device=DEV)
+    q_host = w.q.contiguous().pin_memory()
+    out_host = torch.empty((B, H, 512), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    mla.mla_nvfp4_decode_host(q_host, torch.empty_like(q_host, device=DEV), cache, torch.tensor([gs], device=DEV),
+                              w.softmax_scale, out_host, torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV),
+                              page_table_host=w.page_table.contiguous().pin_memory(),
+                              page_table_dev=torch.empty_like(w.page_table, device=DEV),
+                              seq_lens_host=w.seq_lens.pin_memory(),
+                              seq_lens_dev=torch.empty_like(w.seq_lens, device=DEV),
+                              lse_host=lse_host, lse_dev=torch.empty((B, H), dtype=torch.float32, device=DEV),
+                              workspace=ws, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    header_untouched = bool((ws[:8] == 0xFF).all())
+    assert header_untouched == bool(one)
+    assert torch.equal(out_host, out_d.cpu()) and torch.equal(lse_host, lse_d.cpu())
 
 
 @pytest.mark.parametrize("batch,heads,max_len,seed", [(300, 16, 600, 41), (40, 160, 3000, 42)])
