@@ -107,10 +107,19 @@ constexpr uint32_t kIdescQK = idesc_f16_f32(128, kTok, false, false);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 256, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// The running max is raised (and O rescaled) only when a tile's max exceeds
-// it by more than 2^14: P = 2^(s - m) then stays below 2^14, inside f16,
-// and sum P.V stays far inside fp32.
-constexpr float kRescaleThreshold = 14.0f;
+// The reference (running max, log2 units) is raised, and O rescaled, only
+// when a tile's max exceeds it by more than kRescaleThreshold, and is then
+// set kRefHeadroom above that max, so that the next raise needs the max to
+// grow by both.  P = 2^(s - m) stays at most 2^15.5, inside f16 (max 65504),
+// and sum P.V far inside fp32; right after a raise the largest P is 2^-4, so
+// f16's subnormal range (below 2^-14) begins 10 log2 units under the max,
+// where a P rounds to a multiple of 2^-24 against a row sum of at least
+// 2^-4.  A rescale waits for the two previous P.V products; on the 64 x 4096
+// workload (scores counted on the CPU) some softmax warp of a CTA rescales
+// in ~8 % of tiles with these values, ~43 % with threshold 14 and no
+// headroom.
+constexpr float kRescaleThreshold = 15.5f;
+constexpr float kRefHeadroom = 4.0f;
 
 struct Params {
   const __nv_bfloat16* q;
@@ -605,8 +614,8 @@ __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, v
     float m_use = m_run, alpha = 1.f;
     const bool raise = mx > m_run + kRescaleThreshold;
     if (raise) {
-      m_use = mx;
-      alpha = ex2_approx(m_run - mx);
+      m_use = mx + kRefHeadroom;
+      alpha = ex2_approx(m_run - m_use);
     }
     // an O rescale must follow every earlier P.V and precede PV(j).
     // PV(j-1) and PV(j-2) come from different issuers; each issuer's
@@ -642,7 +651,7 @@ __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, v
       unpk2(fma2(pk2(x[2 * i], x[2 * i + 1]), sc2, nm2), a0, a1);
       const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
       ls2[i & 3] = add2(ls2[i & 3], pk2(p0, p1));
-      pv[i] = pack_f16(p0, p1);  // P <= 2^14 (lazy reference), f16 operand
+      pv[i] = pack_f16(p0, p1);  // P <= 2^15.5 (lazy reference), f16 operand
     }
     float ls[8];
 #pragma unroll
@@ -818,8 +827,8 @@ __device__ __forceinline__ void softmax_quad(const Params& p, Barriers& bars, vo
       m_use[h] = m_run[h];
       alpha[h] = 1.f;
       if (mx[h] > m_run[h] + kRescaleThreshold) {
-        m_use[h] = mx[h];
-        alpha[h] = ex2_approx(m_run[h] - mx[h]);
+        m_use[h] = mx[h] + kRefHeadroom;
+        alpha[h] = ex2_approx(m_run[h] - m_use[h]);
         raise = true;
       }
     }
@@ -844,7 +853,7 @@ __device__ __forceinline__ void softmax_quad(const Params& p, Barriers& bars, vo
       }
       tmem_st_wait();
     }
-    // probabilities two at a time: x * score_scale - m_use, P <= 2^14
+    // probabilities two at a time: x * score_scale - m_use, P <= 2^15.5
     // (lazy reference), f16 operand pairs; the row sums in packed halves
     uint32_t pv[16];  // pv[2i + h]: head h, key pair 8i + kq (column 4i + kq / 2)
 #pragma unroll
