@@ -280,8 +280,14 @@ def _plan_choice(tiles, pairs, max_items, max_rows, overhead=2.0):
     return best
 
 
+def _random_lens(seed, batch, max_len):
+    rng = np.random.default_rng(seed)
+    return tuple(int(x) for x in rng.integers(0, max_len, batch))
+
+
 @pytest.mark.parametrize("lens", [(4096,) * 64, (0, 1, 64, 65, 4000, 130, 0, 2500, 3, 1999, 2368, 700),
-                                  (32768, 1024, 1500, 20000, 5000, 8000, 1100)])
+                                  (32768, 1024, 1500, 20000, 5000, 8000, 1100),
+                                  _random_lens(51, 90, 3000), _random_lens(52, 40, 9000)])
 def test_decode_plan_covers_every_chunk_once(lens):
     w = workloads.decode_paged("plan", len(lens), 16, lens, 432, perm_pages=True, seed=36)
     gs = oracle_gs(w.kv_c)
