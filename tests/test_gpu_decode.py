@@ -51,6 +51,24 @@ def run_oracle(w, gs):
     return attention.decode(f32(w.q), c, w.record_bytes, gs, w.softmax_scale, oracle_slots(w), with_abs=True)
 
 
+@pytest.mark.parametrize("growth", [0.5, 2.0])
+@pytest.mark.parametrize("splits", [0, 1])
+def test_decode_growing_scores(growth, splits):
+    # the latent of key tile j scaled by 1 + growth * j: a head's scores grow
+    # from tile to tile by more than the lazy rescale's threshold, so its
+    # reference is raised (with headroom) and O rescaled many times per
+    # sequence, against both issuers' earlier P.V products
+    lens = (1000, 700)
+    w = workloads.decode_paged("growing", len(lens), 128, lens, 432, perm_pages=True, seed=int(4 * growth))
+    tile = torch.cat([torch.arange(L) // 64 for L in lens]).float()
+    w.kv_c = (w.kv_c.float() * (1.0 + growth * tile)[:, None]).to(torch.bfloat16)
+    gs = oracle_gs(w.kv_c)
+    out, lse = run_gpu(w, gs, splits)
+    o_ref, l_ref, o_abs = run_oracle(w, gs)
+    assert_attention_close(out, o_ref, f"decode growing scores x{growth} splits={splits}", o_abs)
+    assert_lse_close(lse, l_ref, f"decode growing scores x{growth} lse")
+
+
 @pytest.mark.parametrize("rb", [432, 368])
 @pytest.mark.parametrize("splits", [0, 1, 3])
 def test_decode_tiny(rb, splits):
