@@ -199,8 +199,19 @@ __device__ __forceinline__ int page_of(const Params& p, int t) {
   return static_cast<int>(div_magic(static_cast<uint32_t>(t), p.pg_magic, p.pg_shift));
 }
 
+// Key modes: kKeysAny decides paged or top-k from the arguments at run time;
+// kKeysPaged and kKeysTopk fix it at compile time (the exact kernel is
+// instantiated per mode, so each carries only its own addressing code).
+constexpr int kKeysAny = 0, kKeysPaged = 1, kKeysTopk = 2;
+
+template <int kMode = kKeysAny>
+__device__ __forceinline__ bool topk_mode(const Params& p) {
+  return kMode == kKeysTopk || (kMode == kKeysAny && p.topk != nullptr);
+}
+
+template <int kMode = kKeysAny>
 __device__ __forceinline__ int32_t load_index(const Params& p, int b, int t) {
-  if (p.topk != nullptr) {
+  if (topk_mode<kMode>(p)) {
     const int tc = min(max(t, 0), max(p.topk_n - 1, 0));
     return ldg_i32(p.topk + static_cast<int64_t>(b) * p.topk_n + tc);
   }
@@ -208,10 +219,11 @@ __device__ __forceinline__ int32_t load_index(const Params& p, int b, int t) {
   return ldg_i32(p.page_table + static_cast<int64_t>(b) * p.pt_stride + pi);
 }
 
+template <int kMode = kKeysAny>
 __device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t, int n_keys, bool& bad) {
   if (t >= n_keys) return -1;
   int64_t slot;
-  if (p.topk != nullptr) {
+  if (topk_mode<kMode>(p)) {
     if (idx < 0) return -1;  // padding entry
     slot = idx;
   } else {
@@ -491,13 +503,15 @@ __device__ __forceinline__ bool convert_part(const DeqCtx& c, int j, RawPart<Q, 
 
 // The dequantisation loop of one thread.  Returns whether an out-of-range
 // page or slot id was met; flags a RoPE value beyond the f16 range.
-template <int Q, int kRecord>
+template <int Q, int kRecord, int kMode>
 __device__ bool dequant_role(const DeqCtx& c) {
   const Params& p = c.p;
   bool bad = false;
   float rope_max = 0.f;
-  auto slot_of = [&](int j, int32_t idx) { return key_slot(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad); };
-  auto index_of = [&](int j) { return load_index(p, c.b, (c.tile0 + j) * kTok + c.k); };
+  auto slot_of = [&](int j, int32_t idx) {
+    return key_slot<kMode>(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad);
+  };
+  auto index_of = [&](int j) { return load_index<kMode>(p, c.b, (c.tile0 + j) * kTok + c.k); };
 
   const int nt = c.nt;
   const int64_t s_cur = nt > 0 ? slot_of(0, index_of(0)) : -1;  // tile 0
@@ -521,6 +535,16 @@ __device__ bool dequant_role(const DeqCtx& c) {
   for (int j = 0; j < nt; ++j) {
     const int64_t s_2 = (j + 2 < nt) ? slot_of(j + 2, i_2) : -1;
     i_2 = (j + 3 < nt) ? index_of(j + 3) : -1;
+    if constexpr (kMode == kKeysTopk) {
+      // top-k keys are scattered records, each a DRAM access: this part's
+      // bytes of tile j + 2 go to L2 while tile j converts (6 % on 32 x 2048
+      // of 65,536 keys, measured; paged tiles do not need it)
+      if (s_2 >= 0) {
+        const uint8_t* rec = p.cache + s_2 * kRecord + (Q == 2 ? 256 : 128 * (Q == 0 ? c.rank : 1 - c.rank));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(rec));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + 127));
+      }
+    }
     // the next tile's bytes load into each register group as soon as this
     // tile's conversion has read it
     if (!convert_part<Q, kRecord>(c, j, ra, rope_max, j + 1 < nt, s_nxt >= 0 ? p.cache + s_nxt * kRecord : nullptr))
@@ -755,6 +779,7 @@ __device__ __forceinline__ void write_partial(const Params& p, uint32_t tmem, ui
 // 16x128b store gives it, which are its own (key pair k in column k).
 // Otherwise as softmax_tiles: masking of padding keys, lazy reference raise
 // with an O rescale, P as f16 for P.V, running row sums.
+template <int kMode>
 __device__ __forceinline__ void softmax_quad(const Params& p, Barriers& bars, volatile int& abort_s, uint32_t tmem,
                                              uint32_t lane_base, int b, int tile0, int nt, int n_keys,
                                              const float (&score_scale)[2], bool& ok, float (&m_run)[2],
@@ -762,17 +787,17 @@ __device__ __forceinline__ void softmax_quad(const Params& p, Barriers& bars, vo
   uint32_t* err = p.error_word;
   const int lane = threadIdx.x & 31, kq = 2 * (lane & 3);  // the thread's first key of each 8
   // per-tile validity: lane checks keys lane and 32 + lane
-  int32_t ia = load_index(p, b, tile0 * kTok + lane);
-  int32_t ib = load_index(p, b, tile0 * kTok + 32 + lane);
+  int32_t ia = load_index<kMode>(p, b, tile0 * kTok + lane);
+  int32_t ib = load_index<kMode>(p, b, tile0 * kTok + 32 + lane);
   for (int j = 0; j < nt; ++j) {
     const int pb = j & 1;
     const int key = (tile0 + j) * kTok + lane;
     bool badv = false;
-    const unsigned va = __ballot_sync(0xffffffffu, key_slot(p, ia, key, n_keys, badv) >= 0);
-    const unsigned vb = __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0);
+    const unsigned va = __ballot_sync(0xffffffffu, key_slot<kMode>(p, ia, key, n_keys, badv) >= 0);
+    const unsigned vb = __ballot_sync(0xffffffffu, key_slot<kMode>(p, ib, key + 32, n_keys, badv) >= 0);
     if (j + 1 < nt) {
-      ia = load_index(p, b, key + kTok);
-      ib = load_index(p, b, key + kTok + 32);
+      ia = load_index<kMode>(p, b, key + kTok);
+      ib = load_index<kMode>(p, b, key + kTok + 32);
     }
     if (!bar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
       ok = false;
@@ -953,7 +978,7 @@ __device__ __forceinline__ void write_partial_quad(const Params& p, uint32_t tme
   }
 }
 
-template <int kRecord>
+template <int kRecord, int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decode_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
@@ -991,13 +1016,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decod
   } else {
     const int split = blockIdx.x >> 1;
     b = blockIdx.y;
-    const int n_keys_u = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
+    const int n_keys_u = topk_mode<kMode>(p) ? p.topk_n : max(0, p.seq_lens[b]);
     per = ((n_keys_u + kTok - 1) / kTok + p.splits - 1) / p.splits;
     tile0 = split * per;
     direct = p.splits == 1;
     row0 = (static_cast<int64_t>(b) * p.splits + split) * p.num_heads;
   }
-  const int n_keys = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
+  const int n_keys = topk_mode<kMode>(p) ? p.topk_n : max(0, p.seq_lens[b]);
   const int n_tiles_all = n_keys / kTok + (n_keys % kTok != 0);
   const int nt = max(0, min(n_tiles_all, tile0 + per) - tile0);
   uint32_t* err = p.error_word;
@@ -1116,11 +1141,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decod
     DeqCtx c{p, &bars, &abort_s, sV, sT, rank, b, tile0, nt, n_keys, k};
     bool bad;
     if (q == 0)
-      bad = dequant_role<0, kRecord>(c);
+      bad = dequant_role<0, kRecord, kMode>(c);
     else if (q == 1)
-      bad = dequant_role<1, kRecord>(c);
+      bad = dequant_role<1, kRecord, kMode>(c);
     else
-      bad = dequant_role<2, kRecord>(c);
+      bad = dequant_role<2, kRecord, kMode>(c);
     if (bad && rank == 0 && q == 0) flag_error(err, MLA_DEVERR_BOUNDS);
   } else {
     // ------------------------------------------- softmax and epilogue
@@ -1226,7 +1251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsTc, 1) decod
       // every head's scale is written before q_ready completes
       if (ok) ok = bar_wait(&bars.q_ready, 0, err, &abort_s);
       const float sc[2] = {score_scale_s[qh], score_scale_s[qh + 8]};
-      if (ok) softmax_quad(p, bars, abort_s, tmem, lane_base, b, tile0, nt, n_keys, sc, ok, m_q, l_q);
+      if (ok) softmax_quad<kMode>(p, bars, abort_s, tmem, lane_base, b, tile0, nt, n_keys, sc, ok, m_q, l_q);
       if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
     }
     write_partial_quad(p, tmem, lane_base, ok, nt, m_q, l_q, gs, row0, b, hg * kHeads + qh, direct, rank);
@@ -2125,10 +2150,13 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
     smem = kQ4SmAlloc;
     slot = r432 ? 5 : 6;
   } else {
-    kern = a.record_bytes == 432 ? reinterpret_cast<const void*>(decode_tc_kernel<432>)
-                                 : reinterpret_cast<const void*>(decode_tc_kernel<368>);
+    const bool r432 = a.record_bytes == 432, topk = a.topk_indices != nullptr;
+    kern = topk ? (r432 ? reinterpret_cast<const void*>(decode_tc_kernel<432, kKeysTopk>)
+                        : reinterpret_cast<const void*>(decode_tc_kernel<368, kKeysTopk>))
+                : (r432 ? reinterpret_cast<const void*>(decode_tc_kernel<432, kKeysPaged>)
+                        : reinterpret_cast<const void*>(decode_tc_kernel<368, kKeysPaged>));
     smem = kSmAlloc;
-    slot = a.record_bytes == 432 ? 1 : 2;
+    slot = topk ? (r432 ? 8 : 9) : (r432 ? 1 : 2);
   }
   if (const int st = smem_limit_once(kern, static_cast<int>(smem), slot)) return st;
   {
