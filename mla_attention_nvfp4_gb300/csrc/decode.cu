@@ -567,7 +567,7 @@ __device__ bool dequant_role(const DeqCtx& c) {
 // take the same reference and the same rescale decisions) and keep
 // separate row sums.  The exchange also orders the halves' score loads
 // before the P stores that overwrite them.
-template <int kSplit>
+template <int kSplit, int kMode>
 __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, volatile int& abort_s, uint32_t tmem,
                                               uint32_t lane_off, int b, int tile0, int nt, int n_keys,
                                               float score_scale, bool& ok, float& m_run, float& l_run, int half,
@@ -577,18 +577,18 @@ __device__ __forceinline__ void softmax_tiles(const Params& p, Barriers& bars, v
   const int lane = threadIdx.x & 31;
   const int kb = half * kKeys;  // first key of this thread's part of a tile
   // per-tile validity: lane checks keys kb + lane (and kb + lane + 32)
-  int32_t ia = load_index(p, b, tile0 * kTok + kb + lane);
-  int32_t ib = kSplit == 1 ? load_index(p, b, tile0 * kTok + 32 + lane) : 0;
+  int32_t ia = load_index<kMode>(p, b, tile0 * kTok + kb + lane);
+  int32_t ib = kSplit == 1 ? load_index<kMode>(p, b, tile0 * kTok + 32 + lane) : 0;
   for (int j = 0; j < nt; ++j) {
     const int pb = j & 1;
     const int key = (tile0 + j) * kTok + kb + lane;
     bool badv = false;
-    const unsigned va = __ballot_sync(0xffffffffu, key_slot(p, ia, key, n_keys, badv) >= 0);
-    const unsigned vb = kSplit == 1 ? __ballot_sync(0xffffffffu, key_slot(p, ib, key + 32, n_keys, badv) >= 0)
+    const unsigned va = __ballot_sync(0xffffffffu, key_slot<kMode>(p, ia, key, n_keys, badv) >= 0);
+    const unsigned vb = kSplit == 1 ? __ballot_sync(0xffffffffu, key_slot<kMode>(p, ib, key + 32, n_keys, badv) >= 0)
                                     : 0xffffffffu;
     if (j + 1 < nt) {
-      ia = load_index(p, b, key + kTok);
-      if (kSplit == 1) ib = load_index(p, b, key + kTok + 32);
+      ia = load_index<kMode>(p, b, key + kTok);
+      if (kSplit == 1) ib = load_index<kMode>(p, b, key + kTok + 32);
     }
     if (!bar_wait(&bars.s_full[pb], (j >> 1) & 1, err, &abort_s)) {
       ok = false;
@@ -1435,13 +1435,15 @@ __device__ __forceinline__ bool q4_convert(const Q4Ctx& c, int j, const RawQ4<Q,
   return true;
 }
 
-template <int Q, int kRecord>
+template <int Q, int kRecord, int kMode>
 __device__ bool q4_role(const Q4Ctx& c) {
   const Params& p = c.p;
   bool bad = false;
   float rope_max = 0.f;
-  auto slot_of = [&](int j, int32_t idx) { return key_slot(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad); };
-  auto index_of = [&](int j) { return load_index(p, c.b, (c.tile0 + j) * kTok + c.k); };
+  auto slot_of = [&](int j, int32_t idx) {
+    return key_slot<kMode>(p, idx, (c.tile0 + j) * kTok + c.k, c.n_keys, bad);
+  };
+  auto index_of = [&](int j) { return load_index<kMode>(p, c.b, (c.tile0 + j) * kTok + c.k); };
   const int nt = c.nt;
   const int64_t s_cur = nt > 0 ? slot_of(0, index_of(0)) : -1;
   int64_t s_nxt = nt > 1 ? slot_of(1, index_of(1)) : -1;
@@ -1468,7 +1470,7 @@ __device__ bool q4_role(const Q4Ctx& c) {
   return bad;
 }
 
-template <int kRecord>
+template <int kRecord, int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_q4_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
@@ -1501,13 +1503,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
   } else {
     const int split = blockIdx.x >> 1;
     b = blockIdx.y;
-    const int n_keys_u = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
+    const int n_keys_u = topk_mode<kMode>(p) ? p.topk_n : max(0, p.seq_lens[b]);
     per = ((n_keys_u + kTok - 1) / kTok + p.splits - 1) / p.splits;
     tile0 = split * per;
     direct = p.splits == 1;
     row0 = (static_cast<int64_t>(b) * p.splits + split) * p.num_heads;
   }
-  const int n_keys = (p.topk != nullptr) ? p.topk_n : max(0, p.seq_lens[b]);
+  const int n_keys = topk_mode<kMode>(p) ? p.topk_n : max(0, p.seq_lens[b]);
   const int n_tiles_all = n_keys / kTok + (n_keys % kTok != 0);
   const int nt = max(0, min(n_tiles_all, tile0 + per) - tile0);
   uint32_t* err = p.error_word;
@@ -1604,11 +1606,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     Q4Ctx c{p, &bars, &abort_s, sBuf, rank, b, tile0, nt, n_keys, k, scale_ok(gs) ? 1.f / gs : 0.f};
     bool bad;
     if (q == 0)
-      bad = q4_role<0, kRecord>(c);
+      bad = q4_role<0, kRecord, kMode>(c);
     else if (q == 1)
-      bad = q4_role<1, kRecord>(c);
+      bad = q4_role<1, kRecord, kMode>(c);
     else
-      bad = q4_role<2, kRecord>(c);
+      bad = q4_role<2, kRecord, kMode>(c);
     if (bad && rank == 0 && q == 0) flag_error(err, MLA_DEVERR_BOUNDS);
   } else {
     // ------------------------------ query quantisation, softmax, epilogue
@@ -1685,7 +1687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       tc_fence_before();
       mbar_arrive(&bars.q_ready);
       if (!scales_ok && hr == 0 && rank == 0) flag_error(err, MLA_DEVERR_SCALE);
-      softmax_tiles<1>(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run, 0,
+      softmax_tiles<1, kMode>(p, bars, abort_s, tmem, lane_off, b, tile0, nt, n_keys, score_scale, ok, m_run, l_run, 0,
                        nullptr, hr);
       if (ok) ok = bar_wait(&bars.o_full, 0, err, &abort_s);
     }
@@ -2145,10 +2147,13 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
   int slot;
   if (a.gs_q != nullptr) {
     const bool r432 = a.record_bytes == 432;
-    kern = r432 ? reinterpret_cast<const void*>(decode_q4_kernel<432>)
-                : reinterpret_cast<const void*>(decode_q4_kernel<368>);
+    const bool topk = a.topk_indices != nullptr;
+    kern = topk ? (r432 ? reinterpret_cast<const void*>(decode_q4_kernel<432, kKeysTopk>)
+                        : reinterpret_cast<const void*>(decode_q4_kernel<368, kKeysTopk>))
+                : (r432 ? reinterpret_cast<const void*>(decode_q4_kernel<432, kKeysPaged>)
+                        : reinterpret_cast<const void*>(decode_q4_kernel<368, kKeysPaged>));
     smem = kQ4SmAlloc;
-    slot = r432 ? 5 : 6;
+    slot = topk ? (r432 ? 10 : 11) : (r432 ? 5 : 6);
   } else {
     const bool r432 = a.record_bytes == 432, topk = a.topk_indices != nullptr;
     kern = topk ? (r432 ? reinterpret_cast<const void*>(decode_tc_kernel<432, kKeysTopk>)
