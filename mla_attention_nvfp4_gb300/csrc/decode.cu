@@ -540,9 +540,13 @@ __device__ bool dequant_role(const DeqCtx& c) {
       // bytes of tile j + 2 go to L2 while tile j converts (6 % on 32 x 2048
       // of 65,536 keys, measured; paged tiles do not need it)
       if (s_2 >= 0) {
+        // first and last byte of the part's main span, both inside the record:
+        // latent codes [128 r, +128) for parts 0 and 1, scales and RoPE
+        // [256, kRecord - 16) for part 2
+        constexpr int kSpan = (Q == 2) ? kRecord - 16 - 256 - 1 : 127;
         const uint8_t* rec = p.cache + s_2 * kRecord + (Q == 2 ? 256 : 128 * (Q == 0 ? c.rank : 1 - c.rank));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(rec));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + 127));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + kSpan));
       }
     }
     // the next tile's bytes load into each register group as soon as this

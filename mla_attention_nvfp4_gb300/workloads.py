@@ -163,7 +163,7 @@ def decode_mixed(seed=0, device="cpu", batch=128, heads=128, lo=1024, hi=32768) 
 
 
 def decode_topk(seed=0, device="cpu", batch=32, heads=128, context=65536, topk=2048,
-                max_pad=8) -> DecodeWorkload:
+                max_pad=8, record_bytes=432) -> DecodeWorkload:
     g = _gen(seed, device)
     idx = torch.empty((batch, topk), dtype=torch.int64)
     for b in range(batch):
@@ -178,7 +178,7 @@ def decode_topk(seed=0, device="cpu", batch=32, heads=128, context=65536, topk=2
     kv_c = _randn_bf16((T, D_LATENT), g, device)
     k_pe = _randn_bf16((T, D_ROPE), g, device)
     return DecodeWorkload(
-        name="decode_topk", batch=batch, heads=heads, record_bytes=432, q=q, kv_c=kv_c,
+        name="decode_topk", batch=batch, heads=heads, record_bytes=record_bytes, q=q, kv_c=kv_c,
         k_pe=k_pe, slot_mapping=ref.to(device), num_slots=batch * context,
         topk_indices=idx.to(torch.int32).to(device), meta={"context": context, "topk": topk})
 

@@ -90,16 +90,17 @@ def test_decode_shapes(heads, lens):
     assert_lse_close(lse, l_ref, "decode lse")
 
 
+@pytest.mark.parametrize("rb", [432, 368])
 @pytest.mark.parametrize("splits", [0, 1])  # 1: output written by the decode kernel itself
-def test_decode_topk_small(splits):
-    w = workloads.decode_topk(batch=3, heads=32, context=4096, topk=300, max_pad=8, seed=5)
+def test_decode_topk_small(splits, rb):
+    w = workloads.decode_topk(batch=3, heads=32, context=4096, topk=300, max_pad=8, seed=5, record_bytes=rb)
     w.topk_indices[2, :] = -1  # a row with nothing to attend to
     gs = oracle_gs(w.kv_c)
     out, lse = run_gpu(w, gs, splits)
     o_ref, l_ref, o_abs = run_oracle(w, gs)
     assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
-    assert_attention_close(out, o_ref, "decode top-k small", o_abs)
-    assert_lse_close(lse, l_ref, "decode top-k lse")
+    assert_attention_close(out, o_ref, f"decode top-k small rb={rb}", o_abs)
+    assert_lse_close(lse, l_ref, f"decode top-k lse rb={rb}")
 
 
 @pytest.mark.parametrize("rb", [432, 368])
