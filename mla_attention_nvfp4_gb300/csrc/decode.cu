@@ -201,8 +201,10 @@ __device__ __forceinline__ int page_of(const Params& p, int t) {
 
 // Key modes: kKeysAny decides paged or top-k from the arguments at run time;
 // kKeysPaged and kKeysTopk fix it at compile time (the exact kernel is
-// instantiated per mode, so each carries only its own addressing code).
-constexpr int kKeysAny = 0, kKeysPaged = 1, kKeysTopk = 2;
+// instantiated per mode, so each carries only its own addressing code), and
+// kKeysPaged64 is paged with 64-token pages, a 64-key tile being one page
+// (the page and the offset in it by shift and mask).
+constexpr int kKeysAny = 0, kKeysPaged = 1, kKeysTopk = 2, kKeysPaged64 = 3;
 
 template <int kMode = kKeysAny>
 __device__ __forceinline__ bool topk_mode(const Params& p) {
@@ -215,7 +217,8 @@ __device__ __forceinline__ int32_t load_index(const Params& p, int b, int t) {
     const int tc = min(max(t, 0), max(p.topk_n - 1, 0));
     return ldg_i32(p.topk + static_cast<int64_t>(b) * p.topk_n + tc);
   }
-  const int pi = min(page_of(p, max(t, 0)), static_cast<int>(p.pt_stride) - 1);
+  const int pg = kMode == kKeysPaged64 ? max(t, 0) >> 6 : page_of(p, max(t, 0));
+  const int pi = min(pg, static_cast<int>(p.pt_stride) - 1);
   return ldg_i32(p.page_table + static_cast<int64_t>(b) * p.pt_stride + pi);
 }
 
@@ -227,12 +230,13 @@ __device__ __forceinline__ int64_t key_slot(const Params& p, int32_t idx, int t,
     if (idx < 0) return -1;  // padding entry
     slot = idx;
   } else {
-    const int pg = page_of(p, t);
+    const int pg = kMode == kKeysPaged64 ? t >> 6 : page_of(p, t);
     if (pg >= p.pt_stride || idx < 0) {
       bad = true;
       return -1;
     }
-    slot = static_cast<int64_t>(idx) * p.page_size + (t - pg * p.page_size);
+    slot = kMode == kKeysPaged64 ? static_cast<int64_t>(idx) * 64 + (t & 63)
+                                 : static_cast<int64_t>(idx) * p.page_size + (t - pg * p.page_size);
   }
   if (slot >= p.num_slots) {
     bad = true;
@@ -2162,10 +2166,13 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream, int num_sms) {
     const bool r432 = a.record_bytes == 432, topk = a.topk_indices != nullptr;
     kern = topk ? (r432 ? reinterpret_cast<const void*>(decode_tc_kernel<432, kKeysTopk>)
                         : reinterpret_cast<const void*>(decode_tc_kernel<368, kKeysTopk>))
-                : (r432 ? reinterpret_cast<const void*>(decode_tc_kernel<432, kKeysPaged>)
-                        : reinterpret_cast<const void*>(decode_tc_kernel<368, kKeysPaged>));
+                : a.page_size == 64
+                    ? (r432 ? reinterpret_cast<const void*>(decode_tc_kernel<432, kKeysPaged64>)
+                            : reinterpret_cast<const void*>(decode_tc_kernel<368, kKeysPaged64>))
+                    : (r432 ? reinterpret_cast<const void*>(decode_tc_kernel<432, kKeysPaged>)
+                            : reinterpret_cast<const void*>(decode_tc_kernel<368, kKeysPaged>));
     smem = kSmAlloc;
-    slot = topk ? (r432 ? 8 : 9) : (r432 ? 1 : 2);
+    slot = topk ? (r432 ? 8 : 9) : a.page_size == 64 ? (r432 ? 12 : 13) : (r432 ? 1 : 2);
   }
   if (const int st = smem_limit_once(kern, static_cast<int>(smem), slot)) return st;
   {
